@@ -1,0 +1,229 @@
+"""fp64 CPU oracle for paged GQA attention with sinks (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline leg, never by the library.  The arithmetic lives in
+sinkattn_oracle.c (plain C, double precision, OpenMP over query rows); this file
+only builds it with gcc, marshals numpy arrays and reshapes results.
+
+bf16 tensors are handed over as their raw 16-bit patterns, so the oracle reads
+exactly the values the GPU reads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sinkattn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsinkattn_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math: IEEE double semantics kept)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC,
+                        "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_decode.argtypes = [P, P, P, P, P, P, D, I, I, I, I, I, I64, I, P, P, P]
+        lib.oracle_decode.restype = I
+        lib.oracle_prefill.argtypes = [P, P, P, P, I, P, P, P, P, I64, I, P, D, I, I, I, I, P, P, P]
+        lib.oracle_prefill.restype = I
+        lib.oracle_append_kv.argtypes = [P, P, P, I, P, P, I, I64, I, I, I, P, P]
+        lib.oracle_append_kv.restype = I
+        lib.oracle_partial.argtypes = [P, P, P, I, D, I64, I64, P, P, P]
+        lib.oracle_partial.restype = None
+        lib.oracle_merge.argtypes = [I, P, P, P, I, D, P, P]
+        lib.oracle_merge.restype = None
+        lib.oracle_online.argtypes = [P, P, P, I, D, D, I64, I, I64, P, P]
+        lib.oracle_online.restype = None
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = I
+        _lib = lib
+    return _lib
+
+
+def _bits(t) -> np.ndarray:
+    """bf16 torch tensor or uint16 array -> contiguous uint16 numpy array of its bits."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint16
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype == torch.bfloat16, t.dtype
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(t) -> np.ndarray:
+    if t is None:
+        return None
+    a = t if isinstance(t, np.ndarray) else t.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _f32(t) -> Optional[np.ndarray]:
+    if t is None:
+        return None
+    a = t if isinstance(t, np.ndarray) else t.detach().cpu().float().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a) -> Optional[int]:
+    return None if a is None else a.ctypes.data
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def decode(q, k_pages, v_pages, block_table, seq_lens, sinks, scale: float,
+           select: Optional[np.ndarray] = None):
+    """Decode attention.  q [B,Hq,D]; pages [num_pages,Hkv,P,D]; returns (out [B,Hq,D], lse [B,Hq])
+    in float64.  select: bool [B,Hq] restricting which rows are computed (others NaN)."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    B, Hq, D = qb.shape
+    num_pages, Hkv, P, D2 = kb.shape
+    assert D == D2
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    out = np.full((B, Hq, D), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
+    rc = lib.oracle_decode(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(sl), _ptr(sk), float(scale),
+                           B, Hq, Hkv, D, P, num_pages, bt.shape[1], _ptr(sel), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode rejected its inputs ({rc})")
+    return out, lse
+
+
+def prefill(q, k, v, cu_seqlens, sinks, scale: float, k_pages=None, v_pages=None,
+            prefix_block_table=None, prefix_lens=None, select: Optional[np.ndarray] = None,
+            page_size: int = 16):
+    """Causal ragged prefill, optionally over a paged prefix.  Returns (out [T,Hq,D], lse [T,Hq])."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    T, Hq, D = qb.shape
+    Hkv = kb.shape[1]
+    cu = _i32(cu_seqlens)
+    n = cu.shape[0] - 1
+    if k_pages is not None:
+        kp, vp = _bits(k_pages), _bits(v_pages)
+        num_pages, _, page_size, _ = kp.shape
+        pbt, pl = _i32(prefix_block_table), _i32(prefix_lens)
+        maxp = pbt.shape[1]
+    else:
+        kp = vp = pbt = pl = None
+        num_pages, maxp = 0, 0
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
+    rc = lib.oracle_prefill(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), n, _ptr(kp), _ptr(vp), _ptr(pbt),
+                            _ptr(pl), num_pages, maxp, _ptr(_f32(sinks)), float(scale), Hq, Hkv, D,
+                            page_size, _ptr(sel), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_prefill rejected its inputs ({rc})")
+    return out, lse
+
+
+def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages):
+    """Scatter new rows into copies of the pages; returns (k_pages, v_pages) as uint16 arrays."""
+    lib = _load()
+    kb, vb = _bits(k), _bits(v)
+    kp, vp = _bits(k_pages).copy(), _bits(v_pages).copy()
+    num_pages, Hkv, P, D = kp.shape
+    cu, bt, sp = _i32(cu_seqlens), _i32(block_table), _i32(start_pos)
+    rc = lib.oracle_append_kv(_ptr(kb), _ptr(vb), _ptr(cu), cu.shape[0] - 1, _ptr(bt), _ptr(sp),
+                              bt.shape[1], num_pages, Hkv, D, P, _ptr(kp), _ptr(vp))
+    if rc != 0:
+        raise ValueError("oracle_append_kv rejected its inputs")
+    return kp, vp
+
+
+def partial(q, k, v, scale: float, j0: int, j1: int):
+    """Sink-free state (m, l, acc[D]) of contiguous keys [j0, j1); q [D], k/v [n, D] bf16."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    D = qb.shape[-1]
+    m, l = ctypes.c_double(), ctypes.c_double()
+    acc = np.zeros(D)
+    lib.oracle_partial(_ptr(qb), _ptr(kb), _ptr(vb), D, float(scale), j0, j1, ctypes.byref(m),
+                       ctypes.byref(l), _ptr(acc))
+    return m.value, l.value, acc
+
+
+def merge(ms, ls, accs, sink: float):
+    """Log-sum-exp merge of partial states plus the sink; returns (out [D], lse)."""
+    lib = _load()
+    m = np.ascontiguousarray(ms, dtype=np.float64)
+    l = np.ascontiguousarray(ls, dtype=np.float64)
+    a = np.ascontiguousarray(accs, dtype=np.float64)
+    S, D = a.shape
+    out = np.zeros(D)
+    lse = ctypes.c_double()
+    lib.oracle_merge(S, _ptr(m), _ptr(l), _ptr(a), D, float(sink), _ptr(out), ctypes.byref(lse))
+    return out, lse.value
+
+
+def online(q, k, v, scale: float, sink: float, block: int, split_at: int = 0):
+    """Streaming softmax seeded with the sink (see sinkattn_oracle.c); returns (out [D], lse)."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    n, D = kb.shape
+    out = np.zeros(D)
+    lse = ctypes.c_double()
+    lib.oracle_online(_ptr(qb), _ptr(kb), _ptr(vb), D, float(scale), float(sink), n, block, split_at,
+                      _ptr(out), ctypes.byref(lse))
+    return out, lse.value
+
+
+class using_library:
+    """Context manager: route this module's functions through another build of the
+    oracle (used by the tests that plant a mistake in a copy of the oracle source)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        lib = ctypes.CDLL(self.path)
+        for name in ("oracle_decode", "oracle_prefill", "oracle_append_kv", "oracle_partial",
+                     "oracle_merge", "oracle_online", "oracle_max_threads"):
+            f, g = getattr(lib, name), getattr(self._saved, name)
+            f.argtypes, f.restype = g.argtypes, g.restype
+        _lib = lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def source_path() -> str:
+    return _SRC
+
+
+def compile_source(src_text: str, out_dir: str, name: str) -> str:
+    """Compile an oracle source text (e.g. a mutated copy) into out_dir/name.so."""
+    c = os.path.join(out_dir, name + ".c")
+    so = os.path.join(out_dir, name + ".so")
+    with open(c, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", so, c, "-lm"],
+                   check=True)
+    return so

@@ -1,0 +1,366 @@
+/*
+ * fp64 CPU oracle for paged grouped-query attention with per-head attention sinks.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code, header or table with
+ * the CUDA library: it walks the block tables itself, converts bf16 to double itself
+ * and evaluates the attention in double precision straight from its definition.
+ *
+ * What is computed (sources are the extracted pages "GPT-OSS on Day 0"
+ * (perplexity.ai, section "Sink Attention"), "Hosting Qwen on Blackwell"
+ * (perplexity.ai, KV-cache layout paragraph of "Prefill") and TensorSharp
+ * "docs/models/gptoss.md" (section 3 "Forward graph" and section 4.1 "Attention")):
+ *
+ *   For query head h with KV head g = h / (Hq / Hkv), query vector q and the set J
+ *   of keys the query may see:
+ *       s_j  = scale * <q, k_j>
+ *       m    = max(sink_h, max_j s_j)
+ *       den  = exp(sink_h - m) + sum_j exp(s_j - m)
+ *       out  = sum_j exp(s_j - m) * v_j / den
+ *       lse  = m + ln(den)
+ *   i.e. softmax attention over J plus one virtual token whose logit is sink_h and
+ *   whose value is the zero vector (gptoss.md 4.1: a virtual token with zero K and V;
+ *   section 3: the sink term enters the max and the exp-sum, not the numerator).
+ *   A NULL sinks pointer means every sink is -inf (plain GQA attention).
+ *
+ *   J is: decode - every cached token [0, L_b); causal prefill - tokens 0..t of the
+ *   same sequence; chunked prefill - all P_i prefix tokens plus new tokens 0..t,
+ *   the new token t sitting at absolute position P_i + t.
+ *
+ *   KV pages are HND: [num_pages, Hkv, page_size, head_dim], the tokens of one
+ *   (page, head) contiguous (Hosting Qwen on Blackwell, KV-cache layout paragraph).
+ *   Token j of sequence b lives in page block_table[b][j / page_size], slot
+ *   j % page_size.
+ *
+ * Conventions where the pages are silent:
+ *   - the sink is a raw logit in the same (already scaled) domain as s_j;
+ *   - exp and log are natural; lse includes the sink term;
+ *   - no visible key and no sink (m = -inf): out = 0, lse = -inf.
+ *
+ * Also here, for checking the split-KV method the GPU uses (GPT-OSS on Day 0,
+ * "Sink Attention": online softmax with the running max seeded by the sink; the
+ * sink counted in one block only when the sequence is split):
+ *   oracle_partial  - unnormalised state (m, l, acc) of one key range, no sink;
+ *   oracle_merge    - log-sum-exp combination of partial states plus the sink;
+ *   oracle_online   - block-by-block online softmax seeded with m = sink, d = 1.
+ *
+ * bf16 arguments are passed as raw uint16 bit patterns; outputs are double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double sink_of(const float *sinks, int h) {
+    return sinks ? (double)sinks[h] : -INFINITY;
+}
+
+/* The definition above, for one query over n keys given by row pointers.
+ * s is caller scratch of n doubles. */
+static void attend(const uint16_t *q, int D, double scale, double sink, int64_t n,
+                   const uint16_t *const *krow, const uint16_t *const *vrow, double *s,
+                   double *out, double *lse) {
+    double m = sink;
+    for (int64_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(krow[j][d]);
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    if (m == -INFINITY) {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double den = exp(sink - m);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double w = exp(s[j] - m);
+        den += w;
+        for (int d = 0; d < D; ++d) out[d] += w * bf16_to_double(vrow[j][d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    *lse = m + log(den);
+}
+
+/* Address of token `slot` of KV head g in physical page `page` (HND layout). */
+static const uint16_t *page_row(const uint16_t *pages, int64_t page, int Hkv, int P, int D, int g,
+                                int slot) {
+    return pages + (((page * Hkv + g) * (int64_t)P + slot) * D);
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Decode: one query token per sequence.
+ *   q [B, Hq, D]; k_pages, v_pages [num_pages, Hkv, P, D]; block_table [B, max_pages];
+ *   seq_lens [B]; sinks [Hq] or NULL; out [B, Hq, D]; lse [B, Hq].
+ *   select [B * Hq] or NULL: compute only entries with select != 0 (others untouched).
+ * Returns 0, or -1 if a length or page index is out of range (nothing is read then).
+ */
+int oracle_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                  const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                  double scale, int B, int Hq, int Hkv, int D, int P, int64_t num_pages,
+                  int max_pages, const uint8_t *select, double *out, double *lse) {
+    if (Hq % Hkv) return -1;
+    const int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L < 0 || (int64_t)L > (int64_t)max_pages * P) return -1;
+        for (int j = 0; j < (L + P - 1) / P; ++j) {
+            int32_t pg = block_table[(int64_t)b * max_pages + j];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+        if (select && !select[bh]) continue;
+        const int b = (int)(bh / Hq), h = (int)(bh % Hq), g = h / G;
+        const int64_t L = seq_lens[b];
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(L + 1));
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(L + 1));
+        double *s = malloc(sizeof(double) * (size_t)(L + 1));
+        if (!krow || !vrow || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int64_t j = 0; j < L; ++j) {
+                int64_t pg = block_table[(int64_t)b * max_pages + j / P];
+                krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
+                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
+            }
+            attend(q + bh * D, D, scale, sink_of(sinks, h), L, krow, vrow, s, out + bh * D,
+                   lse + bh);
+        }
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * Prefill over packed ragged sequences, optionally after a paged prefix.
+ *   q [T, Hq, D]; k, v [T, Hkv, D] (new tokens); cu_seqlens [n + 1];
+ *   prefix: k_pages / v_pages [num_pages, Hkv, P, D], prefix_block_table [n, max_pages],
+ *   prefix_lens [n]; all NULL for a plain causal prefill.
+ *   out [T, Hq, D]; lse [T, Hq]; select [T * Hq] or NULL.
+ */
+int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   const int32_t *cu_seqlens, int n, const uint16_t *k_pages,
+                   const uint16_t *v_pages, const int32_t *prefix_block_table,
+                   const int32_t *prefix_lens, int64_t num_pages, int max_pages,
+                   const float *sinks, double scale, int Hq, int Hkv, int D, int P,
+                   const uint8_t *select, double *out, double *lse) {
+    if (Hq % Hkv) return -1;
+    const int G = Hq / Hkv;
+    const int64_t T = cu_seqlens[n];
+    int32_t *seq_of = malloc(sizeof(int32_t) * (size_t)(T + 1));
+    if (!seq_of) return -2;
+    for (int i = 0; i < n; ++i) {
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) { free(seq_of); return -1; }
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) seq_of[t] = i;
+        int Pi = prefix_lens ? prefix_lens[i] : 0;
+        if (Pi < 0 || (Pi > 0 && (int64_t)Pi > (int64_t)max_pages * P)) { free(seq_of); return -1; }
+        for (int j = 0; j < (Pi + P - 1) / P; ++j) {
+            int32_t pg = prefix_block_table[(int64_t)i * max_pages + j];
+            if (pg < 0 || pg >= num_pages) { free(seq_of); return -1; }
+        }
+    }
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t th = 0; th < T * Hq; ++th) {
+        if (select && !select[th]) continue;
+        const int64_t t = th / Hq;
+        const int h = (int)(th % Hq), g = h / G, i = seq_of[t];
+        const int64_t Pi = prefix_lens ? prefix_lens[i] : 0;
+        const int64_t tl = t - cu_seqlens[i]; /* position among the new tokens */
+        const int64_t nk = Pi + tl + 1;
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)nk);
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)nk);
+        double *s = malloc(sizeof(double) * (size_t)nk);
+        if (!krow || !vrow || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int64_t j = 0; j < Pi; ++j) {
+                int64_t pg = prefix_block_table[(int64_t)i * max_pages + j / P];
+                krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
+                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
+            }
+            for (int64_t j = 0; j <= tl; ++j) {
+                int64_t row = cu_seqlens[i] + j;
+                krow[Pi + j] = k + (row * Hkv + g) * D;
+                vrow[Pi + j] = v + (row * Hkv + g) * D;
+            }
+            attend(q + th * D, D, scale, sink_of(sinks, h), nk, krow, vrow, s, out + th * D,
+                   lse + th);
+        }
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    free(seq_of);
+    return bad ? -2 : 0;
+}
+
+/*
+ * Append new K/V rows into HND pages ("append (K, V) to KV cache" before the
+ * attention, gptoss.md section 3).  Token t of sequence i goes to position
+ * pos = start_pos[i] + (t - cu_seqlens[i]): page block_table[i][pos / P], slot pos % P.
+ * Copies bit patterns; pages are modified in place.  Returns -1 (nothing written)
+ * if any destination is out of range.
+ */
+int oracle_append_kv(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens, int n,
+                     const int32_t *block_table, const int32_t *start_pos, int max_pages,
+                     int64_t num_pages, int Hkv, int D, int P, uint16_t *k_pages,
+                     uint16_t *v_pages) {
+    for (int i = 0; i < n; ++i) {
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
+            int64_t pos = start_pos[i] + (t - cu_seqlens[i]);
+            if (pos < 0 || pos / P >= max_pages) return -1;
+            int32_t pg = block_table[(int64_t)i * max_pages + pos / P];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
+            int64_t pos = start_pos[i] + (t - cu_seqlens[i]);
+            int64_t pg = block_table[(int64_t)i * max_pages + pos / P];
+            for (int g = 0; g < Hkv; ++g) {
+                uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));
+                uint16_t *vd = (uint16_t *)page_row(v_pages, pg, Hkv, P, D, g, (int)(pos % P));
+                memcpy(kd, k + (t * Hkv + g) * D, sizeof(uint16_t) * (size_t)D);
+                memcpy(vd, v + (t * Hkv + g) * D, sizeof(uint16_t) * (size_t)D);
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Split-KV pieces, on contiguous keys k, v [n, D] and one query q [D].
+ *
+ * oracle_partial: state of keys [j0, j1) without the sink:
+ *   m = max s_j (-inf if the range is empty), l = sum exp(s_j - m),
+ *   acc = sum exp(s_j - m) v_j.
+ */
+void oracle_partial(const uint16_t *q, const uint16_t *k, const uint16_t *v, int D, double scale,
+                    int64_t j0, int64_t j1, double *m_out, double *l_out, double *acc) {
+    double m = -INFINITY;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    for (int64_t j = j0; j < j1; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(k[j * D + d]);
+        if (scale * dot > m) m = scale * dot;
+    }
+    double l = 0.0;
+    if (m > -INFINITY) {
+        for (int64_t j = j0; j < j1; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(k[j * D + d]);
+            double w = exp(scale * dot - m);
+            l += w;
+            for (int d = 0; d < D; ++d) acc[d] += w * bf16_to_double(v[j * D + d]);
+        }
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+/* oracle_merge: combine S partial states (m[s], l[s], acc[s][D]) and the sink:
+ *   M = max(sink, max_s m_s); den = exp(sink - M) + sum_s l_s exp(m_s - M);
+ *   out = sum_s acc_s exp(m_s - M) / den; lse = M + ln(den). */
+void oracle_merge(int S, const double *m, const double *l, const double *acc, int D, double sink,
+                  double *out, double *lse) {
+    double M = sink;
+    for (int s = 0; s < S; ++s)
+        if (m[s] > M) M = m[s];
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (M == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double den = exp(sink - M);
+    for (int s = 0; s < S; ++s) {
+        if (m[s] == -INFINITY) continue;
+        double w = exp(m[s] - M);
+        den += l[s] * w;
+        for (int d = 0; d < D; ++d) out[d] += acc[s * D + d] * w;
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    *lse = M + log(den);
+}
+
+/* oracle_online: the streaming form, keys visited in blocks of `block` keys.
+ * The running max starts at the sink and the running denominator at 1
+ * (= exp(sink - m) with m = sink); each block raises the max, rescales the
+ * denominator and the accumulator by exp(m_old - m_new) and adds its own terms.
+ * When split_at > 0 the keys are cut at that index into two independent
+ * streams, only the first of which is seeded with the sink; the two states are
+ * then combined with oracle_merge's rule (sink already counted, so -inf there). */
+static void online_range(const uint16_t *q, const uint16_t *k, const uint16_t *v, int D,
+                         double scale, int64_t j0, int64_t j1, int block, double m0, double d0,
+                         double *m_out, double *d_out, double *acc) {
+    double m = m0, den = d0;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    for (int64_t b0 = j0; b0 < j1; b0 += block) {
+        int64_t b1 = b0 + block < j1 ? b0 + block : j1;
+        double mb = m;
+        for (int64_t j = b0; j < b1; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(k[j * D + d]);
+            if (scale * dot > mb) mb = scale * dot;
+        }
+        if (mb == -INFINITY) continue;
+        double r = (m == -INFINITY) ? 0.0 : exp(m - mb);
+        den *= r;
+        for (int d = 0; d < D; ++d) acc[d] *= r;
+        for (int64_t j = b0; j < b1; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(k[j * D + d]);
+            double w = exp(scale * dot - mb);
+            den += w;
+            for (int d = 0; d < D; ++d) acc[d] += w * bf16_to_double(v[j * D + d]);
+        }
+        m = mb;
+    }
+    *m_out = m;
+    *d_out = den;
+}
+
+void oracle_online(const uint16_t *q, const uint16_t *k, const uint16_t *v, int D, double scale,
+                   double sink, int64_t n, int block, int64_t split_at, double *out, double *lse) {
+    double *acc = malloc(sizeof(double) * 2 * (size_t)D);
+    double m[2], den[2];
+    if (!acc) return;
+    int64_t cut = (split_at > 0 && split_at < n) ? split_at : n;
+    /* first stream: seeded with the sink (d0 = 1 means exp(sink - m0) with m0 = sink;
+     * when the sink is -inf that term is 0 and the first block's rescale zeroes it). */
+    online_range(q, k, v, D, scale, 0, cut, block, sink, sink == -INFINITY ? 0.0 : 1.0, &m[0],
+                 &den[0], acc);
+    int S = 1;
+    if (cut < n) {
+        online_range(q, k, v, D, scale, cut, n, block, -INFINITY, 0.0, &m[1], &den[1], acc + D);
+        S = 2;
+    }
+    oracle_merge(S, m, den, acc, D, -INFINITY, out, lse);
+    free(acc);
+}

@@ -1,0 +1,337 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each pin ties the oracle to something it does not share code with:
+  * torch's scaled_dot_product_attention in float64 on the CPU, for the sink-free
+    case (plain GQA softmax attention) and, through the virtual-token identity
+    (a zero key/value row whose additive mask is the sink), for the sink case;
+  * closed forms: one key, a hand-derived two-key example (tests/golden), a huge
+    sink, an empty sequence;
+  * invariances: permuting physical pages, splitting the keys and merging, the
+    online (streaming) form seeded with the sink, decode == last causal row,
+    chunked prefill == trailing rows of a full causal prefill;
+  * the append scatter read back through the block table.
+
+test_planted_mistakes_are_caught compiles copies of the oracle source with one
+plausible mistake each (dropped sink term, wrong GQA head, off-by-one slot, sign
+error, ...) and requires every copy to fail at least one pin.
+"""
+import json
+import math
+import os
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from paged_gqa_attention_head_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RTOL, ATOL = 1e-12, 1e-13
+
+
+def _bf16(a):
+    return torch.tensor(a, dtype=torch.float32).to(torch.bfloat16)
+
+
+def contiguous_kv(cache: inputs.PagedCache, b: int):
+    """Gather sequence b's K/V out of the pages: [Hkv, L, D] float64 (layout only)."""
+    L = int(cache.lens[b])
+    npg = (L + 15) // 16
+    pages = cache.block_table[b, :npg].long()
+    Hkv, D = cache.k_pages.shape[1], cache.k_pages.shape[3]
+    k = cache.k_pages[pages].permute(1, 0, 2, 3).reshape(Hkv, npg * 16, D)[:, :L]
+    v = cache.v_pages[pages].permute(1, 0, 2, 3).reshape(Hkv, npg * 16, D)[:, :L]
+    return k.double(), v.double()
+
+
+def sdpa_with_sink(q, k, v, scale, sinks, mask=None):
+    """Library reference: SDPA in float64 over keys plus one zero key/value row whose
+    additive mask column holds each head's sink.  q [Hq, M, D], k/v [Hkv, L, D];
+    mask [M, L] additive or None.  Returns (out [Hq, M, D], lse [Hq, M])."""
+    Hq, M, D = q.shape
+    Hkv, L, _ = k.shape
+    G = Hq // Hkv
+    zero = torch.zeros(Hkv, 1, D, dtype=torch.float64)
+    k1, v1 = torch.cat([k, zero], 1), torch.cat([v, zero], 1)
+    base = torch.zeros(M, L, dtype=torch.float64) if mask is None else mask
+    s = torch.full((Hq,), -math.inf, dtype=torch.float64) if sinks is None else sinks.double()
+    full = torch.cat([base.expand(Hq, M, L), s.view(Hq, 1, 1).expand(Hq, M, 1)], 2)
+    out = F.scaled_dot_product_attention(q[None], k1[None], v1[None], attn_mask=full[None],
+                                         scale=scale, enable_gqa=True)[0]
+    kr = k1.repeat_interleave(G, 0)
+    logits = scale * torch.matmul(q, kr.transpose(1, 2)) + full
+    return out, torch.logsumexp(logits, -1)
+
+
+# ----------------------------------------------------------------------------- pins
+# Each returns None on success and raises AssertionError otherwise, so the same
+# checks serve the normal tests and the planted-mistake test.
+
+def pin_decode_sdpa(o, sinks_on: bool):
+    w = inputs.make_decode([1, 17, 64, 129, 40], 5, 8, 2, 64, seed=3, sinks=sinks_on)
+    out, lse = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                        w.sinks, w.scale)
+    for b in range(5):
+        k, v = contiguous_kv(w.cache, b)
+        ro, rl = sdpa_with_sink(w.q[b].double()[:, None, :], k, v, w.scale, w.sinks)
+        np.testing.assert_allclose(out[b], ro[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_prefill_sdpa(o, with_prefix: bool):
+    new = [5, 33, 1, 20]
+    pre = [0, 17, 40, 16] if with_prefix else None
+    w = inputs.make_prefill(new, 8, 2, 64, seed=4, sinks=True, prefix_lens=pre)
+    kw = {}
+    if with_prefix:
+        kw = dict(k_pages=w.prefix.k_pages, v_pages=w.prefix.v_pages,
+                  prefix_block_table=w.prefix.block_table, prefix_lens=w.prefix.lens)
+    out, lse = o.prefill(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale, **kw)
+    cu = w.cu_seqlens.tolist()
+    for i, L in enumerate(new):
+        q = w.q[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        k = w.k[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        v = w.v[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        P = 0
+        if with_prefix:
+            pk, pv = contiguous_kv(w.prefix, i)
+            P = pk.shape[1]
+            k, v = torch.cat([pk, k], 1), torch.cat([pv, v], 1)
+        t = torch.arange(L)[:, None]
+        j = torch.arange(P + L)[None, :]
+        mask = torch.where(j <= P + t, 0.0, -math.inf).double()
+        ro, rl = sdpa_with_sink(q, k, v, w.scale, w.sinks, mask)
+        np.testing.assert_allclose(out[cu[i]:cu[i + 1]], ro.permute(1, 0, 2).numpy(), rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], rl.T.numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_single_key(o):
+    w = inputs.make_decode([1, 1, 1], 3, 4, 4, 64, seed=5, sinks=True)
+    out, lse = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                        w.sinks, w.scale)
+    for b in range(3):
+        k, v = contiguous_kv(w.cache, b)
+        for h in range(4):
+            s = w.scale * float(np.dot(w.q[b, h].double().numpy(), k[h, 0].numpy()))
+            sk = float(w.sinks[h])
+            sig = 1.0 / (1.0 + math.exp(-(s - sk)))
+            np.testing.assert_allclose(out[b, h], v[h, 0].numpy() * sig, rtol=1e-12, atol=1e-14)
+            assert abs(lse[b, h] - np.logaddexp(s, sk)) < 1e-12
+
+
+def pin_two_keys_golden(o):
+    g = json.load(open(os.path.join(GOLDEN, "two_keys.json")))
+    e = math.e
+    env = {"e": e, "log": math.log}
+    want = np.array([eval(x, {}, env) for x in g["expected_out"]])
+    want_lse = eval(g["expected_lse"], {}, env)
+    # one sequence, one head, one page; the two keys sit in slots 0 and 1
+    D = g["D"]
+    kp = torch.zeros(1, 1, 16, D, dtype=torch.bfloat16)
+    vp = torch.zeros(1, 1, 16, D, dtype=torch.bfloat16)
+    kp[0, 0, :2] = _bf16(g["k"])
+    vp[0, 0, :2] = _bf16(g["v"])
+    q = _bf16([[g["q"]]])
+    out, lse = o.decode(q, kp, vp, torch.zeros(1, 1, dtype=torch.int32), torch.tensor([2]),
+                        torch.tensor([g["sink"]]), g["scale"])
+    np.testing.assert_allclose(out[0, 0], want, rtol=1e-14)
+    assert abs(lse[0, 0] - want_lse) < 1e-14
+
+
+def pin_large_sink(o):
+    w = inputs.make_decode([1, 17, 64], 3, 4, 2, 64, seed=6, sinks=True)
+    for big in (1e4, 30.0):
+        s = torch.full((4,), big)
+        out, lse = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                            s, w.scale)
+        # |s_j| < 10 here, so every key weighs at most e^(10 - big) relative to the sink
+        bound = 64 * math.exp(10.0 - big) * 5.0
+        assert np.all(np.abs(out) <= bound)
+        assert np.all(np.abs(lse - big) <= 64 * math.exp(10.0 - big))
+        if big == 1e4:
+            assert np.all(out == 0.0) and np.all(lse == big)
+
+
+def pin_empty(o):
+    w = inputs.make_decode([0, 5], 2, 4, 2, 64, seed=7, sinks=True)
+    out, lse = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                        w.sinks, w.scale)
+    assert np.all(out[0] == 0.0)
+    np.testing.assert_array_equal(lse[0], w.sinks.double().numpy())
+    out2, lse2 = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                          None, w.scale)
+    assert np.all(out2[0] == 0.0) and np.all(np.isneginf(lse2[0]))
+
+
+def pin_page_permutation(o):
+    w = inputs.make_decode([3, 50, 100, 16], 4, 8, 2, 64, seed=8, sinks=True, poison=True)
+    c = w.cache
+    out, lse = o.decode(w.q, c.k_pages, c.v_pages, c.block_table, w.seq_lens, w.sinks, w.scale)
+    perm = torch.randperm(c.num_pages, generator=torch.Generator().manual_seed(1))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(c.num_pages)
+    kp2, vp2 = c.k_pages[perm], c.v_pages[perm]  # new page i holds old page perm[i]
+    bt2 = torch.where(c.block_table >= 0, inv[c.block_table.clamp(min=0).long()].int(), c.block_table)
+    out2, lse2 = o.decode(w.q, kp2, vp2, bt2, w.seq_lens, w.sinks, w.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_decode_vs_prefill_row(o):
+    L = 77
+    w = inputs.make_prefill([L], 8, 2, 64, seed=9, sinks=True)
+    pout, plse = o.prefill(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale)
+    for t in (0, 15, 16, 76):
+        npg = (t + 1 + 15) // 16
+        kp = torch.zeros(npg, 2, 16, 64, dtype=torch.bfloat16)
+        vp = torch.zeros(npg, 2, 16, 64, dtype=torch.bfloat16)
+        for j in range(t + 1):
+            kp[j // 16, :, j % 16] = w.k[j]
+            vp[j // 16, :, j % 16] = w.v[j]
+        bt = torch.arange(npg, dtype=torch.int32)[None]
+        dout, dlse = o.decode(w.q[t:t + 1], kp, vp, bt, torch.tensor([t + 1]), w.sinks, w.scale)
+        np.testing.assert_allclose(dout[0], pout[t], rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(dlse[0], plse[t], rtol=RTOL, atol=ATOL)
+
+
+def pin_chunked_vs_full(o):
+    new, pre = [9, 20], [35, 16]
+    w = inputs.make_prefill(new, 8, 2, 64, seed=10, sinks=True, prefix_lens=pre)
+    out, lse = o.prefill(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale, k_pages=w.prefix.k_pages,
+                         v_pages=w.prefix.v_pages, prefix_block_table=w.prefix.block_table,
+                         prefix_lens=w.prefix.lens)
+    cu = w.cu_seqlens.tolist()
+    for i in range(2):
+        pk, pv = contiguous_kv(w.prefix, i)  # [Hkv, P, D]
+        kf = torch.cat([pk.permute(1, 0, 2), w.k[cu[i]:cu[i + 1]].double()], 0).to(torch.bfloat16)
+        vf = torch.cat([pv.permute(1, 0, 2), w.v[cu[i]:cu[i + 1]].double()], 0).to(torch.bfloat16)
+        # full causal prefill over prefix + new; the prefix queries are arbitrary (zeros)
+        qf = torch.cat([torch.zeros(pre[i], 8, 64, dtype=torch.bfloat16), w.q[cu[i]:cu[i + 1]]], 0)
+        fo, fl = o.prefill(qf, kf, vf, torch.tensor([0, pre[i] + new[i]]), w.sinks, w.scale)
+        np.testing.assert_allclose(out[cu[i]:cu[i + 1]], fo[pre[i]:], rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], fl[pre[i]:], rtol=RTOL, atol=ATOL)
+
+
+def _one_query(seed=11, n=300):
+    q = inputs.normal_bf16((64,), seed, 1)
+    k = inputs.normal_bf16((n, 64), seed, 2)
+    v = inputs.normal_bf16((n, 64), seed, 3)
+    return q, k, v
+
+
+def _plain(o, q, k, v, scale, sink):
+    """The definition, through oracle_prefill's last causal row (one head, one sequence)."""
+    n = k.shape[0]
+    qq = torch.zeros(n, 1, 64, dtype=torch.bfloat16)
+    qq[-1, 0] = q
+    out, lse = o.prefill(qq, k[:, None], v[:, None], torch.tensor([0, n]),
+                         None if sink == -math.inf else torch.tensor([sink]), 0.125)
+    return out[-1, 0], lse[-1, 0]
+
+
+def pin_split_merge(o):
+    q, k, v = _one_query()
+    for sink in (0.75, -math.inf, 4.0):  # fp32-exact: sinks are stored as fp32
+        ref_out, ref_lse = _plain(o, q, k, v, 0.125, sink)
+        for cuts in ([0, 300], [0, 1, 300], [0, 128, 129, 250, 300], [0, 0, 16, 300, 300]):
+            parts = [o.partial(q, k, v, 0.125, a, b) for a, b in zip(cuts[:-1], cuts[1:])]
+            out, lse = o.merge([p[0] for p in parts], [p[1] for p in parts], [p[2] for p in parts], sink)
+            np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-14)
+            assert abs(lse - ref_lse) < 1e-12
+
+
+def pin_online(o):
+    q, k, v = _one_query(seed=12)
+    for sink in (0.3125, -math.inf, 6.0):  # fp32-exact
+        ref_out, ref_lse = _plain(o, q, k, v, 0.125, sink)
+        for block, split in ((16, 0), (128, 0), (7, 100), (300, 0), (64, 256)):
+            out, lse = o.online(q, k, v, 0.125, sink, block, split)
+            np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-14)
+            assert abs(lse - ref_lse) < 1e-12
+
+
+def pin_append_roundtrip(o):
+    a = inputs.make_append([5, 16, 33, 0, 1], [0, 7, 16, 3, 31], 2, 64, seed=13)
+    c = a.cache
+    kp, vp = o.append_kv(a.k, a.v, a.cu_seqlens, c.block_table, a.start_pos, c.k_pages, c.v_pages)
+    k_old = c.k_pages.view(torch.int16).numpy().view(np.uint16)
+    touched = np.zeros(kp.shape[:1] + kp.shape[2:3], dtype=bool)  # [page, slot]
+    cu = a.cu_seqlens.tolist()
+    kb = a.k.view(torch.int16).numpy().view(np.uint16)
+    vb = a.v.view(torch.int16).numpy().view(np.uint16)
+    for i in range(5):
+        for t in range(cu[i], cu[i + 1]):
+            pos = int(a.start_pos[i]) + t - cu[i]
+            pg = int(c.block_table[i, pos // 16])
+            assert np.array_equal(kp[pg, :, pos % 16], kb[t]) and np.array_equal(vp[pg, :, pos % 16], vb[t])
+            touched[pg, pos % 16] = True
+    keep = ~touched
+    assert np.array_equal(kp.transpose(0, 2, 1, 3)[keep], k_old.transpose(0, 2, 1, 3)[keep])
+
+
+PINS = {
+    "decode_sdpa_nosink": lambda o: pin_decode_sdpa(o, False),
+    "decode_sdpa_sink": lambda o: pin_decode_sdpa(o, True),
+    "prefill_sdpa": lambda o: pin_prefill_sdpa(o, False),
+    "chunked_sdpa": lambda o: pin_prefill_sdpa(o, True),
+    "single_key": pin_single_key,
+    "two_keys_golden": pin_two_keys_golden,
+    "large_sink": pin_large_sink,
+    "empty": pin_empty,
+    "page_permutation": pin_page_permutation,
+    "decode_vs_prefill_row": pin_decode_vs_prefill_row,
+    "chunked_vs_full": pin_chunked_vs_full,
+    "split_merge": pin_split_merge,
+    "online": pin_online,
+    "append_roundtrip": pin_append_roundtrip,
+}
+
+
+@pytest.mark.parametrize("name", sorted(PINS))
+def test_pin(oracle_mod, name):
+    PINS[name](oracle_mod)
+
+
+# (what the mistake is, text in the oracle source, its replacement)
+MUTATIONS = [
+    ("sink dropped from the denominator", "double den = exp(sink - m);", "double den = 0.0;"),
+    ("sink left out of the running max", "    double m = sink;\n    for (int64_t j = 0; j < n; ++j) {",
+     "    double m = -INFINITY;\n    for (int64_t j = 0; j < n; ++j) {"),
+    ("sink multiplied by the scale (decode)", "attend(q + bh * D, D, scale, sink_of(sinks, h)",
+     "attend(q + bh * D, D, scale, scale * sink_of(sinks, h)"),
+    ("GQA head taken modulo (decode)", "h = (int)(bh % Hq), g = h / G;", "h = (int)(bh % Hq), g = h % Hkv;"),
+    ("GQA head taken modulo (prefill)", "g = h / G, i = seq_of[t];", "g = h % Hkv, i = seq_of[t];"),
+    ("slot off by one (decode keys)",
+     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh",
+     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh"),
+    ("exponent sign flipped", "double w = exp(s[j] - m);", "double w = exp(m - s[j]);"),
+    ("lse without the max", "*lse = m + log(den);\n}", "*lse = log(den);\n}"),
+    ("keys used as values", "out[d] += w * bf16_to_double(vrow[j][d]);", "out[d] += w * bf16_to_double(krow[j][d]);"),
+    ("causal window shifted by one", "krow[Pi + j] = k + (row * Hkv + g) * D;",
+     "krow[Pi + j] = k + ((row > 0 ? row - 1 : row) * Hkv + g) * D;"),
+    ("prefix page slot off by one",
+     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            for (int64_t j = 0; j <= tl",
+     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            for (int64_t j = 0; j <= tl"),
+    ("merge ignores the partial's max", "den += l[s] * w;", "den += l[s];"),
+    ("online form skips the rescale", "den *= r;", "den *= 1.0;"),
+    ("append writes the next slot",
+     "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));",
+     "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)((pos + 1) % P));"),
+]
+
+
+def test_planted_mistakes_are_caught(oracle_mod):
+    src = open(oracle_mod.source_path()).read()
+    with tempfile.TemporaryDirectory() as tmp:
+        for idx, (what, old, new) in enumerate(MUTATIONS):
+            assert src.count(old) == 1, f"mutation anchor not unique: {what}"
+            so = oracle_mod.compile_source(src.replace(old, new), tmp, f"mutant{idx}")
+            failed = []
+            with oracle_mod.using_library(so):
+                for name, pin in PINS.items():
+                    try:
+                        pin(oracle_mod)
+                    except (AssertionError, ValueError, FloatingPointError):
+                        failed.append(name)
+            assert failed, f"no pin caught the planted mistake: {what}"
