@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of paged GQA attention with sinks on GB300.
+
+One JSON line on stdout (rank 0).  The headline workload is the gpt-oss-shape
+decode batch (64 sequences, 64 query / 8 KV heads, head_dim 64, KV lengths
+uniform in [512, 8192], page size 16, shuffled pages): a step is one decode
+pass - the split-KV kernel and the LSE merge - over that batch, and `value` is
+KV bytes read per second (every cached K and V byte once).  The prefill side
+of the metric (causal ragged prefill of 4 sequences {4096, 2048, 1024, 512}, the
+K/V append, and chunked prefill of 8 x 512 new tokens over 16384-token paged
+prefixes) and the other decode shapes are measured in the same run and reported
+under "rows".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(attention has no exchange step); value = units of all ranks / max rank time.
+`--impl reference` times the fp64 CPU oracle on the same metric instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sink-attn decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of BF16 peak)"
+HEADLINE = "gptoss_decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def file_sha(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        h.update(open(os.path.join(ROOT, r), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, sources: list[str]):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_sha") != file_sha(*sources):
+        return None
+    return d.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is busy."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 - 0.15 <= ts <= t1 + 0.15):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_identifier(torch, dev) -> str:
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ----------------------------------------------------------------------------- ours
+def time_loop(torch, fn, steps: int, stream, marks=None):
+    """Run fn() `steps` times between CUDA events on `stream`; returns total ms.
+    `marks`, if given, is a list that fn appends (start, end) event pairs to."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    from paged_gqa_attention_head_gb300 import build as libbuild, inputs, sinkattn as sa
+
+    libbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    pk, peak_src = peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- headline: decode of the gpt-oss-shape batch
+    w = inputs.make_workload(HEADLINE, seed=0)
+    c = w.cache
+    d = dict(q=w.q.to(dev), kp=c.k_pages.to(dev), vp=c.v_pages.to(dev),
+             bt=c.block_table.to(dev), sl=c.lens.to(dev), sk=w.sinks.to(dev))
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+    kv_bytes = w.kv_bytes()
+    phase_events = []
+
+    def step():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        _, _, ws, desc = sa.decode_splitkv(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"],
+                                           w.scale, out=out, lse=lse)
+        e1.record(stream)
+        sa.decode_merge(d["sl"], d["sk"], out, lse, desc, ws)
+        phase_events.append((e0, e1))
+
+    gid = gpu_identifier(torch, dev)
+    sampler = ClockSampler(gid)
+    t_load0 = time.time()
+    # warm-up: W steps, then keep the GPU busy ~1 s so the clock samples reflect load
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t_end = time.time() + 1.0
+    nwarm = max(3, args.warmup)
+    while time.time() < t_end:
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
+        nwarm += 50
+    phase_events.clear()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = time_loop(torch, step, args.steps, stream)
+    if dist:
+        dist.barrier()
+    t_load1 = time.time()
+    clocks = sampler.stop(t_load0, t_load1)
+    split_ms = sum(a.elapsed_time(b) for a, b in phase_events) / len(phase_events)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    ach = kv_bytes / (split_ms * 1e-3) / 1e9
+    assert sa.get_status(sa.workspace(0, dev)) == 0, "device status reported a problem"
+
+    # ---- e2e: the same decode through the C ABI with host buffers copied every step
+    pinned = {k: d[k].cpu().pin_memory() for k in ("q", "bt", "sl", "sk")}
+    dev_in = {k: torch.empty_like(d[k]) for k in pinned}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        for k in pinned:
+            dev_in[k].copy_(pinned[k], non_blocking=True)
+        sa.decode(dev_in["q"], d["kp"], d["vp"], dev_in["bt"], dev_in["sl"], dev_in["sk"], w.scale,
+                  out=out, lse=lse)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_ms = time_loop(torch, e2e_step, args.steps, stream) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = host_out.numel() * 2 + host_lse.numel() * 4
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": nwarm, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": "gpt-oss-shape decode: B=64, 64 q / 8 KV heads, head_dim 64, "
+                               "page 16, KV len ~ U[512, 8192], fp32 sinks",
+                   "global_batch": 64 * world, "kv_tokens": int(c.lens.sum()), "kv_bytes": kv_bytes,
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 "
+                   f"({kv_bytes / 1e6:.0f} MB of KV per step vs 129 MB L2)"},
+        "tokens_per_s": round(world * 64 / (ms_step * 1e-3), 1),
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "q, block table, lengths and sinks copied from pinned host memory and "
+                        "out + lse read back every step; the KV cache is resident state"},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": round(ach, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": traffic_for("decode_splitkv_kernel",
+                                            ["paged_gqa_attention_head_gb300/csrc/decode.cu"]),
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "kernel_ms": round(split_ms, 5)},
+        "clocks": clocks,
+    }
+
+    # ---- the other rows, each timed on its own (not part of the headline step)
+    if not args.no_rows:
+        result["rows"] = measure_rows(torch, sa, inputs, dev, stream, pk, peak_src)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
+    rows = {}
+    reps = 20
+
+    def decode_row(name):
+        w = inputs.make_workload(name, seed=0)
+        c = w.cache
+        args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
+                c.lens.to(dev), None if w.sinks is None else w.sinks.to(dev), w.scale)
+        out = torch.empty_like(args[0])
+        lse = torch.empty(args[0].shape[:2], dtype=torch.float32, device=dev)
+        f = lambda: sa.decode(*args, out=out, lse=lse)  # noqa: E731
+        for _ in range(3):
+            f()
+        ms = time_loop(torch, f, reps, stream) / reps
+        gbs = w.kv_bytes() / (ms * 1e-3) / 1e9
+        r = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+             "kv_bytes": w.kv_bytes(), "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1)}
+        del args, out, lse, w
+        torch.cuda.empty_cache()
+        return r
+
+    for name in ("qwen3_decode", "longctx_decode"):
+        rows[name] = decode_row(name)
+
+    # append of the prefill workload's K/V into HND pages
+    a = inputs.make_append([4096, 2048, 1024, 512], [0, 0, 0, 0], 8, 64, seed=0)
+    ac = a.cache
+    aargs = (a.k.to(dev), a.v.to(dev), a.cu_seqlens.to(dev), ac.block_table.to(dev),
+             a.start_pos.to(dev), ac.k_pages.to(dev), ac.v_pages.to(dev))
+    f = lambda: sa.append_kv(*aargs)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = time_loop(torch, f, reps, stream) / reps
+    moved = 2 * 2 * a.k.numel() * 2  # read k, v and write them
+    rows["gptoss_append"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
+                             "bytes": moved}
+
+    for name in ("gptoss_prefill", "longctx_chunked"):
+        p = inputs.make_workload(name, seed=0)
+        kw = {}
+        if p.prefix is not None:
+            kw = dict(k_pages=p.prefix.k_pages.to(dev), v_pages=p.prefix.v_pages.to(dev),
+                      prefix_block_table=p.prefix.block_table.to(dev),
+                      prefix_lens=p.prefix.lens.to(dev))
+        pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+        try:
+            sa.prefill(*pargs, **kw)
+        except sa.SinkAttnError as e:
+            rows[name] = {"unavailable": str(e)}
+            continue
+        f = lambda: sa.prefill(*pargs, **kw)  # noqa: E731
+        for _ in range(3):
+            f()
+        ms = time_loop(torch, f, reps, stream) / reps
+        tf = p.flops() / (ms * 1e-3) / 1e12
+        rows[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
+                      "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": p.flops(),
+                      "peak_source": f"{peak_src} bf16_tflops"}
+    return rows
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The fp64 oracle on the host cores over the same decode batch, repeated
+    until about `budget_s` seconds of work."""
+    import oracle
+    c = w.cache
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
+    one = time.perf_counter() - t0
+    reps = max(1, min(500, int(budget_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
+    el = time.perf_counter() - t0
+    return {"value": round(reps * w.kv_bytes() / el / 1e9, 3), "unit": "GB/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"the whole decode batch (64 sequences x 64 heads) x {reps} repetitions, "
+                      f"{el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference
+def run_reference(args):
+    import oracle
+    from paged_gqa_attention_head_gb300 import inputs
+
+    oracle.build()
+    w = inputs.make_workload(HEADLINE, seed=0)
+    c = w.cache
+    B = w.q.shape[0]
+    t0 = time.perf_counter()
+    oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
+    one = time.perf_counter() - t0
+    # each step: a bounded sample of the batch (whole sequences x all heads) of about 2 s
+    nseq = max(1, min(B, int(B * 2.0 / max(one, 1e-3))))
+    sel = __import__("numpy").zeros((B, w.q.shape[1]), dtype=bool)
+    sel[:nseq] = True
+    sample_bytes = int(c.lens[:nseq].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    for _ in range(args.warmup):
+        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, select=sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, select=sel)
+    el = time.perf_counter() - t0
+    value = args.steps * sample_bytes / el / 1e9
+    sample = f"first {nseq} of 64 sequences x all 64 heads per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gpt-oss-shape decode: B=64, 64 q / 8 KV heads, head_dim 64, "
+                               "page 16, KV len ~ U[512, 8192], fp32 sinks", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

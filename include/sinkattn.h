@@ -1,0 +1,207 @@
+/*
+ * sinkattn.h - C ABI of libsinkattn: paged grouped-query attention with per-head
+ * attention sinks on GB300 (sm_103a).
+ *
+ * What is computed.  For query head h, its KV head g = h / (Hq / Hkv), a query
+ * vector q and the keys J the query may see:
+ *     s_j = scale * <q, k_j>
+ *     m   = max(sink_h, max_j s_j)
+ *     out = sum_j e^(s_j - m) v_j / (e^(sink_h - m) + sum_j e^(s_j - m))
+ *     lse = m + ln(e^(sink_h - m) + sum_j e^(s_j - m))        (natural log)
+ * The sink is a per-head learned logit that takes part in the softmax as a
+ * virtual token with zero key and zero value ("GPT-OSS on Day 0", section "Sink
+ * Attention"; TensorSharp docs/models/gptoss.md, section 3 "Forward graph" and
+ * section 4.1 "Attention").  The sink is used as given (it is not multiplied by
+ * `scale`).  sinks == NULL means every sink is -inf: plain GQA attention.
+ * A query that sees no key and has no sink gets out = 0 and lse = -inf.
+ *
+ * KV cache layout (HND, "Hosting Qwen on Blackwell", KV-cache paragraph of the
+ * "Prefill" part: heads leading, the tokens of a page contiguous):
+ *     k_pages, v_pages: bf16 [num_pages, num_kv_heads, page_size, head_dim]
+ *     token j of sequence b is slot j % page_size of page block_table[b][j / page_size]
+ *     block_table: int32 [num_seqs, max_pages_per_seq], row-major
+ *
+ * Supported: bf16 data, fp32 sinks, head_dim 64 or 128, page_size 16,
+ * num_qo_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers into memory the caller owns; the
+ *     library never allocates or frees inside a compute call.  Scratch space
+ *     comes from a caller-provided device workspace whose size is queried first.
+ *     Pointers must be 16-byte aligned; tensors are dense and row-major.
+ *   - Work is enqueued on `stream` (a cudaStream_t); calls return after enqueueing.
+ *     Launch shapes depend only on host arguments and the device, never on device
+ *     data, so the calls can be recorded into CUDA graphs.
+ *   - The return value is a sinkattn_error code.  Invalid host arguments are
+ *     rejected before anything is enqueued.  Nothing is printed; nothing traps.
+ *   - Problems that only the device can see (a block-table entry outside
+ *     [0, num_pages), a length beyond the block table, a malformed cu_seqlens)
+ *     make the kernels skip the offending access and set a bit in a status word
+ *     that lives in the workspace; read it with sinkattn_get_status.  Outputs of
+ *     the affected rows are then unspecified (but no memory outside the given
+ *     buffers is touched).
+ */
+#ifndef SINKATTN_H
+#define SINKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *sinkattn_stream_t;
+
+typedef enum sinkattn_error {
+    SINKATTN_OK = 0,
+    SINKATTN_ERR_INVALID_ARG = 1,         /* a NULL/misaligned pointer or inconsistent size */
+    SINKATTN_ERR_UNSUPPORTED = 2,         /* valid but not implemented (dtype, head_dim, group) */
+    SINKATTN_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below the size query's answer */
+    SINKATTN_ERR_CUDA = 4                 /* a CUDA runtime call failed */
+} sinkattn_error;
+
+/* Bits of the device status word (sinkattn_get_status). */
+#define SINKATTN_STATUS_BAD_PAGE 0x1u       /* block-table entry outside [0, num_pages) */
+#define SINKATTN_STATUS_BAD_LENGTH 0x2u     /* a length < 0 or > max_pages_per_seq * page_size */
+#define SINKATTN_STATUS_BAD_CU_SEQLENS 0x4u /* cu_seqlens not non-decreasing from 0 to total */
+#define SINKATTN_STATUS_WAIT_TIMEOUT 0x8u   /* a pipeline wait hit its iteration limit */
+
+/* Shapes of a paged KV cache and of the heads that read it. */
+typedef struct sinkattn_paged_desc {
+    int32_t num_seqs;          /* B: sequences (decode) or requests (prefill) */
+    int32_t num_qo_heads;      /* Hq */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;          /* D: 64 or 128 */
+    int32_t page_size;         /* P: 16 */
+    int32_t num_pages;         /* pages in k_pages / v_pages (may be 0 for a prefill without prefix) */
+    int32_t max_pages_per_seq; /* columns of the block table */
+} sinkattn_paged_desc;
+
+/* Human-readable name of an error code (static string). */
+const char *sinkattn_error_string(int code);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+int sinkattn_version(void);
+
+/* ------------------------------------------------------------------ decode --
+ * Split-KV decode ("GPT-OSS on Day 0", section "Sink Attention": the attention is
+ * parallelised over heads and along the KV length, the partial softmax states are
+ * combined, and the sink enters exactly once).  One query token per sequence; it
+ * attends all seq_lens[b] cached tokens (the current token's K/V already appended).
+ *
+ * Workspace: query its size for a descriptor, then pass at least that many bytes,
+ * 256-byte aligned.  The first 256 bytes are a header holding the status word; it
+ * must be zero before the first call (sinkattn_workspace_init, or a memset).  The
+ * size depends on the descriptor and on the number of SMs of the CURRENT device.
+ * Calls that share one workspace must be ordered on the GPU (same stream, or
+ * synchronised); overlapping calls on one workspace race.
+ */
+int sinkattn_decode_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes);
+
+/* Zero the workspace header (status word) on `stream`. */
+int sinkattn_workspace_init(void *workspace, size_t ws_bytes, sinkattn_stream_t stream);
+
+/*
+ * q:           bf16 [B, Hq, D]
+ * k_pages/v_pages: bf16 [num_pages, Hkv, 16, D]   (HND, see top of file)
+ * block_table: int32 [B, max_pages_per_seq]; only the first ceil(seq_lens[b]/16)
+ *              entries of row b are read
+ * seq_lens:    int32 [B], each in [0, max_pages_per_seq * 16]
+ * sinks:       fp32 [Hq] or NULL (= -inf, no sink)
+ * scale:       multiplies q.k (typically 1/sqrt(D))
+ * out:         bf16 [B, Hq, D]                       (written)
+ * lse:         fp32 [B, Hq] natural-log normaliser including the sink, or NULL
+ * workspace:   device scratch of ws_bytes (>= sinkattn_decode_workspace_size)
+ *
+ * Equivalent to sinkattn_decode_splitkv followed by sinkattn_decode_merge.
+ */
+int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
+                    const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                    float scale, void *out, float *lse, const sinkattn_paged_desc *desc,
+                    void *workspace, size_t ws_bytes, sinkattn_stream_t stream);
+
+/* First kernel of sinkattn_decode: every page of every (sequence, KV head) is read
+ * once; the work is cut into equal page ranges, one per warp of a persistent grid.
+ * A (sequence, KV head) read entirely by one warp gets its final out/lse here (sink
+ * folded in); the others leave sink-free partial states (m, l, acc) in the workspace.
+ * Same arguments as sinkattn_decode. */
+int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const float *sinks, float scale, void *out, float *lse,
+                            const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                            sinkattn_stream_t stream);
+
+/* Second kernel of sinkattn_decode: log-sum-exp merge of the partial states of each
+ * split (sequence, KV head) with the sink term added once:
+ *     M = max(sink, max_s m_s);  den = e^(sink - M) + sum_s l_s e^(m_s - M)
+ *     out = sum_s acc_s e^(m_s - M) / den;  lse = M + ln den
+ * Must follow sinkattn_decode_splitkv on the same workspace with the same
+ * seq_lens, sinks and descriptor.  Also writes out = 0, lse = sink for empty
+ * sequences. */
+int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out, float *lse,
+                          const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                          sinkattn_stream_t stream);
+
+/* ----------------------------------------------------------------- prefill --
+ * Causal prefill over packed ragged sequences ("Fast embeddings on GPUs", section
+ * on kernels: ragged inputs without padding, paged prefill), optionally after a
+ * paged prefix (chunked prefill).  Query t of request i (0 <= t < new_len_i) sits at
+ * absolute position prefix_len_i + t and attends every prefix token plus new tokens
+ * 0..t of the same request (causal mask of gptoss.md section 3, aligned to the end).
+ * QK^T and PV run on the tcgen05 tensor cores with TMEM accumulators; the online
+ * softmax's running max and denominator start from the sink.
+ *
+ * q:          bf16 [T, Hq, D]   (T = total_tokens = cu_seqlens[num_seqs])
+ * k, v:       bf16 [T, Hkv, D]  (the new tokens' keys and values)
+ * cu_seqlens: int32 [num_seqs + 1], cu_seqlens[0] = 0, non-decreasing
+ * k_pages, v_pages, prefix_block_table [num_seqs, max_pages_per_seq], prefix_lens
+ *             [num_seqs]: the paged prefix; all four NULL for a plain causal prefill
+ * sinks, scale, lse: as for decode, with lse [T, Hq]
+ * out:        bf16 [T, Hq, D]
+ * desc:       num_seqs, heads, head_dim, page_size; num_pages and max_pages_per_seq
+ *             describe the prefix pages (ignored without a prefix)
+ * workspace:  at least sinkattn_prefill_workspace_size bytes (status header only)
+ */
+int sinkattn_prefill_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes);
+
+int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                     int32_t total_tokens, const void *k_pages, const void *v_pages,
+                     const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                     const float *sinks, float scale, void *out, float *lse,
+                     const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                     sinkattn_stream_t stream);
+
+/* ------------------------------------------------------------------ append --
+ * Write new K/V rows into the paged cache ("append (K, V) to KV cache" before the
+ * attention, gptoss.md section 3).  Token t of request i (cu_seqlens[i] <= t <
+ * cu_seqlens[i+1]) goes to position pos = start_pos[i] + t - cu_seqlens[i], i.e. slot
+ * pos % 16 of page block_table[i][pos / 16], for every KV head.  A bit-exact copy.
+ *
+ * k, v:        bf16 [T, Hkv, D]
+ * cu_seqlens:  int32 [num_seqs + 1]
+ * block_table: int32 [num_seqs, max_pages_per_seq]
+ * start_pos:   int32 [num_seqs], tokens already in each sequence's pages
+ * k_pages, v_pages: bf16 [num_pages, Hkv, 16, D], updated in place
+ * workspace:   optional (may be NULL): if given (>= 256 bytes), rows whose
+ *              destination is out of range set status bits there; they are skipped
+ *              either way.
+ */
+int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,
+                       int32_t total_tokens, const int32_t *block_table,
+                       const int32_t *start_pos, void *k_pages, void *v_pages,
+                       const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                       sinkattn_stream_t stream);
+
+/* ------------------------------------------------------------------ status --
+ * Read the status word of a workspace and clear it (synchronous: waits for the work
+ * already enqueued on `stream`).  *status_out gets an OR of SINKATTN_STATUS_* bits
+ * accumulated since the last read; 0 means no device-side problem was seen. */
+int sinkattn_get_status(void *workspace, uint32_t *status_out, sinkattn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H */

@@ -12,6 +12,6 @@ __all__ = ["inputs", "sinkattn"]
 
 def __getattr__(name):
     if name == "sinkattn":
-        from . import sinkattn
-        return sinkattn
+        import importlib
+        return importlib.import_module(__name__ + ".sinkattn")
     raise AttributeError(name)

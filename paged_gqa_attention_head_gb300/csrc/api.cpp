@@ -1,0 +1,359 @@
+// C ABI of libsinkattn (declared in include/sinkattn.h): argument checks,
+// workspace layout, TMA tensor-map encoding and kernel launches.  No device
+// memory is allocated here; scratch lives in the caller's workspace.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/sinkattn.h"
+#include "internal.h"
+
+using namespace sinkattn;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first), 128-byte swizzled boxes.
+int encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+               const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return SINKATTN_ERR_CUDA;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+                     dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SINKATTN_OK : SINKATTN_ERR_INVALID_ARG;
+}
+
+// Pages [num_pages, Hkv, 16, D]: dims {D, 16, Hkv, num_pages}; a box is one
+// (page, head) row block of 16 tokens x 64 elements.
+int encode_pages_map(CUtensorMap *m, const void *pages, int num_pages, int Hkv, int D) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2,
+                                   (cuuint64_t)Hkv * kPageSize * D * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, 1, 1};
+    return encode_map(m, pages, 4, dims, strides, box);
+}
+
+// Rows [T, H, D]: dims {D, H, T}; a box is `rows` consecutive tokens of one head.
+int encode_rows_map(CUtensorMap *m, const void *base, int T, int H, int D, int rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    return encode_map(m, base, 3, dims, strides, box);
+}
+
+int check_heads(const sinkattn_paged_desc *d) {
+    if (!d) return SINKATTN_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
+        d->num_pages < 0 || d->max_pages_per_seq < 0)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (d->num_qo_heads % d->num_kv_heads) return SINKATTN_ERR_INVALID_ARG;
+    const int G = d->num_qo_heads / d->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return SINKATTN_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return SINKATTN_ERR_UNSUPPORTED;
+    if (d->page_size != kPageSize) return SINKATTN_ERR_UNSUPPORTED;
+    return SINKATTN_OK;
+}
+
+int check_decode_desc(const sinkattn_paged_desc *d) {
+    int rc = check_heads(d);
+    if (rc) return rc;
+    if (d->num_pages < 1 || d->max_pages_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
+    // page-unit offsets are 32-bit inside the kernels
+    if ((int64_t)d->num_seqs * d->max_pages_per_seq * d->num_kv_heads >= (int64_t)INT32_MAX)
+        return SINKATTN_ERR_UNSUPPORTED;
+    if ((int64_t)d->num_seqs * d->num_kv_heads >= (int64_t)INT32_MAX / 2) return SINKATTN_ERR_UNSUPPORTED;
+    return SINKATTN_OK;
+}
+
+struct DecodeLayout {
+    size_t prefix, plan, ml, acc, total;
+    int ctas, warps_per_cta, smem, total_warps;
+};
+
+int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    if (decode_launch_shape(d->head_dim, d->num_seqs, device, &L->ctas, &L->warps_per_cta,
+                            &L->smem) != cudaSuccess)
+        return SINKATTN_ERR_CUDA;
+    L->total_warps = L->ctas * L->warps_per_cta;
+    const int G = d->num_qo_heads / d->num_kv_heads;
+    const size_t slots = (size_t)L->total_warps + (size_t)d->num_seqs * d->num_kv_heads;
+    size_t off = kStatusBytes;
+    L->prefix = off;
+    off += align_up(((size_t)d->num_seqs + 1) * 4);
+    L->plan = off;
+    off += kAlign;
+    L->ml = off;
+    off += align_up(slots * G * 2 * sizeof(float));
+    L->acc = off;
+    off += slots * G * d->head_dim * sizeof(float);
+    L->total = align_up(off);
+    return SINKATTN_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA; }
+
+struct DecodePrep {
+    DecodeArgs args;
+    DecodeLayout layout;
+};
+
+int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq_lens,
+                   const float *sinks, float scale, void *out, float *lse,
+                   const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                   DecodePrep *P) {
+    int rc = check_decode_desc(desc);
+    if (rc) return rc;
+    if (!q || !block_table || !seq_lens || !out || !workspace) return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, kAlign) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (sinks && !aligned(sinks, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    rc = decode_layout(desc, &P->layout);
+    if (rc) return rc;
+    if (ws_bytes < P->layout.total) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+    DecodeArgs &a = P->args;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.q = q;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.sinks = sinks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.out = out;
+    a.lse = lse;
+    a.B = desc->num_seqs;
+    a.Hq = desc->num_qo_heads;
+    a.Hkv = desc->num_kv_heads;
+    a.G = desc->num_qo_heads / desc->num_kv_heads;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_seq;
+    a.total_warps = P->layout.total_warps;
+    a.status = reinterpret_cast<uint32_t *>(ws);
+    a.ws_prefix = reinterpret_cast<int32_t *>(ws + P->layout.prefix);
+    a.ws_plan = reinterpret_cast<int64_t *>(ws + P->layout.plan);
+    a.part_ml = reinterpret_cast<float *>(ws + P->layout.ml);
+    a.part_acc = reinterpret_cast<float *>(ws + P->layout.acc);
+    return SINKATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sinkattn_error_string(int code) {
+    switch (code) {
+        case SINKATTN_OK: return "ok";
+        case SINKATTN_ERR_INVALID_ARG: return "invalid argument";
+        case SINKATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SINKATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case SINKATTN_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown error";
+    }
+}
+
+int sinkattn_version(void) { return 10000; }
+
+int sinkattn_decode_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes) {
+    if (!bytes) return SINKATTN_ERR_INVALID_ARG;
+    int rc = check_decode_desc(desc);
+    if (rc) return rc;
+    DecodeLayout L;
+    rc = decode_layout(desc, &L);
+    if (rc) return rc;
+    *bytes = L.total;
+    return SINKATTN_OK;
+}
+
+int sinkattn_workspace_init(void *workspace, size_t ws_bytes, sinkattn_stream_t stream) {
+    if (!workspace || ws_bytes < kStatusBytes || !aligned(workspace, kAlign))
+        return SINKATTN_ERR_INVALID_ARG;
+    return cuda_rc(cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream));
+}
+
+int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const float *sinks, float scale, void *out, float *lse,
+                            const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                            sinkattn_stream_t stream) {
+    DecodePrep P;
+    int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
+                            ws_bytes, &P);
+    if (rc) return rc;
+    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0) return SINKATTN_OK;
+    CUtensorMap kmap, vmap;
+    rc = encode_pages_map(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    rc = encode_pages_map(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    return cuda_rc(launch_decode_splitkv(desc->head_dim, P.args, kmap, vmap, P.layout.ctas,
+                                         P.layout.smem, (cudaStream_t)stream));
+}
+
+int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out, float *lse,
+                          const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                          sinkattn_stream_t stream) {
+    DecodePrep P;
+    // the merge reads the plan written by the split-KV kernel; q and the block
+    // table are not used, so stand-in non-null pointers pass the checks
+    int rc = prepare_decode(out, seq_lens, seq_lens, sinks, 1.f, out, lse, desc, workspace,
+                            ws_bytes, &P);
+    if (rc) return rc;
+    if (desc->num_seqs == 0) return SINKATTN_OK;
+    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, (cudaStream_t)stream));
+}
+
+int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
+                    const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
+                    float scale, void *out, float *lse, const sinkattn_paged_desc *desc,
+                    void *workspace, size_t ws_bytes, sinkattn_stream_t stream) {
+    int rc = sinkattn_decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out,
+                                     lse, desc, workspace, ws_bytes, stream);
+    if (rc) return rc;
+    return sinkattn_decode_merge(seq_lens, sinks, out, lse, desc, workspace, ws_bytes, stream);
+}
+
+int sinkattn_prefill_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes) {
+    if (!bytes) return SINKATTN_ERR_INVALID_ARG;
+    int rc = check_heads(desc);
+    if (rc) return rc;
+    *bytes = kStatusBytes;
+    return SINKATTN_OK;
+}
+
+int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                     int32_t total_tokens, const void *k_pages, const void *v_pages,
+                     const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                     const float *sinks, float scale, void *out, float *lse,
+                     const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                     sinkattn_stream_t stream) {
+    int rc = check_heads(desc);
+    if (rc) return rc;
+    if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !cu_seqlens || !out || !workspace) return SINKATTN_ERR_INVALID_ARG;
+    if (ws_bytes < kStatusBytes) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        !aligned(workspace, kAlign) || !aligned(cu_seqlens, 4) || (sinks && !aligned(sinks, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    const bool has_prefix = k_pages || v_pages || prefix_block_table || prefix_lens;
+    if (has_prefix) {
+        if (!k_pages || !v_pages || !prefix_block_table || !prefix_lens) return SINKATTN_ERR_INVALID_ARG;
+        if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(prefix_block_table, 4) ||
+            !aligned(prefix_lens, 4))
+            return SINKATTN_ERR_INVALID_ARG;
+        if (desc->num_pages < 1 || desc->max_pages_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
+    }
+    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
+    const int D = desc->head_dim, Hq = desc->num_qo_heads, Hkv = desc->num_kv_heads;
+    CUtensorMap qmap, kmap, vmap, kpmap, vpmap;
+    if ((rc = encode_rows_map(&qmap, q, total_tokens, Hq, D, 128))) return rc;
+    if ((rc = encode_rows_map(&kmap, k, total_tokens, Hkv, D, 128))) return rc;
+    if ((rc = encode_rows_map(&vmap, v, total_tokens, Hkv, D, 128))) return rc;
+    if (has_prefix) {
+        if ((rc = encode_pages_map(&kpmap, k_pages, desc->num_pages, Hkv, D))) return rc;
+        if ((rc = encode_pages_map(&vpmap, v_pages, desc->num_pages, Hkv, D))) return rc;
+    } else {
+        kpmap = kmap;  // unused
+        vpmap = vmap;
+    }
+    PrefillArgs a;
+    a.cu_seqlens = cu_seqlens;
+    a.prefix_block_table = has_prefix ? prefix_block_table : nullptr;
+    a.prefix_lens = has_prefix ? prefix_lens : nullptr;
+    a.k_pages = has_prefix ? k_pages : nullptr;
+    a.v_pages = has_prefix ? v_pages : nullptr;
+    a.sinks = sinks;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.out = out;
+    a.lse = lse;
+    a.T = total_tokens;
+    a.n = desc->num_seqs;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.D = D;
+    a.num_pages = has_prefix ? desc->num_pages : 0;
+    a.max_pages = has_prefix ? desc->max_pages_per_seq : 0;
+    a.status = static_cast<uint32_t *>(workspace);
+    cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
+    if (e == cudaErrorNotSupported) return SINKATTN_ERR_UNSUPPORTED;
+    return cuda_rc(e);
+}
+
+int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,
+                       int32_t total_tokens, const int32_t *block_table,
+                       const int32_t *start_pos, void *k_pages, void *v_pages,
+                       const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                       sinkattn_stream_t stream) {
+    int rc = check_heads(desc);
+    if (rc) return rc;
+    if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (!k || !v || !cu_seqlens || !block_table || !start_pos || !k_pages || !v_pages)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(cu_seqlens, 4) || !aligned(block_table, 4) || !aligned(start_pos, 4))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (workspace && (ws_bytes < kStatusBytes || !aligned(workspace, kAlign)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_pages < 1 || desc->max_pages_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
+    AppendArgs a;
+    a.k = k;
+    a.v = v;
+    a.cu_seqlens = cu_seqlens;
+    a.block_table = block_table;
+    a.start_pos = start_pos;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.T = total_tokens;
+    a.n = desc->num_seqs;
+    a.Hkv = desc->num_kv_heads;
+    a.D = desc->head_dim;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_seq;
+    a.status = static_cast<uint32_t *>(workspace);
+    return cuda_rc(launch_append_kv(a, (cudaStream_t)stream));
+}
+
+int sinkattn_get_status(void *workspace, uint32_t *status_out, sinkattn_stream_t stream) {
+    if (!workspace || !status_out || !aligned(workspace, kAlign)) return SINKATTN_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SINKATTN_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    *status_out = v;
+    return SINKATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,529 @@
+// Split-KV paged decode with per-head sinks, and the log-sum-exp merge.
+//
+// Method ("GPT-OSS on Day 0", section "Sink Attention"): the attention of one
+// query token is parallelised over heads and along the KV length; each piece
+// keeps an online-softmax state (running max m, running sum l, unnormalised
+// output acc) and the pieces are combined afterwards; the sink logit is counted
+// exactly once.  KV pages are HND ("Hosting Qwen on Blackwell", KV-cache
+// layout): one (page, KV head) is 16 contiguous rows of head_dim bf16.
+//
+// GB300 design.  Decode reads every KV byte once and does ~8-16 flop per byte,
+// so it is bound by HBM bandwidth.  The work is the list of all (sequence,
+// KV head, page) units in order; a persistent grid cuts that list into equal
+// contiguous ranges, one per warp, so every warp moves the same number of bytes
+// whatever the length mix.  Each warp streams its pages through a private ring
+// of shared-memory stages filled by TMA (4-D tensor maps over the page pool,
+// 128-byte swizzle), and computes all G query heads of the KV head with
+// m16n8k16 tensor-core MMAs (heads on the M axis, 16 tokens of a page on N).
+// A (sequence, KV head) that one warp covers entirely is finished in place with
+// the sink folded in; otherwise the warp leaves a sink-free partial state and
+// the merge kernel combines the pieces and adds the sink.
+#include <float.h>
+
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sinkattn {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMinUnitsPerWarp = 16;  // pages per warp at least (keeps partials few)
+
+template <int D>
+struct DecodeCfg {
+    static constexpr int kWarps = 4;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kStages = D == 64 ? 6 : 3;
+    static constexpr int kHalves = D / 64;               // 128-byte column blocks per row
+    static constexpr int kPageBytes = kPageSize * D * 2;  // one (page, head) of K or of V
+    static constexpr int kStageBytes = 2 * kPageBytes;
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kNTiles = D / 8;
+};
+
+template <int D>
+int decode_smem_bytes(int B) {
+    using C = DecodeCfg<D>;
+    return 1024 /* alignment slack */ + C::kWarps * C::kWarpBytes +
+           C::kWarps * C::kStages * (8 + 4) + (2 * B + 1) * 4;
+}
+
+__device__ __forceinline__ float quad_max(float x) {
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+    return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// Lengths (validated, clamped) and the exclusive prefix sum of pages per
+// sequence into shared memory.  128 threads.
+__device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len) {
+    __shared__ int s_warp_tot[4];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int per_t = (a.B + 127) / 128;
+    const int b0 = min(a.B, tid * per_t), b1 = min(a.B, b0 + per_t);
+    const int cap = a.max_pages * kPageSize;
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+        int L = a.seq_lens[b];
+        if (L < 0 || L > cap) {
+            set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
+            L = L < 0 ? 0 : cap;
+        }
+        s_len[b] = L;
+        local += (L + kPageSize - 1) / kPageSize;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp_tot[wid] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < wid; ++w) run += s_warp_tot[w];
+    for (int b = b0; b < b1; ++b) {
+        s_prefix[b] = run;
+        run += (s_len[b] + kPageSize - 1) / kPageSize;
+    }
+    if (tid == 0) s_prefix[a.B] = s_warp_tot[0] + s_warp_tot[1] + s_warp_tot[2] + s_warp_tot[3];
+    __syncthreads();
+}
+
+// Position in the unit list: sequence b, KV head g, page p of the sequence.
+struct Cursor {
+    int b, g, p, pb;  // pb = pages of sequence b
+};
+
+template <int D>
+__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
+    decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+    using C = DecodeCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kWarps * C::kWarpBytes);
+    int *s_nvalid = reinterpret_cast<int *>(bars + C::kWarps * S);
+    int *s_prefix = s_nvalid + C::kWarps * S;
+    int *s_len = s_prefix + a.B + 1;
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    if (lane < S) mbar_init(&bars[wid * S + lane], 1);
+    fence_mbar_init();
+    scan_pages(a, s_prefix, s_len);  // contains __syncthreads
+
+    const int64_t T = (int64_t)a.Hkv * s_prefix[a.B];
+    int64_t per = (T + a.total_warps - 1) / a.total_warps;
+    if (per < kMinUnitsPerWarp) per = kMinUnitsPerWarp;
+    if (blockIdx.x == 0) {
+        for (int b = tid; b <= a.B; b += blockDim.x) a.ws_prefix[b] = s_prefix[b];
+        if (tid == 0) {
+            a.ws_plan[0] = T;
+            a.ws_plan[1] = per;
+        }
+    }
+    const int wglob = blockIdx.x * C::kWarps + wid;
+    const int64_t u_begin = (int64_t)wglob * per;
+    if (u_begin >= T) return;  // warp-uniform; no block-wide barrier follows
+    const int n_units = (int)min(per, T - u_begin);
+
+    uint8_t *wbuf = smem + wid * C::kWarpBytes;
+    uint64_t *wbar = bars + wid * S;
+    int *wnv = s_nvalid + wid * S;
+
+    // locate the first unit: the last sequence whose first unit is <= u_begin
+    Cursor cur;
+    {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)a.Hkv * s_prefix[mid] <= u_begin)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        cur.b = lo;
+        cur.pb = s_prefix[lo + 1] - s_prefix[lo];
+        const int64_t local = u_begin - (int64_t)a.Hkv * s_prefix[lo];
+        cur.g = (int)(local / cur.pb);
+        cur.p = (int)(local % cur.pb);
+    }
+    auto advance = [&](Cursor &c) {
+        if (++c.p == c.pb) {
+            c.p = 0;
+            if (++c.g == a.Hkv) {
+                c.g = 0;
+                do {
+                    ++c.b;
+                    c.pb = c.b < a.B ? s_prefix[c.b + 1] - s_prefix[c.b] : 1;
+                } while (c.b < a.B && c.pb == 0);
+            }
+        }
+    };
+
+    // Block-table window: lane l holds entry p0 + l of sequence win_b.
+    int win_b = -1, win_p0 = 0, win_val = -1;
+    auto page_of = [&](const Cursor &c) -> int {
+        const int p0 = c.p & ~31;
+        if (c.b != win_b || p0 != win_p0) {
+            win_b = c.b;
+            win_p0 = p0;
+            const int pp = p0 + lane;
+            win_val = pp < c.pb ? a.block_table[(int64_t)c.b * a.max_pages + pp] : -1;
+        }
+        return __shfl_sync(0xffffffffu, win_val, c.p - p0);
+    };
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto produce = [&](int stage, const Cursor &c) {
+        const int pg = page_of(c);
+        const bool ok = pg >= 0 && pg < a.num_pages;
+        if (lane == 0) {
+            const int nv = ok ? min(kPageSize, s_len[c.b] - kPageSize * c.p) : 0;
+            wnv[stage] = nv;
+            uint64_t *bar = &wbar[stage];
+            uint8_t *kb = wbuf + stage * C::kStageBytes;
+            uint8_t *vb = kb + C::kPageBytes;
+            if (ok) {
+                mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+                for (int x = 0; x < C::kHalves; ++x) {
+                    tma_load_4d_hint(kb + x * 2048, &kmap, bar, x * 64, 0, c.g, pg, policy);
+                    tma_load_4d_hint(vb + x * 2048, &vmap, bar, x * 64, 0, c.g, pg, policy);
+                }
+            } else {
+                set_status(a.status, SINKATTN_STATUS_BAD_PAGE);
+                mbar_arrive(bar);
+            }
+        }
+    };
+
+    Cursor pc = cur;
+    const int n_pro = min(S, n_units);
+    for (int u = 0; u < n_pro; ++u) {
+        produce(u, pc);
+        advance(pc);
+    }
+
+    // per-lane fragment coordinates
+    const int gr = lane >> 2;        // row (query head) of c0/c1; +8 for c2/c3
+    const int tc = (lane & 3) * 2;   // first column of this lane's pair
+    const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix index, row within it
+
+    uint32_t qa[C::kKSteps][4];
+    float acc[C::kNTiles][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int seg_p0 = cur.p;
+    bool seg_start = true;
+
+    for (int u = 0; u < n_units; ++u) {
+        const int stage = u % S;
+        if (!mbar_wait(&wbar[stage], (uint32_t)((u / S) & 1))) {
+            // give up: record it, let the copies already issued land, leave
+            if (lane == 0) set_status(a.status, SINKATTN_STATUS_WAIT_TIMEOUT);
+            for (int v = u; v < min(n_units, u + S); ++v)
+                mbar_wait(&wbar[v % S], (uint32_t)((v / S) & 1), 100000000ull);
+            return;
+        }
+        uint8_t *kb = wbuf + stage * C::kStageBytes;
+        uint8_t *vb = kb + C::kPageBytes;
+        const int nv = wnv[stage];
+        if (nv < kPageSize) {
+            // rows past the sequence end (or a skipped page) may hold anything,
+            // even NaN; P is 0 there but 0 * NaN is not 0, so clear those V rows
+            const int nrow = kPageSize - nv, per_half = nrow * 8;
+            for (int i = lane; i < per_half * C::kHalves; i += 32) {
+                const int h = i / per_half, j = i % per_half;
+                *reinterpret_cast<uint4 *>(vb + h * 2048 + (nv + j / 8) * 128 + (j % 8) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+
+        if (seg_start) {
+            const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                                      ((int64_t)cur.b * a.Hq + (int64_t)cur.g * a.G) * D;
+#pragma unroll
+            for (int kk = 0; kk < C::kKSteps; ++kk) {
+                const int col = kk * 16 + tc;
+                const bool r0 = gr < a.G, r1 = gr + 8 < a.G;
+                qa[kk][0] = r0 ? *reinterpret_cast<const uint32_t *>(qg + gr * D + col) : 0u;
+                qa[kk][1] = r1 ? *reinterpret_cast<const uint32_t *>(qg + (gr + 8) * D + col) : 0u;
+                qa[kk][2] = r0 ? *reinterpret_cast<const uint32_t *>(qg + gr * D + col + 8) : 0u;
+                qa[kk][3] =
+                    r1 ? *reinterpret_cast<const uint32_t *>(qg + (gr + 8) * D + col + 8) : 0u;
+            }
+#pragma unroll
+            for (int n = 0; n < C::kNTiles; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            seg_p0 = cur.p;
+            seg_start = false;
+        }
+
+        // S = Q K^T for the 16 tokens of this page (two n-tiles of 8 tokens)
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const uint32_t kbase = smem_u32(kb);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
+            const int tok = (lm >> 1) * 8 + lr, chunk = kk * 2 + (lm & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), b0, b1, b2, b3);
+            mma_16816(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tok = n * 8 + tc + (i & 1);
+                s[n][i] = tok < nv ? s[n][i] * a.scale_log2 : -INFINITY;
+            }
+        const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
+        const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            p[n][0] = fast_exp2(s[n][0] - base0);
+            p[n][1] = fast_exp2(s[n][1] - base0);
+            p[n][2] = fast_exp2(s[n][2] - base1);
+            p[n][3] = fast_exp2(s[n][3] - base1);
+        }
+        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+#pragma unroll
+        for (int n = 0; n < C::kNTiles; ++n) {
+            acc[n][0] *= al0;
+            acc[n][1] *= al0;
+            acc[n][2] *= al1;
+            acc[n][3] *= al1;
+        }
+        const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
+        const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
+
+        // O += P V: V rows are tokens (the k axis), columns head_dim (n axis)
+        const uint32_t vbase = smem_u32(vb);
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+            const int tok = (lm & 1) * 8 + lr, chunk = c * 2 + (lm >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), b0, b1, b2, b3);
+            mma_16816(acc[2 * c], pa0, pa1, pa2, pa3, b0, b1);
+            mma_16816(acc[2 * c + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+
+        const bool seg_end = (cur.p == cur.pb - 1) || (u == n_units - 1);
+        if (seg_end) {
+            const float L0 = quad_sum(l0), L1 = quad_sum(l1);
+            const bool whole = seg_p0 == 0 && cur.p == cur.pb - 1;
+            if (whole) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int r = gr + half * 8;
+                    if (r < a.G) {
+                        const int h = cur.g * a.G + r;
+                        const float m = half ? m1 : m0, l = half ? L1 : L0;
+                        const float sk = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+                        const float M = fmaxf(m, sk);
+                        float scl = 0.f, lse2 = -INFINITY;
+                        if (M != -INFINITY) {
+                            const float wm = m == -INFINITY ? 0.f : exp2f(m - M);
+                            const float den = l * wm + (sk == -INFINITY ? 0.f : exp2f(sk - M));
+                            scl = wm / den;
+                            lse2 = M + log2f(den);
+                        }
+                        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                                            ((int64_t)cur.b * a.Hq + h) * D;
+#pragma unroll
+                        for (int n = 0; n < C::kNTiles; ++n)
+                            *reinterpret_cast<uint32_t *>(og + n * 8 + tc) =
+                                pack_bf16x2(acc[n][2 * half] * scl, acc[n][2 * half + 1] * scl);
+                        if (a.lse && (lane & 3) == 0)
+                            a.lse[(int64_t)cur.b * a.Hq + h] = lse2 * kLn2;
+                    }
+                }
+            } else {
+                const int64_t slot = (int64_t)wglob + (int64_t)cur.b * a.Hkv + cur.g;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int r = gr + half * 8;
+                    if (r < a.G) {
+                        const int64_t row = slot * a.G + r;
+                        float *pa = a.part_acc + row * D;
+#pragma unroll
+                        for (int n = 0; n < C::kNTiles; ++n)
+                            *reinterpret_cast<float2 *>(pa + n * 8 + tc) =
+                                make_float2(acc[n][2 * half], acc[n][2 * half + 1]);
+                        if ((lane & 3) == 0)
+                            *reinterpret_cast<float2 *>(a.part_ml + row * 2) =
+                                make_float2(half ? m1 : m0, half ? L1 : L0);
+                    }
+                }
+            }
+            seg_start = true;
+        }
+        advance(cur);
+
+        // every lane's reads and V-row clears of this stage are ordered before
+        // the TMA that lane 0 issues into it next
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (u + S < n_units) {
+            produce(stage, pc);
+            advance(pc);
+        }
+    }
+}
+
+// One CTA per (sequence, KV head): combine the partial states of a split
+// sequence and add the sink; write out = 0, lse = sink for empty sequences.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+    const int b = blockIdx.x / a.Hkv, g = blockIdx.x % a.Hkv;
+    const int p0 = a.ws_prefix[b], pb = a.ws_prefix[b + 1] - p0;
+    const int G = a.G;
+    __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
+    if (pb == 0) {
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) og[i] = __float2bfloat16(0.f);
+        if (a.lse)
+            for (int r = threadIdx.x; r < G; r += blockDim.x)
+                a.lse[(int64_t)b * a.Hq + g * G + r] = a.sinks ? a.sinks[g * G + r] : -INFINITY;
+        return;
+    }
+    const int64_t start = (int64_t)a.Hkv * p0 + (int64_t)g * pb, last = start + pb - 1;
+    const int64_t per = a.ws_plan[1];
+    const int64_t w_lo = start / per, w_hi = last / per;
+    if (w_lo == w_hi) return;  // finished by the split-KV kernel
+    const int nsplit = (int)(w_hi - w_lo + 1);
+    const int64_t slot0 = w_lo + (int64_t)b * a.Hkv + g;
+    constexpr int kQuads = D / 4;
+    for (int i = threadIdx.x; i < G * kQuads; i += blockDim.x) {
+        const int r = i / kQuads, d4 = i % kQuads, h = g * G + r;
+        const float sk = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+        float M = sk;
+        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, a.part_ml[((slot0 + s) * G + r) * 2]);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse2 = -INFINITY;
+        if (M != -INFINITY) {
+            float den = sk == -INFINITY ? 0.f : exp2f(sk - M);
+            for (int s = 0; s < nsplit; ++s) {
+                const int64_t row = (slot0 + s) * G + r;
+                const float2 ml = *reinterpret_cast<const float2 *>(a.part_ml + row * 2);
+                if (ml.x == -INFINITY) continue;
+                const float w = exp2f(ml.x - M);
+                den += ml.y * w;
+                const float4 v = *reinterpret_cast<const float4 *>(a.part_acc + row * D + d4 * 4);
+                o.x += w * v.x;
+                o.y += w * v.y;
+                o.z += w * v.z;
+                o.w += w * v.w;
+            }
+            const float inv = 1.f / den;
+            o.x *= inv;
+            o.y *= inv;
+            o.z *= inv;
+            o.w *= inv;
+            lse2 = M + log2f(den);
+        }
+        uint2 packed = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+        *reinterpret_cast<uint2 *>(og + r * D + d4 * 4) = packed;
+        if (a.lse && d4 == 0) a.lse[(int64_t)b * a.Hq + h] = lse2 * kLn2;
+    }
+}
+
+template <int D>
+cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
+    using C = DecodeCfg<D>;
+    const int bytes = decode_smem_bytes<D>(B);
+    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    int sms = 0, occ = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_splitkv_kernel<D>,
+                                                      C::kThreads, bytes);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    *ctas = sms * occ;
+    *warps = C::kWarps;
+    *smem = bytes;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_per_cta,
+                                int *smem_bytes) {
+    // occupancy queries cost microseconds; remember the answer per (device, D, B)
+    struct Entry {
+        int device, D, B, ctas, warps, smem;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry &e : cache)
+            if (e.device == device && e.D == D && e.B == B) {
+                *ctas = e.ctas;
+                *warps_per_cta = e.warps;
+                *smem_bytes = e.smem;
+                return cudaSuccess;
+            }
+    }
+    cudaError_t e;
+    if (D == 64)
+        e = shape_for<64>(B, device, ctas, warps_per_cta, smem_bytes);
+    else if (D == 128)
+        e = shape_for<128>(B, device, ctas, warps_per_cta, smem_bytes);
+    else
+        return cudaErrorInvalidValue;
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache.size() > 256) cache.clear();
+        cache.push_back({device, D, B, *ctas, *warps_per_cta, *smem_bytes});
+    }
+    return e;
+}
+
+cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap &kmap,
+                                  const CUtensorMap &vmap, int ctas, int smem_bytes,
+                                  cudaStream_t stream) {
+    if (D == 64)
+        decode_splitkv_kernel<64><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+    else
+        decode_splitkv_kernel<128><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_merge(int D, const DecodeArgs &a, cudaStream_t stream) {
+    const unsigned grid = (unsigned)a.B * (unsigned)a.Hkv;
+    if (grid == 0) return cudaSuccess;
+    if (D == 64)
+        decode_merge_kernel<64><<<grid, 128, 0, stream>>>(a);
+    else
+        decode_merge_kernel<128><<<grid, 128, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace sinkattn

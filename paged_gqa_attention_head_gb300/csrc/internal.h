@@ -1,0 +1,68 @@
+// Internal interfaces between the C ABI (api.cpp) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sinkattn {
+
+constexpr int kPageSize = 16;
+constexpr uint32_t kStatusBytes = 256;  // workspace header holding the status word
+
+// Arguments of the two decode kernels (plain device pointers and sizes).
+struct DecodeArgs {
+    const void *q;               // bf16 [B, Hq, D]
+    const int32_t *block_table;  // [B, max_pages]
+    const int32_t *seq_lens;     // [B]
+    const float *sinks;          // [Hq] or nullptr
+    float scale_log2;            // scale * log2(e)
+    void *out;                   // bf16 [B, Hq, D]
+    float *lse;                  // [B, Hq] or nullptr
+    int B, Hq, Hkv, G, num_pages, max_pages;
+    int total_warps;        // warps of the split-KV grid
+    uint32_t *status;       // workspace header
+    int32_t *ws_prefix;     // [B + 1] pages-per-sequence prefix sum (written by CTA 0)
+    int64_t *ws_plan;       // [2]: total page units, page units per warp
+    float *part_ml;         // [slots, G, 2] partial (max, sum), log2 domain
+    float *part_acc;        // [slots, G, D] partial unnormalised outputs
+};
+
+// Grid and shared memory of the split-KV decode kernel for head_dim D and
+// batch B on `device`.  Deterministic for a given (device, D, B).
+cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_per_cta,
+                                int *smem_bytes);
+cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap &kmap,
+                                  const CUtensorMap &vmap, int ctas, int smem_bytes,
+                                  cudaStream_t stream);
+cudaError_t launch_decode_merge(int D, const DecodeArgs &a, cudaStream_t stream);
+
+struct AppendArgs {
+    const void *k, *v;  // bf16 [T, Hkv, D]
+    const int32_t *cu_seqlens;
+    const int32_t *block_table;
+    const int32_t *start_pos;
+    void *k_pages, *v_pages;
+    int T, n, Hkv, D, num_pages, max_pages;
+    uint32_t *status;
+};
+cudaError_t launch_append_kv(const AppendArgs &a, cudaStream_t stream);
+
+struct PrefillArgs {
+    const int32_t *cu_seqlens;  // [n + 1]
+    const int32_t *prefix_block_table;  // [n, max_pages] or nullptr
+    const int32_t *prefix_lens;         // [n] or nullptr
+    const void *k_pages, *v_pages;      // prefix pages (plain loads of ragged pages)
+    const float *sinks;
+    float scale_log2;
+    void *out;   // bf16 [T, Hq, D]
+    float *lse;  // [T, Hq] or nullptr
+    int T, n, Hq, Hkv, G, D, num_pages, max_pages;
+    uint32_t *status;
+};
+// Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.
+cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, const CUtensorMap &kpmap,
+                           const CUtensorMap &vpmap, cudaStream_t stream);
+
+}  // namespace sinkattn

@@ -64,9 +64,24 @@ def normal_f32(n: int, seed: int, stream: int) -> np.ndarray:
 
 
 def normal_bf16(shape, seed: int, stream: int) -> torch.Tensor:
+    """Same values as normal_f32(...) rounded to bf16, converted chunk by chunk so
+    that large tensors never exist in float32 all at once."""
     n = int(np.prod(shape)) if len(shape) else 1
-    f = torch.from_numpy(normal_f32(n, seed, stream))
-    return f.to(torch.bfloat16).reshape(shape)
+    out = torch.empty(n, dtype=torch.bfloat16)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def work(i: int) -> None:
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        buf = _rng(seed, stream, i).standard_normal(hi - lo, dtype=np.float32)
+        out[lo:hi] = torch.from_numpy(buf).to(torch.bfloat16)
+
+    if nchunks <= 1:
+        if n:
+            work(0)
+    else:
+        with ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out.reshape(shape)
 
 
 def poison_rows_(t: torch.Tensor) -> None:

@@ -1,0 +1,278 @@
+"""Thin ctypes binding of libsinkattn (include/sinkattn.h).
+
+Argument marshalling only: tensors are checked (device, dtype, contiguity,
+shape), their device pointers and the current CUDA stream are passed to the C
+ABI, and error codes become exceptions.  Every step of the attention runs in
+the library's CUDA kernels; there is no fallback.  Workspaces are torch
+allocations owned by this module (one per device and size, zero-initialised).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
+STATUS_BAD_PAGE, STATUS_BAD_LENGTH, STATUS_BAD_CU_SEQLENS, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
+PAGE_SIZE = 16
+
+# every symbol the header declares, with (restype, argtypes)
+_P, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+
+
+class PagedDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", _I32), ("num_qo_heads", _I32), ("num_kv_heads", _I32),
+                ("head_dim", _I32), ("page_size", _I32), ("num_pages", _I32),
+                ("max_pages_per_seq", _I32)]
+
+
+_DP = ctypes.POINTER(PagedDesc)
+SIGNATURES = {
+    "sinkattn_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sinkattn_version": (ctypes.c_int, []),
+    "sinkattn_decode_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
+    "sinkattn_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
+    "sinkattn_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_decode_splitkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_decode_merge": (ctypes.c_int, [_P, _P, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_prefill_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
+    "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
+                                        _P, _SZ, _P]),
+    "sinkattn_append_kv": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+}
+
+_lib = None
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {error_string(code)} ({code})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libsinkattn.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m "
+                               "paged_gqa_attention_head_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return load().sinkattn_error_string(code).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise SinkAttnError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_workspaces: dict = {}
+
+
+def workspace(nbytes: int, device: torch.device, tag: str = "default") -> torch.Tensor:
+    """A zero-initialised uint8 device buffer of at least nbytes, cached per (device, tag)."""
+    key = (device, tag)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def paged_desc(num_seqs, num_qo_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
+               page_size=PAGE_SIZE) -> PagedDesc:
+    return PagedDesc(num_seqs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+                     max_pages_per_seq)
+
+
+_ws_sizes: dict = {}
+
+
+def decode_workspace_size(desc: PagedDesc) -> int:
+    """Bytes of decode workspace for desc on the current device (memoised)."""
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else -1,
+           tuple(getattr(desc, f) for f, _ in desc._fields_))
+    n = _ws_sizes.get(key)
+    if n is None:
+        c = _SZ()
+        _check(load().sinkattn_decode_workspace_size(ctypes.byref(desc), ctypes.byref(c)),
+               "decode_workspace_size")
+        n = _ws_sizes[key] = c.value
+    return n
+
+
+def prefill_workspace_size(desc: PagedDesc) -> int:
+    n = _SZ()
+    _check(load().sinkattn_prefill_workspace_size(ctypes.byref(desc), ctypes.byref(n)),
+           "prefill_workspace_size")
+    return n.value
+
+
+def get_status(ws: torch.Tensor) -> int:
+    """Read and clear the device status word of a workspace (synchronous)."""
+    v = ctypes.c_uint32()
+    _check(load().sinkattn_get_status(_ptr(ws), ctypes.byref(v), _stream(ws.device)), "get_status")
+    return v.value
+
+
+def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
+                 want_lse):
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, dev, 4)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    if D2 != D or tuple(v_pages.shape) != tuple(k_pages.shape) or P != PAGE_SIZE:
+        raise ValueError("k_pages / v_pages must be [num_pages, Hkv, 16, D] matching q")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens rows must equal the batch")
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, 1)
+        if sinks.shape[0] != Hq:
+            raise ValueError("sinks must have one entry per query head")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, dev, 3)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, dev, 2)
+    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1])
+    nbytes = decode_workspace_size(desc)
+    if ws is None:
+        ws = workspace(nbytes, dev)
+    elif ws.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    return desc, out, lse, ws, scale
+
+
+def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None, lse=None,
+           workspace_buf=None, return_lse=True):
+    """Split-KV paged decode with sinks (sinkattn_decode).  Returns (out, lse)."""
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse)
+    _check(load().sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                  _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
+                                  ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(q.device)),
+           "sinkattn_decode")
+    return out, lse
+
+
+def decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
+                   lse=None, workspace_buf=None, return_lse=True):
+    """First decode kernel only (sinkattn_decode_splitkv); follow with decode_merge."""
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse)
+    _check(load().sinkattn_decode_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                          _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
+                                          ctypes.byref(desc), _ptr(ws), ws.numel(),
+                                          _stream(q.device)), "sinkattn_decode_splitkv")
+    return out, lse, ws, desc
+
+
+def decode_merge(seq_lens, sinks, out, lse, desc, ws):
+    """Second decode kernel (sinkattn_decode_merge) on the split-KV kernel's workspace."""
+    _check(load().sinkattn_decode_merge(_ptr(seq_lens), _ptr(sinks), _ptr(out), _ptr(lse),
+                                        ctypes.byref(desc), _ptr(ws), ws.numel(),
+                                        _stream(out.device)), "sinkattn_decode_merge")
+    return out, lse
+
+
+def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
+            prefix_block_table=None, prefix_lens=None, out=None, lse=None, workspace_buf=None,
+            return_lse=True):
+    """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  Returns (out, lse)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(k, "k", torch.bfloat16, dev, 3)
+    _need(v, "v", torch.bfloat16, dev, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D):
+        raise ValueError("k / v must be [T, Hkv, D] matching q")
+    n = cu_seqlens.shape[0] - 1
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, 1)
+    num_pages = maxp = 0
+    if k_pages is not None:
+        _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
+        _need(v_pages, "v_pages", torch.bfloat16, dev, 4)
+        _need(prefix_block_table, "prefix_block_table", torch.int32, dev, 2)
+        _need(prefix_lens, "prefix_lens", torch.int32, dev, 1)
+        num_pages, maxp = k_pages.shape[0], prefix_block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
+    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp)
+    nbytes = prefill_workspace_size(desc)
+    ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().sinkattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), T, _ptr(k_pages),
+                                   _ptr(v_pages), _ptr(prefix_block_table), _ptr(prefix_lens),
+                                   _ptr(sinks), scale, _ptr(out), _ptr(lse), ctypes.byref(desc),
+                                   _ptr(ws), ws.numel(), _stream(dev)), "sinkattn_prefill")
+    return out, lse
+
+
+def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages, workspace_buf=None):
+    """Scatter new K/V rows into the paged cache in place (sinkattn_append_kv)."""
+    dev = k.device
+    _need(k, "k", torch.bfloat16, dev, 3)
+    _need(v, "v", torch.bfloat16, dev, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(start_pos, "start_pos", torch.int32, dev, 1)
+    _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, dev, 4)
+    T, Hkv, D = k.shape
+    n = cu_seqlens.shape[0] - 1
+    desc = paged_desc(n, Hkv, Hkv, D, k_pages.shape[0], block_table.shape[1])
+    ws = workspace_buf if workspace_buf is not None else workspace(256, dev, "append")
+    _check(load().sinkattn_append_kv(_ptr(k), _ptr(v), _ptr(cu_seqlens), T, _ptr(block_table),
+                                     _ptr(start_pos), _ptr(k_pages), _ptr(v_pages),
+                                     ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(dev)),
+           "sinkattn_append_kv")
+    return k_pages, v_pages

@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks reject bad calls before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sinkattn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sinkattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("sinkattn_decode", "sinkattn_prefill", "sinkattn_decode_merge",
+              "sinkattn_decode_splitkv", "sinkattn_append_kv", "sinkattn_get_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", built_lib], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (sinkattn_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol(sa):
+    assert sorted(sa.SIGNATURES) == declared_functions()
+    lib = sa.load()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_error_strings_and_version(sa):
+    assert sa.error_string(0) == "ok"
+    assert "workspace" in sa.error_string(3)
+    assert sa.load().sinkattn_version() >= 10000
+
+
+def _desc(sa, **kw):
+    d = dict(num_seqs=4, num_qo_heads=8, num_kv_heads=2, head_dim=64, num_pages=10,
+             max_pages_per_seq=4)
+    d.update(kw)
+    return sa.paged_desc(**d)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(head_dim=96), 2), (dict(num_qo_heads=12, num_kv_heads=4), 2),   # G = 3
+    (dict(num_qo_heads=9), 1), (dict(num_pages=0), 1), (dict(max_pages_per_seq=0), 1),
+    (dict(num_kv_heads=0), 1), (dict(num_qo_heads=64, num_kv_heads=2), 2),  # G = 32
+])
+def test_decode_workspace_size_rejects(sa, bad, code):
+    n = ctypes.c_size_t()
+    d = _desc(sa, **bad)
+    assert sa.load().sinkattn_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == code
+
+
+def test_page_size_must_be_16(sa):
+    n = ctypes.c_size_t()
+    d = _desc(sa)
+    d.page_size = 32
+    assert sa.load().sinkattn_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 2
+
+
+def test_null_pointers_rejected_before_cuda(sa):
+    lib = sa.load()
+    d = _desc(sa)
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None,
+                               ctypes.byref(d), None, 0, None) == 1
+    assert lib.sinkattn_prefill(None, None, None, None, 0, None, None, None, None, None, 0.125,
+                                None, None, ctypes.byref(d), None, 0, None) == 1
+    assert lib.sinkattn_append_kv(None, None, None, 0, None, None, None, None, ctypes.byref(d),
+                                  None, 0, None) == 1
+    assert lib.sinkattn_get_status(None, None, None) == 1
+
+
+def test_misaligned_pointers_rejected(sa):
+    lib = sa.load()
+    d = _desc(sa)
+    buf = (ctypes.c_uint8 * 4096)()
+    base = ctypes.addressof(buf)
+    p16 = (base + 15) // 16 * 16
+    # a prefill whose q is 2 bytes off a 16-byte boundary
+    rc = lib.sinkattn_prefill(p16 + 2, p16, p16, p16, 8, None, None, None, None, None, 0.125,
+                              p16, None, ctypes.byref(d), (base + 255) // 256 * 256, 256, None)
+    assert rc == 1
+
+
+def test_prefix_arguments_all_or_nothing(sa):
+    lib = sa.load()
+    d = _desc(sa)
+    buf = (ctypes.c_uint8 * 8192)()
+    p = (ctypes.addressof(buf) + 255) // 256 * 256
+    # k_pages given without the other prefix arguments
+    rc = lib.sinkattn_prefill(p, p, p, p, 8, p, None, None, None, None, 0.125, p, None,
+                              ctypes.byref(d), p, 256, None)
+    assert rc == 1
