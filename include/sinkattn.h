@@ -144,6 +144,37 @@ int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out
                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                           sinkattn_stream_t stream);
 
+/* ------------------------------------------------------- decode, no allocation --
+ * No counterpart on the source pages: an addition for callers that cannot allocate
+ * device memory where they run attention - code whose device memory is owned by
+ * another allocator, latency-critical paths that must not call cudaMalloc, or hosts
+ * that forbid allocation after start-up.  It computes exactly what sinkattn_decode
+ * computes, but its scratch is a fixed array inside the library instead of a
+ * caller-provided workspace; the caller still passes every input and output.
+ *
+ * Limit: the scratch array holds SINKATTN_NOALLOC_SCRATCH_BYTES (32 MiB).  Shapes
+ * whose sinkattn_decode_workspace_size exceeds it are rejected with
+ * SINKATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  Every GPU that loads
+ * the library holds the array until the process exits.
+ *
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  The
+ * call itself allocates nothing and calls no allocating routine.  All calls on a
+ * device share the one array and it keeps the previous call's contents, so calls
+ * that overlap on the GPU (different streams without ordering, or different host
+ * threads) race; order them on one stream or synchronise.
+ *
+ * status: device pointer to one uint32, or NULL.  When given, it receives the
+ * SINKATTN_STATUS_* bits of this call (overwritten, not OR-ed), in stream order.
+ */
+#define SINKATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const float *sinks, float scale, void *out, float *lse,
+                            const sinkattn_paged_desc *desc, uint32_t *status,
+                            sinkattn_stream_t stream);
+
 /* ----------------------------------------------------------------- prefill --
  * Causal prefill over packed ragged sequences ("Fast embeddings on GPUs", section
  * on kernels: ragged inputs without padding, paged prefill), optionally after a

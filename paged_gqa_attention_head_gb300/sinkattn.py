@@ -41,6 +41,7 @@ SIGNATURES = {
     "sinkattn_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_splitkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_merge": (ctypes.c_int, [_P, _P, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _P]),
     "sinkattn_prefill_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
     "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
                                         _P, _SZ, _P]),
@@ -276,3 +277,27 @@ def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages, worksp
                                      ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(dev)),
            "sinkattn_append_kv")
     return k_pages, v_pages
+
+
+def decode_noalloc(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
+                   lse=None, status=None):
+    """sinkattn_decode_noalloc: the same decode with the library's fixed scratch array
+    instead of a workspace, for callers that cannot allocate device memory.  Calls on
+    one device must not overlap on the GPU.  status: optional int32/uint32 device
+    tensor of one element receiving this call's status bits."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
+    B, Hq, D = q.shape
+    num_pages, Hkv = k_pages.shape[:2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1])
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().sinkattn_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                          _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
+                                          ctypes.byref(desc), _ptr(status), _stream(dev)),
+           "sinkattn_decode_noalloc")
+    return out, lse
