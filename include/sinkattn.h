@@ -85,6 +85,10 @@ const char *sinkattn_error_string(int code);
 /* Library version as 10000 * major + 100 * minor + patch. */
 int sinkattn_version(void);
 
+/* Name of the CUDA runtime error behind the most recent SINKATTN_ERR_CUDA returned to
+ * the calling host thread (static string; "no error" if there was none). */
+const char *sinkattn_last_cuda_error(void);
+
 /* ------------------------------------------------------------------ decode --
  * Split-KV decode ("GPT-OSS on Day 0", section "Sink Attention": the attention is
  * parallelised over heads and along the KV length, the partial softmax states are
@@ -189,7 +193,7 @@ int sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pa
  * cu_seqlens: int32 [num_seqs + 1], cu_seqlens[0] = 0, non-decreasing
  * k_pages, v_pages, prefix_block_table [num_seqs, max_pages_per_seq], prefix_lens
  *             [num_seqs]: the paged prefix; all four NULL for a plain causal prefill
- * sinks, scale, lse: as for decode, with lse [T, Hq]
+ * sinks, scale, lse: as for decode, with lse [T, Hq]; scale must be positive and finite
  * out:        bf16 [T, Hq, D]
  * desc:       num_seqs, heads, head_dim, page_size; num_pages and max_pages_per_seq
  *             describe the prefix pages (ignored without a prefix)

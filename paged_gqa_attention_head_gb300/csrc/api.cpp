@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <math.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <mutex>
@@ -20,6 +22,17 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+thread_local const char *g_last_cuda_where = "";
+thread_local char g_last_cuda_text[160];
+
+int cuda_rc(cudaError_t e, const char *where = "") {
+    if (e == cudaSuccess) return SINKATTN_OK;
+    g_last_cuda_error = e;
+    g_last_cuda_where = where;
+    return SINKATTN_ERR_CUDA;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -98,10 +111,12 @@ struct DecodeLayout {
 
 int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
     int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;
-    if (decode_launch_shape(d->head_dim, d->num_seqs, device, &L->ctas, &L->warps_per_cta,
-                            &L->smem) != cudaSuccess)
-        return SINKATTN_ERR_CUDA;
+    int rc = cuda_rc(cudaGetDevice(&device), "cudaGetDevice");
+    if (rc) return rc;
+    rc = cuda_rc(decode_launch_shape(d->head_dim, d->num_seqs, device, &L->ctas, &L->warps_per_cta,
+                                     &L->smem),
+                 "decode launch shape");
+    if (rc) return rc;
     L->total_warps = L->ctas * L->warps_per_cta;
     const int G = d->num_qo_heads / d->num_kv_heads;
     const size_t slots = (size_t)L->total_warps + (size_t)d->num_seqs * d->num_kv_heads;
@@ -118,7 +133,6 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
     return SINKATTN_OK;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SINKATTN_OK : SINKATTN_ERR_CUDA; }
 
 struct DecodePrep {
     DecodeArgs args;
@@ -165,7 +179,16 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
 
 }  // namespace
 
+void sinkattn::record_cuda_error(cudaError_t e, const char *where) { cuda_rc(e, where); }
+
 extern "C" {
+
+const char *sinkattn_last_cuda_error(void) {
+    if (g_last_cuda_error == cudaSuccess) return "no error";
+    snprintf(g_last_cuda_text, sizeof g_last_cuda_text, "%s in %s", cudaGetErrorName(g_last_cuda_error),
+             g_last_cuda_where);
+    return g_last_cuda_text;
+}
 
 const char *sinkattn_error_string(int code) {
     switch (code) {
@@ -194,7 +217,7 @@ int sinkattn_decode_workspace_size(const sinkattn_paged_desc *desc, size_t *byte
 int sinkattn_workspace_init(void *workspace, size_t ws_bytes, sinkattn_stream_t stream) {
     if (!workspace || ws_bytes < kStatusBytes || !aligned(workspace, kAlign))
         return SINKATTN_ERR_INVALID_ARG;
-    return cuda_rc(cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream));
+    return cuda_rc(cudaMemsetAsync(workspace, 0, kStatusBytes, (cudaStream_t)stream), "cudaMemsetAsync");
 }
 
 int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pages,
@@ -215,7 +238,8 @@ int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pa
     rc = encode_pages_map(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
     if (rc) return rc;
     return cuda_rc(launch_decode_splitkv(desc->head_dim, P.args, kmap, vmap, P.layout.ctas,
-                                         P.layout.smem, (cudaStream_t)stream));
+                                         P.layout.smem, (cudaStream_t)stream),
+                   "split-KV decode launch");
 }
 
 int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out, float *lse,
@@ -228,7 +252,7 @@ int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out
                             ws_bytes, &P);
     if (rc) return rc;
     if (desc->num_seqs == 0) return SINKATTN_OK;
-    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, (cudaStream_t)stream));
+    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, (cudaStream_t)stream), "merge launch");
 }
 
 int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
@@ -258,6 +282,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     int rc = check_heads(desc);
     if (rc) return rc;
     if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < INFINITY)) return SINKATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !cu_seqlens || !out || !workspace) return SINKATTN_ERR_INVALID_ARG;
     if (ws_bytes < kStatusBytes) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -306,7 +331,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     a.status = static_cast<uint32_t *>(workspace);
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
     if (e == cudaErrorNotSupported) return SINKATTN_ERR_UNSUPPORTED;
-    return cuda_rc(e);
+    return cuda_rc(e, "prefill launch");
 }
 
 int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,
@@ -341,17 +366,17 @@ int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,
     a.num_pages = desc->num_pages;
     a.max_pages = desc->max_pages_per_seq;
     a.status = static_cast<uint32_t *>(workspace);
-    return cuda_rc(launch_append_kv(a, (cudaStream_t)stream));
+    return cuda_rc(launch_append_kv(a, (cudaStream_t)stream), "append launch");
 }
 
 int sinkattn_get_status(void *workspace, uint32_t *status_out, sinkattn_stream_t stream) {
     if (!workspace || !status_out || !aligned(workspace, kAlign)) return SINKATTN_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t v = 0;
-    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return SINKATTN_ERR_CUDA;
-    if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return SINKATTN_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    int rc = cuda_rc(cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s), "status read");
+    if (!rc) rc = cuda_rc(cudaMemsetAsync(workspace, 0, sizeof v, s), "status clear");
+    if (!rc) rc = cuda_rc(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (rc) return rc;
     *status_out = v;
     return SINKATTN_OK;
 }

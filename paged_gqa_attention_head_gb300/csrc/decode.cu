@@ -309,8 +309,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             p[n][2] = fast_exp2(s[n][2] - base1);
             p[n][3] = fast_exp2(s[n][3] - base1);
         }
-        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
 #pragma unroll
         for (int n = 0; n < C::kNTiles; ++n) {
             acc[n][0] *= al0;
@@ -318,8 +316,21 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             acc[n][2] *= al1;
             acc[n][3] *= al1;
         }
-        const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
-        const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
+        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        // P = P_hi + P_lo, both bf16: the rounding of P to bf16 alone (relative 2^-9)
+        // is too coarse for short sequences, the pair keeps ~16 bits
+        uint32_t ph[4], pl[4];
+        {
+            const float pv[4][2] = {{p[0][0], p[0][1]}, {p[0][2], p[0][3]},
+                                    {p[1][0], p[1][1]}, {p[1][2], p[1][3]}};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ph[e] = pack_bf16x2(pv[e][0], pv[e][1]);
+                pl[e] = pack_bf16x2(pv[e][0] - __uint_as_float(ph[e] << 16),
+                                    pv[e][1] - __uint_as_float(ph[e] & 0xFFFF0000u));
+            }
+        }
 
         // O += P V: V rows are tokens (the k axis), columns head_dim (n axis)
         const uint32_t vbase = smem_u32(vb);
@@ -328,8 +339,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             const int tok = (lm & 1) * 8 + lr, chunk = c * 2 + (lm >> 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), b0, b1, b2, b3);
-            mma_16816(acc[2 * c], pa0, pa1, pa2, pa3, b0, b1);
-            mma_16816(acc[2 * c + 1], pa0, pa1, pa2, pa3, b2, b3);
+            mma_16816(acc[2 * c], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_16816(acc[2 * c + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+            mma_16816(acc[2 * c], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            mma_16816(acc[2 * c + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
         }
 
         const bool seg_end = (cur.p == cur.pb - 1) || (u == n_units - 1);
@@ -455,8 +468,19 @@ template <int D>
 cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     using C = DecodeCfg<D>;
     const int bytes = decode_smem_bytes<D>(B);
-    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // The kernel's dynamic shared-memory ceiling is one setting per kernel, shared
+    // by every batch size: raise it to the device maximum (the occupancy below
+    // still uses this batch's real size).
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, decode_splitkv_kernel<D>);
+    if (e != cudaSuccess) return e;
+    const int ceiling = optin - (int)fa.sharedSizeBytes;  // dynamic + static <= opt-in maximum
+    if (bytes > ceiling) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(decode_splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ceiling);
     if (e != cudaSuccess) return e;
     int sms = 0, occ = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);

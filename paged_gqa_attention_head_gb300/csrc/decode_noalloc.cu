@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/sinkattn.h"
+#include "internal.h"
 
 namespace {
 
@@ -28,13 +29,20 @@ void *g_scratch_ptr[kMaxDevices] = {};
 // device (the host-side symbol itself is not a device address).
 int scratch_address(void **out) {
     int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) {
+        sinkattn::record_cuda_error(e, "cudaGetDevice");
+        return SINKATTN_ERR_CUDA;
+    }
     if (device < 0 || device >= kMaxDevices) return SINKATTN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_ptr[device]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p)
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || !p) {
+            sinkattn::record_cuda_error(e, "cudaGetSymbolAddress");
             return SINKATTN_ERR_CUDA;
+        }
         g_scratch_ptr[device] = p;
     }
     *out = g_scratch_ptr[device];
@@ -58,12 +66,20 @@ extern "C" int sinkattn_decode_noalloc(const void *q, const void *k_pages, const
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The status word is the only scratch that must start at zero; everything
     // else the merge reads is written earlier in this call by the split-KV kernel.
-    if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s) != cudaSuccess) return SINKATTN_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) {
+        sinkattn::record_cuda_error(e, "scratch status clear");
+        return SINKATTN_ERR_CUDA;
+    }
     rc = sinkattn_decode(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, desc,
                          scratch, kScratchBytes, stream);
     if (rc) return rc;
-    if (status &&
-        cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-        return SINKATTN_ERR_CUDA;
+    if (status) {
+        e = cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) {
+            sinkattn::record_cuda_error(e, "status copy");
+            return SINKATTN_ERR_CUDA;
+        }
+    }
     return SINKATTN_OK;
 }

@@ -7,6 +7,10 @@
 
 namespace sinkattn {
 
+// Remember the CUDA error behind a SINKATTN_ERR_CUDA return and the call that
+// produced it (per host thread).
+void record_cuda_error(cudaError_t e, const char *where);
+
 constexpr int kPageSize = 16;
 constexpr uint32_t kStatusBytes = 256;  // workspace header holding the status word
 

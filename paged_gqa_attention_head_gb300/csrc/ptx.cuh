@@ -144,6 +144,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Sum of the two bf16 halves of a packed pair, as float (exact).
+__device__ __forceinline__ float bf16x2_sum(uint32_t v) {
+    return __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -36,6 +36,7 @@ _DP = ctypes.POINTER(PagedDesc)
 SIGNATURES = {
     "sinkattn_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sinkattn_version": (ctypes.c_int, []),
+    "sinkattn_last_cuda_error": (ctypes.c_char_p, []),
     "sinkattn_decode_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
     "sinkattn_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "sinkattn_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
@@ -55,7 +56,10 @@ _lib = None
 class SinkAttnError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {error_string(code)} ({code})")
+        detail = ""
+        if code == ERR_CUDA:
+            detail = f" [{load().sinkattn_last_cuda_error().decode()}]"
+        super().__init__(f"{what}: {error_string(code)} ({code}){detail}")
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:

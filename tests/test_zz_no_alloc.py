@@ -30,7 +30,7 @@ def _noalloc(sa, d, scale, status):
         q.data_ptr(), d["kp"].data_ptr(), d["vp"].data_ptr(), d["bt"].data_ptr(),
         d["sl"].data_ptr(), None if sk is None else sk.data_ptr(), ctypes.c_float(scale),
         out.data_ptr(), lse.data_ptr(), ctypes.byref(desc), status.data_ptr(), stream)
-    assert rc == 0, sa.error_string(rc)
+    assert rc == 0, f"{sa.error_string(rc)} [{sa.load().sinkattn_last_cuda_error().decode()}]"
     return out, lse
 
 
