@@ -11,21 +11,27 @@
 // HND pages).  Query t of request i sits at absolute position P_i + t and sees
 // every prefix key and new keys 0..t.
 //
-// GB300 design.  One CTA computes a 128-row query tile of one head against all
-// the key tiles it may see (prefix tiles first, then the causal new-token tiles
-// up to the diagonal; fully masked tiles are never visited):
-//   warp 0      TMA producer: the Q tile once, K and V tiles into a ring of
-//               stages (new tokens: one 3-D box of 128 rows; prefix: eight 16-row
-//               page boxes through the block table, with a ragged or invalid page
-//               copied by the warp and zero-filled)
-//   warp 1      allocates TMEM; one thread issues S = Q K^T (M=128, N=128) into
-//               one of two TMEM S buffers, then O += P V (M=128, N=D) into TMEM
-//   warps 2..5  softmax: each thread owns one query row; reads its S row from
-//               TMEM, masks, keeps the running max (rescaling O in TMEM only when
-//               the max grows by more than 2^8), writes P into shared memory
-//               as two bf16 tiles P_hi + P_lo (128-byte swizzled, the MMA's
-//               K-major A layout); O += P_hi V + P_lo V keeps ~16 bits of P
-// S for tile j+1 is computed while the softmax works on tile j.
+// GB300 design.  A persistent grid (one CTA per SM) walks work items, heaviest
+// first.  An item is one 128-row query block of one request for TWO query heads
+// of the same KV head (tiles A and B), so every K/V tile in shared memory feeds
+// two S = Q K^T products and the two softmax warpgroups run side by side while
+// the tensor core alternates between them.  Key tiles: prefix tiles first, then
+// the causal new-token tiles up to the diagonal; fully masked tiles are skipped.
+//   warp 0      TMA producer: both Q tiles of an item, K and V tiles into a ring
+//               of stages (new tokens: one 3-D box of 128 rows; prefix: 16-row page
+//               boxes through the block table; a ragged or invalid page is copied
+//               by the warp and zero-filled)
+//   warp 1      owns TMEM; one thread issues S_x = Q_x K^T (M=128, N=128) and
+//               O_x += P_x V (M=128, N=D, P read from TMEM)
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one query row per
+//               thread; pass 1 reads the S row from TMEM for its max, pass 2 reads it
+//               again, forms P = exp2(s - m) and writes it back over S as two bf16
+//               halves P_hi + P_lo (bf16 P alone, relative 2^-9, is too coarse for
+//               rows with few keys); O is rescaled in TMEM only when the running
+//               max grows by more than 2^8.
+// TMEM columns per tile x: S/P at [256x, 256x + 128), O at [256x + 128, 256x + 128 + D).
+// MMAs issued by one thread complete in order, so when S_x(j) is complete the
+// P.V of tile j - 1 has landed in O_x and P_x(j - 1) has been consumed.
 #include <float.h>
 
 #include "internal.h"
@@ -40,32 +46,31 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
 constexpr int kBM = 128;                   // query rows per tile
 constexpr int kBN = 128;                   // keys per tile
-constexpr int kThreads = 192;              // 6 warps
+constexpr int kThreads = 320;              // 10 warps
 constexpr uint32_t kTmemCols = 512;
+constexpr int kLocateMax = 1024;  // requests / levels of the shared-memory tile lookup
 
 template <int D>
 struct PrefillCfg {
-    static constexpr int kHalves = D / 64;                 // 128-byte column blocks
-    static constexpr int kStages = 2;                      // K/V ring depth
-    static constexpr int kPBufs = D == 64 ? 2 : 1;         // P buffers (hi + lo each)
-    static constexpr int kQBytes = kBM * D * 2;
-    static constexpr int kKVBytes = kBN * D * 2;           // one K (or V) tile
-    static constexpr int kPHalf = kBM * kBN * 2;           // P_hi or P_lo of one tile
-    static constexpr int kPBytes = 2 * kPHalf;             // P_hi then P_lo
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kHalves = D / 64;           // 128-byte column blocks
+    static constexpr int kStages = D == 64 ? 4 : 2;  // K/V ring depth
+    static constexpr int kQBytes = kBM * D * 2;      // one Q tile
+    static constexpr int kKVBytes = kBN * D * 2;     // one K (or V) tile
+    static constexpr int kOffQ = 0;                  // Q tiles A and B
+    static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
-    static constexpr int kNumBars = 1 + 3 * kStages + 4 + 2 * kPBufs + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr int kNumBars = 2 + 3 * kStages + 8 + 1;
+    static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
+    static constexpr int kOffMisc = kOffLoc + 3 * kLocateMax * 4;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 64;
-    static constexpr uint32_t kColS = 0;      // two S buffers: columns [0,128), [128,256)
-    static constexpr uint32_t kColO = 256;    // O: columns [256, 256 + D)
+    static constexpr uint32_t kColSP(int x) { return 256u * x; }
+    static constexpr uint32_t kColO(int x) { return 256u * x + 128u; }
 };
 
 struct Bars {
-    uint64_t *q_full, *k_full, *v_full, *kv_empty, *s_full, *s_free, *p_full, *p_empty, *drain;
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *kv_empty, *s_full, *p_full, *pv_done, *o_free,
+        *drain;
 };
 
 // Bounded wait that also gives up as soon as another role has given up.
@@ -90,28 +95,136 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Which (request, query block) this CTA works on: query blocks are ranked by
-// their index inside the request, largest first (they see the most key tiles),
-// so the longest work starts first.  Returns false if the rank is past the end.
-__device__ bool locate_tile(const PrefillArgs &a, int rank, int *req, int *qb) {
-    int maxnq = 0;
-    for (int i = 0; i < a.n; ++i) {
+// Work list.  Query blocks are ordered by their index inside the request (the
+// number of causal key tiles they see), largest first, then by request, then by
+// head (pair); items are dealt round-robin to the persistent CTAs.  Set-up, once
+// per CTA: s_nq[i] = query blocks of request i; s_cnt[lev] = requests with more
+// than lev query blocks; s_cum[lev] = query blocks at levels above lev.
+struct WorkList {
+    const int *nq, *cnt, *cum;
+    int n, levels, tiles, heads_per_item, groups;  // groups = items per query block
+    bool fast;
+};
+
+__device__ void worklist_setup(const PrefillArgs &a, int *s_nq, int *s_cnt, int *s_cum, int *s_misc,
+                               WorkList *wl) {
+    const int tid = threadIdx.x;
+    const bool fast = a.n <= kLocateMax;
+    if (tid == 0) s_misc[0] = 0;
+    __syncthreads();
+    int mx = 0;
+    for (int i = tid; i < a.n; i += blockDim.x) {
         const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-        maxnq = max(maxnq, (L + kBM - 1) / kBM);
+        const int q = L > 0 ? (L + kBM - 1) / kBM : 0;
+        if (fast) s_nq[i] = q;
+        mx = max(mx, q);
     }
-    for (int lev = maxnq - 1; lev >= 0; --lev)
-        for (int i = 0; i < a.n; ++i) {
-            const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-            if ((L + kBM - 1) / kBM > lev) {
-                if (rank == 0) {
-                    *req = i;
-                    *qb = lev;
-                    return true;
-                }
-                --rank;
+    atomicMax(&s_misc[0], mx);
+    __syncthreads();
+    const int levels = s_misc[0];
+    const bool fast_lv = fast && levels <= kLocateMax;
+    if (fast_lv)
+        for (int lev = tid; lev < levels; lev += blockDim.x) {
+            int c = 0;
+            for (int i = 0; i < a.n; ++i) c += s_nq[i] > lev;
+            s_cnt[lev] = c;
+        }
+    __syncthreads();
+    if (tid == 0) {
+        int tiles = 0;
+        if (fast_lv) {
+            for (int lev = levels - 1; lev >= 0; --lev) {
+                s_cum[lev] = tiles;
+                tiles += s_cnt[lev];
+            }
+        } else {
+            for (int i = 0; i < a.n; ++i) {
+                const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
+                tiles += L > 0 ? (L + kBM - 1) / kBM : 0;
             }
         }
-    return false;
+        s_misc[1] = tiles;
+    }
+    __syncthreads();
+    wl->nq = s_nq;
+    wl->cnt = s_cnt;
+    wl->cum = s_cum;
+    wl->n = a.n;
+    wl->levels = levels;
+    wl->tiles = s_misc[1];
+    wl->heads_per_item = a.G >= 2 ? 2 : 1;
+    wl->groups = a.Hq / wl->heads_per_item;
+    wl->fast = fast_lv;
+}
+
+struct Item {
+    int req, qb, h0;
+};
+
+// Item of a given rank (any thread; reads the set-up tables).
+__device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
+    Item it;
+    const int tr = rank / wl.groups;
+    it.h0 = (rank % wl.groups) * wl.heads_per_item;
+    it.req = 0;
+    it.qb = 0;
+    if (wl.fast) {
+        // the level holding tile rank tr: cum[lev] <= tr < cum[lev] + cnt[lev]; cum
+        // decreases as lev grows, so this is the smallest lev with cum[lev] <= tr
+        int lo = 0, hi = wl.levels - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (wl.cum[mid] <= tr)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        int k = tr - wl.cum[lo];
+        for (int i = 0; i < wl.n; ++i)
+            if (wl.nq[i] > lo && k-- == 0) {
+                it.req = i;
+                break;
+            }
+        it.qb = lo;
+        return it;
+    }
+    // slow path: walk levels from the top over global memory
+    int mq = 0;
+    for (int i = 0; i < a.n; ++i) {
+        const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
+        mq = max(mq, L > 0 ? (L + kBM - 1) / kBM : 0);
+    }
+    int r = tr;
+    for (int lev = mq - 1; lev >= 0; --lev)
+        for (int i = 0; i < a.n; ++i) {
+            const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
+            if (L > 0 && (L + kBM - 1) / kBM > lev && r-- == 0) {
+                it.req = i;
+                it.qb = lev;
+                return it;
+            }
+        }
+    return it;
+}
+
+struct ItemGeom {
+    int row0, L, P, n_pre, n_kv, g;
+};
+
+__device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it) {
+    ItemGeom q;
+    q.row0 = a.cu_seqlens[it.req];
+    q.L = a.cu_seqlens[it.req + 1] - q.row0;
+    q.P = 0;
+    if (a.prefix_lens) {
+        q.P = a.prefix_lens[it.req];
+        const int cap = a.max_pages * kPageSize;
+        q.P = q.P < 0 ? 0 : (q.P > cap ? cap : q.P);
+    }
+    q.n_pre = (q.P + kBN - 1) / kBN;
+    q.n_kv = q.n_pre + it.qb + 1;
+    q.g = it.h0 / a.G;
+    return q;
 }
 
 template <int D>
@@ -121,388 +234,422 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vpmap, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     constexpr int NS = C::kStages;
-    constexpr int NP = C::kPBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sK = smem + C::kOffK;
     uint8_t *sV = smem + C::kOffV;
-    uint8_t *sP = smem + C::kOffP;
-    uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *bb = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
     Bars bars;
-    bars.q_full = bar_base;
-    bars.k_full = bar_base + 1;
+    bars.q_full = bb;
+    bars.q_empty = bb + 1;
+    bars.k_full = bb + 2;
     bars.v_full = bars.k_full + NS;
     bars.kv_empty = bars.v_full + NS;
     bars.s_full = bars.kv_empty + NS;
-    bars.s_free = bars.s_full + 2;
-    bars.p_full = bars.s_free + 2;
-    bars.p_empty = bars.p_full + NP;
-    bars.drain = bars.p_empty + NP;
+    bars.p_full = bars.s_full + 2;
+    bars.pv_done = bars.p_full + 2;
+    bars.o_free = bars.pv_done + 2;
+    bars.drain = bars.o_free + 2;
+    int *s_loc = reinterpret_cast<int *>(smem + C::kOffLoc);
     int *misc = reinterpret_cast<int *>(smem + C::kOffMisc);
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);  // misc[0]: TMEM base
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 1;
-    int *s_tile = misc + 2;  // request, query block, valid flag
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % a.Hq;
-    const int rank = blockIdx.x / a.Hq;
+
+    WorkList wl;
+    worklist_setup(a, s_loc, s_loc + kLocateMax, s_loc + 2 * kLocateMax, misc + 4, &wl);
+    const int n_items = wl.tiles * wl.groups;
+    if ((int)blockIdx.x >= n_items) return;  // CTA-uniform, before any allocation
+    const int ntiles = wl.heads_per_item;    // query tiles per item (1 or 2)
 
     if (tid == 0) {
-        int req = 0, qb = 0;
-        const bool ok = locate_tile(a, rank, &req, &qb);
-        s_tile[0] = req;
-        s_tile[1] = qb;
-        s_tile[2] = ok ? 1 : 0;
         *s_abort = 0;
         mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars.s_full[b], 1);
-            mbar_init(&bars.s_free[b], 4);
-        }
-        for (int b = 0; b < NP; ++b) {
-            mbar_init(&bars.p_full[b], 4);
-            mbar_init(&bars.p_empty[b], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars.s_full[x], 1);
+            mbar_init(&bars.p_full[x], 4);
+            mbar_init(&bars.pv_done[x], 1);
+            mbar_init(&bars.o_free[x], 4);
         }
         mbar_init(bars.drain, 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    if (!s_tile[2]) return;  // CTA-uniform: nothing allocated yet
-
-    const int req = s_tile[0], qb = s_tile[1];
-    const int row0 = a.cu_seqlens[req];
-    const int L = a.cu_seqlens[req + 1] - row0;
-    const int g = h / a.G;
-    int P = 0;
-    if (a.prefix_lens) {
-        P = a.prefix_lens[req];
-        const int cap = a.max_pages * kPageSize;
-        if (P < 0 || P > cap) {
-            if (tid == 0) set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
-            P = P < 0 ? 0 : cap;
-        }
-    }
-    const int n_pre = (P + kBN - 1) / kBN;
-    const int n_kv = n_pre + qb + 1;
-
-    if (warp == 1) {
-        tc::alloc(s_tmem, kTmemCols);
-    }
+    if (warp == 1) tc::alloc(s_tmem, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *s_tmem;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ================================================================ producer
         if (lane == 0) {
             tma_prefetch_desc(&qmap);
-            mbar_arrive_expect_tx(bars.q_full, C::kQBytes);
-#pragma unroll
-            for (int x = 0; x < C::kHalves; ++x)
-                tma_load_3d(sQ + x * 16384, &qmap, bars.q_full, x * 64, h, row0 + qb * kBM);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
         }
-        for (int j = 0; j < n_kv; ++j) {
-            const int s = j % NS;
-            if (j >= NS && !wait_or_abort(&bars.kv_empty[s], (uint32_t)(((j / NS) + 1) & 1), s_abort,
-                                          a.status))
-                break;
-            uint8_t *kt = sK + s * C::kKVBytes;
-            uint8_t *vt = sV + s * C::kKVBytes;
-            if (j < n_pre) {
-                // eight pages of 16 tokens; whole valid pages by TMA, the rest by the warp
-                const int pt = j;
-                uint32_t nfull = 0;
-#pragma unroll
-                for (int pp = 0; pp < 8; ++pp) {
-                    const int page = pt * 8 + pp;
-                    const int nrow = min(kPageSize, max(0, P - page * kPageSize));
-                    if (nrow > 0) {
-                        const int pg = a.prefix_block_table[(int64_t)req * a.max_pages + page];
-                        if (pg < 0 || pg >= a.num_pages) {
-                            if (lane == 0) set_status(a.status, SINKATTN_STATUS_BAD_PAGE);
-                        } else if (nrow == kPageSize) {
-                            ++nfull;
-                        }
-                    }
-                }
-                if (lane == 0) {
-                    mbar_expect_tx(&bars.k_full[s], nfull * kPageSize * D * 2);
-                    mbar_expect_tx(&bars.v_full[s], nfull * kPageSize * D * 2);
-                }
-#pragma unroll 1
-                for (int pp = 0; pp < 8; ++pp) {
-                    const int page = pt * 8 + pp;
-                    const int nrow = min(kPageSize, max(0, P - page * kPageSize));
-                    int pg = -1;
-                    if (nrow > 0) {
-                        pg = a.prefix_block_table[(int64_t)req * a.max_pages + page];
-                        if (pg < 0 || pg >= a.num_pages) pg = -1;
-                    }
-                    if (nrow == kPageSize && pg >= 0) {
-                        if (lane == 0) {
-#pragma unroll
-                            for (int x = 0; x < C::kHalves; ++x) {
-                                tma_load_4d(kt + x * 16384 + pp * 2048, &kpmap, &bars.k_full[s], x * 64,
-                                            0, g, pg);
-                                tma_load_4d(vt + x * 16384 + pp * 2048, &vpmap, &bars.v_full[s], x * 64,
-                                            0, g, pg);
-                            }
-                        }
-                    } else {
-                        // ragged or invalid page: copy the valid rows, zero the rest
-                        const int nv = pg >= 0 ? nrow : 0;
-                        const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-                        const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-                        for (int e = lane; e < kPageSize * C::kHalves * 8; e += 32) {
-                            const int slot = e / (C::kHalves * 8);
-                            const int x = (e / 8) % C::kHalves;
-                            const int c = e % 8;
-                            uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-                            if (slot < nv) {
-                                const int64_t off =
-                                    (((int64_t)pg * a.Hkv + g) * kPageSize + slot) * D + x * 64 + c * 8;
-                                kv = *reinterpret_cast<const uint4 *>(kg + off);
-                                vv = *reinterpret_cast<const uint4 *>(vg + off);
-                            }
-                            const uint32_t o = x * 16384 + sw128(pp * kPageSize + slot, c);
-                            *reinterpret_cast<uint4 *>(kt + o) = kv;
-                            *reinterpret_cast<uint4 *>(vt + o) = vv;
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars.k_full[s]);
-                    mbar_arrive(&bars.v_full[s]);
-                }
-            } else if (lane == 0) {
-                const int kt_idx = j - n_pre;
-                mbar_arrive_expect_tx(&bars.k_full[s], C::kKVBytes);
-#pragma unroll
-                for (int x = 0; x < C::kHalves; ++x)
-                    tma_load_3d(kt + x * 16384, &kmap, &bars.k_full[s], x * 64, g, row0 + kt_idx * kBN);
-                mbar_arrive_expect_tx(&bars.v_full[s], C::kKVBytes);
-#pragma unroll
-                for (int x = 0; x < C::kHalves; ++x)
-                    tma_load_3d(vt + x * 16384, &vmap, &bars.v_full[s], x * 64, g, row0 + kt_idx * kBN);
+        int kv = 0;  // key tiles loaded so far (ring position)
+        int k = 0;   // items so far
+        bool ok = true;
+        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
+            const Item it = item_of(a, wl, rank);
+            const ItemGeom gm = geom_of(a, it);
+            if (lane == 0 && a.prefix_lens) {
+                const int Praw = a.prefix_lens[it.req];
+                if (Praw < 0 || Praw > a.max_pages * kPageSize)
+                    set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
             }
-            __syncwarp();
+            // Q tiles of this item, once the previous item's last S products are done
+            if (k > 0 && !wait_or_abort(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bars.q_full, ntiles * C::kQBytes);
+                for (int x = 0; x < ntiles; ++x)
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        tma_load_3d(sQ + x * C::kQBytes + hf * 16384, &qmap, bars.q_full, hf * 64,
+                                    it.h0 + x, gm.row0 + it.qb * kBM);
+            }
+            for (int j = 0; j < gm.n_kv; ++j, ++kv) {
+                const int s = kv % NS, u = kv / NS;
+                if (u > 0 &&
+                    !wait_or_abort(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *kt = sK + s * C::kKVBytes;
+                uint8_t *vt = sV + s * C::kKVBytes;
+                if (j < gm.n_pre) {
+                    // eight pages of 16 tokens; whole valid pages by TMA, the rest by the warp
+                    uint32_t nfull = 0;
+#pragma unroll
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int page = j * 8 + pp;
+                        const int nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
+                        if (nrow > 0) {
+                            const int pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
+                            if (pg < 0 || pg >= a.num_pages) {
+                                if (lane == 0) set_status(a.status, SINKATTN_STATUS_BAD_PAGE);
+                            } else if (nrow == kPageSize) {
+                                ++nfull;
+                            }
+                        }
+                    }
+                    if (lane == 0) {
+                        mbar_expect_tx(&bars.k_full[s], nfull * kPageSize * D * 2);
+                        mbar_expect_tx(&bars.v_full[s], nfull * kPageSize * D * 2);
+                    }
+#pragma unroll 1
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int page = j * 8 + pp;
+                        const int nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
+                        int pg = -1;
+                        if (nrow > 0) {
+                            pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
+                            if (pg < 0 || pg >= a.num_pages) pg = -1;
+                        }
+                        if (nrow == kPageSize && pg >= 0) {
+                            if (lane == 0) {
+#pragma unroll
+                                for (int hf = 0; hf < C::kHalves; ++hf) {
+                                    tma_load_4d(kt + hf * 16384 + pp * 2048, &kpmap, &bars.k_full[s],
+                                                hf * 64, 0, gm.g, pg);
+                                    tma_load_4d(vt + hf * 16384 + pp * 2048, &vpmap, &bars.v_full[s],
+                                                hf * 64, 0, gm.g, pg);
+                                }
+                            }
+                        } else {
+                            // ragged or invalid page: copy the valid rows, zero the rest
+                            const int nv = pg >= 0 ? nrow : 0;
+                            const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
+                            const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+                            for (int e = lane; e < kPageSize * C::kHalves * 8; e += 32) {
+                                const int slot = e / (C::kHalves * 8);
+                                const int hf = (e / 8) % C::kHalves;
+                                const int c = e % 8;
+                                uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
+                                if (slot < nv) {
+                                    const int64_t off =
+                                        (((int64_t)pg * a.Hkv + gm.g) * kPageSize + slot) * D + hf * 64 + c * 8;
+                                    kx = *reinterpret_cast<const uint4 *>(kg + off);
+                                    vx = *reinterpret_cast<const uint4 *>(vg + off);
+                                }
+                                const uint32_t o = hf * 16384 + sw128(pp * kPageSize + slot, c);
+                                *reinterpret_cast<uint4 *>(kt + o) = kx;
+                                *reinterpret_cast<uint4 *>(vt + o) = vx;
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bars.k_full[s]);
+                        mbar_arrive(&bars.v_full[s]);
+                    }
+                } else if (lane == 0) {
+                    const int row = gm.row0 + (j - gm.n_pre) * kBN;
+                    mbar_arrive_expect_tx(&bars.k_full[s], C::kKVBytes);
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        tma_load_3d(kt + hf * 16384, &kmap, &bars.k_full[s], hf * 64, gm.g, row);
+                    mbar_arrive_expect_tx(&bars.v_full[s], C::kKVBytes);
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        tma_load_3d(vt + hf * 16384, &vmap, &bars.v_full[s], hf * 64, gm.g, row);
+                }
+                __syncwarp();
+            }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ================================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, true);
             const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-            const uint32_t p_addr = smem_u32(sP);
-            bool ok = wait_or_abort(bars.q_full, 0, s_abort, a.status);
-            // O += P_hi V + P_lo V: P = P_hi + P_lo carries ~16 bits of each weight
-            auto issue_pv = [&](int j) -> bool {
-                const int pb = j % NP, s = j % NS;
-                if (!wait_or_abort(&bars.p_full[pb], (uint32_t)((j / NP) & 1), s_abort, a.status))
-                    return false;
-                if (!wait_or_abort(&bars.v_full[s], (uint32_t)((j / NS) & 1), s_abort, a.status))
-                    return false;
-                tc::fence_after_sync();
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t adesc = tc::smem_desc_sw128(
-                            p_addr + pb * C::kPBytes + part * C::kPHalf + (kk >> 2) * 16384 + (kk & 3) * 32,
-                            16, 1024);
-                        const uint64_t bdesc =
-                            tc::smem_desc_sw128(v_addr + s * C::kKVBytes + kk * 2048, 16384, 1024);
-                        tc::mma_f16_ss(tmem + C::kColO, adesc, bdesc, idesc_o,
-                                       (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    }
-                tc::commit(&bars.p_empty[pb]);
-                tc::commit(&bars.kv_empty[s]);
-                return true;
-            };
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int b = j & 1, s = j % NS;
-                if (!wait_or_abort(&bars.k_full[s], (uint32_t)((j / NS) & 1), s_abort, a.status)) {
-                    ok = false;
-                    break;
-                }
-                if (j >= 2 &&
-                    !wait_or_abort(&bars.s_free[b], (uint32_t)(((j - 2) >> 1) & 1), s_abort, a.status)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
+            int kv = 0;                   // key tiles consumed so far (ring position)
+            uint32_t tcount[2] = {0, 0};  // tiles processed per query tile x (barrier phases)
+            int k = 0;
+            bool ok = true;
+            auto issue_s = [&](int x, int s) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t adesc = tc::smem_desc_sw128(q_addr + koff, 16, 1024);
-                    const uint64_t bdesc = tc::smem_desc_sw128(k_addr + s * C::kKVBytes + koff, 16, 1024);
-                    tc::mma_f16_ss(tmem + C::kColS + b * kBN, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t adesc = tc::smem_desc_sw128(q_addr + x * C::kQBytes + off, 16, 1024);
+                    const uint64_t bdesc = tc::smem_desc_sw128(k_addr + s * C::kKVBytes + off, 16, 1024);
+                    tc::mma_f16_ss(tmem + C::kColSP(x), adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                tc::commit(&bars.s_full[b]);
-                if (j >= 1 && !issue_pv(j - 1)) {
+                tc::commit(&bars.s_full[x]);
+            };
+            for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
+                const Item it = item_of(a, wl, rank);
+                const ItemGeom gm = geom_of(a, it);
+                if (!wait_or_abort(bars.q_full, (uint32_t)(k & 1), s_abort, a.status)) {
                     ok = false;
                     break;
                 }
-            }
-            if (ok) issue_pv(n_kv - 1);
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // row of the tile this thread owns
-        const int t = qb * kBM + r;         // position among the request's new tokens
-        const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
-        float m_used = sink2;                        // running max, seeded with the sink
-        float l = sink2 == -INFINITY ? 0.f : 1.f;    // running denominator: e^(sink - m) = 1
-        bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int b = j & 1;
-            if (!wait_or_abort(&bars.s_full[b], (uint32_t)((j >> 1) & 1), s_abort, a.status)) {
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            uint32_t sv[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tc::ld_32x32b_x32(trow + C::kColS + b * kBN + c * 32,
-                                  *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-            tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.s_free[b]);
-
-            // visible keys of this tile for this row
-            int ncols;
-            if (j < n_pre)
-                ncols = min(kBN, P - j * kBN);
-            else if (j - n_pre == qb)
-                ncols = r + 1;  // diagonal tile: keys 0..r
-            else
-                ncols = kBN;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c)
-                if (c < ncols) mx = fmaxf(mx, __uint_as_float(sv[c]));
-            const float mt = mx * a.scale_log2;
-            if (j == 0) {
-                const float mn = fmaxf(m_used, mt);
-                l = (m_used == -INFINITY) ? 0.f : l * fast_exp2(m_used - mn);
-                m_used = mn;
-            } else {
-                const bool need = mt > m_used + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float mn = fmaxf(m_used, mt);
-                    const float alpha = need ? fast_exp2(m_used - mn) : 1.f;
-                    if (need) {
-                        l *= alpha;
-                        m_used = mn;
-                    }
-                    // O must hold every P.V issued so far before it is rescaled
-                    if (!wait_or_abort(&bars.p_empty[(j - 1) % NP], (uint32_t)(((j - 1) / NP) & 1),
-                                       s_abort, a.status)) {
+                // first key tile: S for every query tile
+                {
+                    const int s = kv % NS, u = kv / NS;
+                    if (!wait_or_abort(&bars.k_full[s], (uint32_t)(u & 1), s_abort, a.status)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tc::ld_32x32b_x32(trow + C::kColO + c * 32, o);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::st_32x32b_x32(trow + C::kColO + c * 32, o);
-                    }
-                    tc::wait_st();
+                    for (int x = 0; x < ntiles; ++x) issue_s(x, s);
+                    if (gm.n_kv == 1) tc::commit(bars.q_empty);
                 }
+                for (int j = 0; ok && j < gm.n_kv; ++j) {
+                    const int s = (kv + j) % NS, u = (kv + j) / NS;
+                    const int s1 = (kv + j + 1) % NS, u1 = (kv + j + 1) / NS;
+                    if (!wait_or_abort(&bars.v_full[s], (uint32_t)(u & 1), s_abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int x = 0; x < ntiles; ++x) {
+                        if (!wait_or_abort(&bars.p_full[x], tcount[x] & 1, s_abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        ++tcount[x];
+                        if (j == 0 && k > 0 &&
+                            !wait_or_abort(&bars.o_free[x], (uint32_t)((k - 1) & 1), s_abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        // O_x += P_hi V + P_lo V; P chunk c (keys 32c..32c+31): hi in columns
+                        // 32c..32c+15, lo in 32c+16..32c+31 of the tile's S/P region
+#pragma unroll
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < kBN / 16; ++kk) {
+                                const uint32_t acol =
+                                    C::kColSP(x) + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part;
+                                const uint64_t bdesc =
+                                    tc::smem_desc_sw128(v_addr + s * C::kKVBytes + kk * 2048, 16384, 1024);
+                                tc::mma_f16_ts(tmem + C::kColO(x), tmem + acol, bdesc, idesc_o,
+                                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        if (j == gm.n_kv - 1) tc::commit(&bars.pv_done[x]);
+                        if (j + 1 < gm.n_kv) {
+                            if (x == 0 &&
+                                !wait_or_abort(&bars.k_full[s1], (uint32_t)(u1 & 1), s_abort, a.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after_sync();
+                            issue_s(x, s1);
+                            if (j + 1 == gm.n_kv - 1 && x == ntiles - 1) tc::commit(bars.q_empty);
+                        }
+                    }
+                    if (!ok) break;
+                    tc::commit(&bars.kv_empty[s]);
+                }
+                kv += gm.n_kv;
             }
-            const float neg = m_used == -INFINITY ? 0.f : -m_used;
-            const int pb = j % NP;
-            // P buffer pb is free once the P.V of tile j - NP has completed
-            if (j >= NP && !wait_or_abort(&bars.p_empty[pb], (uint32_t)(((j / NP) + 1) & 1), s_abort,
-                                          a.status)) {
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax
+        const int x = (warp - 2) >> 2;  // query tile of this warpgroup
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // tile row of this thread
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tsp = tmem + lane_base + C::kColSP(x);
+        const uint32_t tO = tmem + lane_base + C::kColO(x);
+        uint32_t tcount = 0;
+        int k = 0;
+        bool ok = x < ntiles;
+        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
+            const Item it = item_of(a, wl, rank);
+            const ItemGeom gm = geom_of(a, it);
+            const int h = it.h0 + x;
+            const int t = it.qb * kBM + r;  // position among the request's new tokens
+            const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+            float m_used = sink2;                      // running max, seeded with the sink
+            float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
+            for (int j = 0; j < gm.n_kv; ++j) {
+                if (!wait_or_abort(&bars.s_full[x], tcount & 1, s_abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                ++tcount;
+                tc::fence_after_sync();
+                int ncols;  // keys of this tile the row may see
+                if (j < gm.n_pre)
+                    ncols = min(kBN, gm.P - j * kBN);
+                else if (j - gm.n_pre == it.qb)
+                    ncols = r + 1;  // diagonal tile: keys 0..r
+                else
+                    ncols = kBN;
+                // pass 1: row max
+                float mx8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v0[32], v1[32];
+                    tc::ld_32x32b_x32(tsp + half * 64, v0);
+                    tc::ld_32x32b_x32(tsp + half * 64 + 32, v1);
+                    tc::wait_ld();
+                    const int c0 = half * 64;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float f0 = (c0 + c < ncols) ? __uint_as_float(v0[c]) : -INFINITY;
+                        const float f1 = (c0 + 32 + c < ncols) ? __uint_as_float(v1[c]) : -INFINITY;
+                        mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(f0, f1));
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mt = mx * a.scale_log2;
+                if (j == 0) {
+                    const float mn = fmaxf(m_used, mt);
+                    l = (m_used == -INFINITY) ? 0.f : l * fast_exp2(m_used - mn);
+                    m_used = mn;
+                } else {
+                    const bool need = mt > m_used + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O_x holds every earlier P.V: S_x(j) was issued after them
+                        const float mn = fmaxf(m_used, mt);
+                        const float alpha = need ? fast_exp2(m_used - mn) : 1.f;
+                        if (need) {
+                            l *= alpha;
+                            m_used = mn;
+                        }
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tc::ld_32x32b_x32(tO + c * 32, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tc::st_32x32b_x32(tO + c * 32, o);
+                        }
+                    }
+                }
+                // pass 2: P = exp2(s * scale - m) written over S as bf16 hi / lo halves
+                const float neg = m_used == -INFINITY ? 0.f : -m_used;
+                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ch = 0; ch < kBN / 32; ++ch) {
+                    uint32_t v[32];
+                    tc::ld_32x32b_x32(tsp + ch * 32, v);
+                    tc::wait_ld();
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = ch * 32 + 2 * e;
+                        const float s0 = (c < ncols) ? __uint_as_float(v[2 * e]) : -INFINITY;
+                        const float s1 = (c + 1 < ncols) ? __uint_as_float(v[2 * e + 1]) : -INFINITY;
+                        const float p0 = fast_exp2(fmaf(s0, a.scale_log2, neg));
+                        const float p1 = fast_exp2(fmaf(s1, a.scale_log2, neg));
+                        sum8[(2 * e) & 7] += p0;
+                        sum8[(2 * e + 1) & 7] += p1;
+                        hi[e] = pack_bf16x2(p0, p1);
+                        lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16),
+                                            p1 - __uint_as_float(hi[e] & 0xFFFF0000u));
+                    }
+                    tc::st_32x32b_x16(tsp + ch * 32, hi);
+                    tc::st_32x32b_x16(tsp + ch * 32 + 16, lo);
+                }
+                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full[x]);
+            }
+            if (!ok) break;
+            // epilogue: O / l for this row, once the item's last P.V has landed
+            if (!wait_or_abort(&bars.pv_done[x], (uint32_t)(k & 1), s_abort, a.status)) {
                 ok = false;
                 break;
             }
-            uint8_t *pt = sP + pb * C::kPBytes;
-            float sum = 0.f;
-            // P is written as P_hi = bf16(p) and P_lo = bf16(p - P_hi); the bf16 rounding
-            // of p alone (relative 2^-9) is too coarse for rows with few keys
-#pragma unroll
-            for (int c8 = 0; c8 < kBN / 8; ++c8) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c8 * 8 + 2 * e;
-                    const float p0 =
-                        c < ncols ? fast_exp2(fmaf(__uint_as_float(sv[c]), a.scale_log2, neg)) : 0.f;
-                    const float p1 =
-                        c + 1 < ncols ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, neg)) : 0.f;
-                    sum += p0 + p1;
-                    hi[e] = pack_bf16x2(p0, p1);
-                    lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16),
-                                        p1 - __uint_as_float(hi[e] & 0xFFFF0000u));
-                }
-                const uint32_t o = (c8 >> 3) * 16384 + sw128(r, c8 & 7);
-                *reinterpret_cast<uint4 *>(pt + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(pt + C::kPHalf + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            l += sum;
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.p_full[pb]);
-        }
-        // epilogue: O / l for this row
-        if (ok && wait_or_abort(&bars.p_empty[(n_kv - 1) % NP], (uint32_t)(((n_kv - 1) / NP) & 1),
-                                s_abort, a.status)) {
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool valid = t < L && row0 >= 0 && row0 + t < a.T;
+            const bool valid = t < gm.L && gm.row0 >= 0 && gm.row0 + t < a.T;
             __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) +
-                                ((int64_t)(row0 + t) * a.Hq + h) * D;
+                                ((int64_t)(gm.row0 + t) * a.Hq + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tc::ld_32x32b_x32(trow + C::kColO + c * 32, o);
+                tc::ld_32x32b_x32(tO + c * 32, o);
                 tc::wait_ld();
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(og + c * 32 + e) = v;
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(og + c * 32 + e) = w;
                     }
                 }
             }
             if (valid && a.lse)
-                a.lse[(int64_t)(row0 + t) * a.Hq + h] =
-                    (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+                a.lse[(int64_t)(gm.row0 + t) * a.Hq + h] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.o_free[x]);
         }
     }
 
-    // all roles done: wait for the MMAs still in flight after an abort, then free TMEM
+    // all roles done: after an abort wait for MMAs still in flight, then free TMEM
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
         if (*s_abort && lane == 0) {
-            // a final commit arrives once every MMA issued so far has completed
             tc::commit(bars.drain);
             mbar_wait(bars.drain, 0, 100000000ull);
         }
@@ -525,12 +672,11 @@ cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtens
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    // bound on the number of 128-row query blocks: sum_i ceil(L_i / 128) <= T / 128 + n
-    const int64_t tiles = (int64_t)(a.T + kBM - 1) / kBM + a.n;
-    const int64_t grid = tiles * a.Hq;
-    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-    prefill_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap,
-                                                                           vpmap, a);
+    int device = 0, sms = 0;
+    if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) return e;
+    // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more)
+    prefill_kernel<D><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
     return cudaGetLastError();
 }
 
