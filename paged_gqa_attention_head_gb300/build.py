@@ -20,6 +20,30 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 
 
+# The prefill kernel re-balances registers between warpgroups with setmaxnreg; the
+# split adds up to exactly the registers it is launched with (384 threads x 168), so
+# the build refuses any other register count (a larger split than the launch
+# budget would make setmaxnreg wait forever).
+PREFILL_LAUNCH_REGS = 168
+
+
+def _check_prefill_regs(ptxas_log: str) -> None:
+    fn = None
+    found = 0
+    for line in ptxas_log.splitlines():
+        if "Compiling entry function" in line:
+            fn = line
+        elif "Used" in line and "registers" in line and fn and "prefill_kernel" in fn:
+            regs = int(line.split("Used")[1].split("registers")[0])
+            found += 1
+            if regs != PREFILL_LAUNCH_REGS:
+                raise RuntimeError(f"prefill_kernel uses {regs} registers, expected "
+                                   f"{PREFILL_LAUNCH_REGS} (its setmaxnreg split depends on it)")
+            fn = None
+    if found == 0:
+        raise RuntimeError("ptxas did not report the prefill kernel's registers")
+
+
 def _flags(extra_ptxas_verbose: bool) -> list[str]:
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]
@@ -39,10 +63,13 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     def compile_one(src: str) -> tuple[str, str]:
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [NVCC, "-c", src, "-o", obj] + _flags(verbose)
+        is_prefill = os.path.basename(src) == "prefill.cu"
+        cmd = [NVCC, "-c", src, "-o", obj] + _flags(verbose or is_prefill)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if is_prefill:
+            _check_prefill_regs(r.stderr)
         return obj, r.stderr
 
     with ThreadPoolExecutor(max_workers=len(srcs)) as ex:

@@ -23,12 +23,12 @@
 //               by the warp and zero-filled)
 //   warp 1      owns TMEM; one thread issues S_x = Q_x K^T (M=128, N=128) and
 //               O_x += P_x V (M=128, N=D, P read from TMEM)
-//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one query row per
-//               thread; pass 1 reads the S row from TMEM for its max, pass 2 reads it
-//               again, forms P = exp2(s - m) and writes it back over S as two bf16
-//               halves P_hi + P_lo (bf16 P alone, relative 2^-9, is too coarse for
-//               rows with few keys); O is rescaled in TMEM only when the running
-//               max grows by more than 2^8.
+//   warps 2..3  idle (they complete warpgroup 0, which hands registers to softmax)
+//   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: one query row per
+//               thread; the whole S row is read from TMEM once, P = exp2(s - m) is
+//               written back over S as two bf16 halves P_hi + P_lo (bf16 P alone,
+//               relative 2^-9, is too coarse for rows with few keys); O is rescaled
+//               in TMEM only when the running max grows by more than 2^8.
 // TMEM columns per tile x: S/P at [256x, 256x + 128), O at [256x + 128, 256x + 128 + D).
 // MMAs issued by one thread complete in order, so when S_x(j) is complete the
 // P.V of tile j - 1 has landed in O_x and P_x(j - 1) has been consumed.
@@ -46,7 +46,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
 constexpr int kBM = 128;                   // query rows per tile
 constexpr int kBN = 128;                   // keys per tile
-constexpr int kThreads = 320;              // 10 warps
+constexpr int kThreads = 384;              // 12 warps = 3 warpgroups
+// Register split: the kernel is built for 168 registers per thread (384 x 168 =
+// 64512); warpgroup 0 (producer, MMA, two idle warps) gives up to 72 and the two
+// softmax warpgroups take 216: 128 x 72 + 256 x 216 = 64512.  The build checks
+// that ptxas used exactly 168.
+constexpr uint32_t kRegsLaunch = 168, kRegsSide = 72, kRegsSoftmax = 216;
+static_assert(128 * kRegsSide + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLocateMax = 1024;  // requests / levels of the shared-memory tile lookup
 
@@ -291,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================================================ producer
+        reg_dealloc<kRegsSide>();
         if (lane == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
@@ -412,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
+        reg_dealloc<kRegsSide>();
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, true);
@@ -499,9 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp < 4) {
+        reg_dealloc<kRegsSide>();  // idle warps of warpgroup 0
     } else {
         // ================================================================ softmax
-        const int x = (warp - 2) >> 2;  // query tile of this warpgroup
+        reg_alloc<kRegsSoftmax>();
+        const int x = (warp - 4) >> 2;  // query tile of this warpgroup
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -532,24 +543,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ncols = r + 1;  // diagonal tile: keys 0..r
                 else
                     ncols = kBN;
-                // pass 1: row max
+                // the whole S row of this tile
+                uint32_t sv[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c)
+                    tc::ld_32x32b_x32(tsp + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                tc::wait_ld();
+                if (ncols < kBN) {  // diagonal, ragged or prefix-tail tile: hide invisible keys
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c >= ncols) sv[c] = 0xFF800000u;  // -inf
+                }
                 float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+                for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sv[e]);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v0[32], v1[32];
-                    tc::ld_32x32b_x32(tsp + half * 64, v0);
-                    tc::ld_32x32b_x32(tsp + half * 64 + 32, v1);
-                    tc::wait_ld();
-                    const int c0 = half * 64;
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float f0 = (c0 + c < ncols) ? __uint_as_float(v0[c]) : -INFINITY;
-                        const float f1 = (c0 + 32 + c < ncols) ? __uint_as_float(v1[c]) : -INFINITY;
-                        mx8[c & 7] = fmaxf(mx8[c & 7], fmaxf(f0, f1));
-                    }
-                }
+                for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float mt = mx * a.scale_log2;
@@ -578,27 +587,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // pass 2: P = exp2(s * scale - m) written over S as bf16 hi / lo halves
+                // P = exp2(s * scale - m), written back over S: per 32 keys, 16 columns of
+                // P_hi = P with its low 16 bits cleared, then 16 columns of P_lo = bf16(P - P_hi)
                 const float neg = m_used == -INFINITY ? 0.f : -m_used;
                 float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ch = 0; ch < kBN / 32; ++ch) {
-                    uint32_t v[32];
-                    tc::ld_32x32b_x32(tsp + ch * 32, v);
-                    tc::wait_ld();
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int c = ch * 32 + 2 * e;
-                        const float s0 = (c < ncols) ? __uint_as_float(v[2 * e]) : -INFINITY;
-                        const float s1 = (c + 1 < ncols) ? __uint_as_float(v[2 * e + 1]) : -INFINITY;
-                        const float p0 = fast_exp2(fmaf(s0, a.scale_log2, neg));
-                        const float p1 = fast_exp2(fmaf(s1, a.scale_log2, neg));
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), a.scale_log2, neg));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, neg));
                         sum8[(2 * e) & 7] += p0;
                         sum8[(2 * e + 1) & 7] += p1;
-                        hi[e] = pack_bf16x2(p0, p1);
-                        lo[e] = pack_bf16x2(p0 - __uint_as_float(hi[e] << 16),
-                                            p1 - __uint_as_float(hi[e] & 0xFFFF0000u));
+                        const uint32_t t0 = __float_as_uint(p0) & 0xFFFF0000u;
+                        const uint32_t t1 = __float_as_uint(p1) & 0xFFFF0000u;
+                        hi[e] = (t0 >> 16) | t1;  // exact: both are bf16 values already
+                        lo[e] = pack_bf16x2(p0 - __uint_as_float(t0), p1 - __uint_as_float(t1));
                     }
                     tc::st_32x32b_x16(tsp + ch * 32, hi);
                     tc::st_32x32b_x16(tsp + ch * 32 + 16, lo);

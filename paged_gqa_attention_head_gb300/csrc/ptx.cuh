@@ -144,6 +144,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Re-balance registers between warpgroups (all four warps of a warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Sum of the two bf16 halves of a packed pair, as float (exact).
 __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
     return __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
