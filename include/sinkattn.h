@@ -67,6 +67,7 @@ typedef enum sinkattn_error {
 #define SINKATTN_STATUS_BAD_LENGTH 0x2u     /* a length < 0 or > max_pages_per_seq * page_size */
 #define SINKATTN_STATUS_BAD_CU_SEQLENS 0x4u /* cu_seqlens not non-decreasing from 0 to total */
 #define SINKATTN_STATUS_WAIT_TIMEOUT 0x8u   /* a pipeline wait hit its iteration limit */
+#define SINKATTN_STATUS_VALUE_RANGE 0x10u   /* prefill: a V value with |v| >= 2^22 or not finite */
 
 /* Shapes of a paged KV cache and of the heads that read it. */
 typedef struct sinkattn_paged_desc {
@@ -186,7 +187,10 @@ int sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pa
  * absolute position prefix_len_i + t and attends every prefix token plus new tokens
  * 0..t of the same request (causal mask of gptoss.md section 3, aligned to the end).
  * QK^T and PV run on the tcgen05 tensor cores with TMEM accumulators; the online
- * softmax's running max and denominator start from the sink.
+ * softmax's running max and denominator start from the sink.  The P.V product takes
+ * P and V in fp16 (11-bit significand, fp32 accumulation): each V tile is scaled by a
+ * power of two into fp16 range, which covers |v| < 2^22; larger or non-finite values
+ * set SINKATTN_STATUS_VALUE_RANGE (their outputs are then unspecified).
  *
  * q:          bf16 [T, Hq, D]   (T = total_tokens = cu_seqlens[num_seqs])
  * k, v:       bf16 [T, Hkv, D]  (the new tokens' keys and values)

@@ -23,15 +23,17 @@
 //               by the warp and zero-filled)
 //   warp 1      owns TMEM; one thread issues S_x = Q_x K^T (M=128, N=128) and
 //               O_x += P_x V (M=128, N=D, P read from TMEM)
-//   warps 2..3  idle (they complete warpgroup 0, which hands registers to softmax)
+//   warps 2..3  convert each V tile in shared memory from bf16 to fp16, scaled by a
+//               power of two 2^-k that keeps it in fp16 range (k = 0 unless |v| >= 2^15)
 //   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: one query row per
-//               thread; the whole S row is read from TMEM once, P = exp2(s - m) is
-//               written back over S as two bf16 halves P_hi + P_lo (bf16 P alone,
-//               relative 2^-9, is too coarse for rows with few keys); O is rescaled
-//               in TMEM only when the running max grows by more than 2^8.
-// TMEM columns per tile x: S/P at [256x, 256x + 128), O at [256x + 128, 256x + 128 + D).
-// MMAs issued by one thread complete in order, so when S_x(j) is complete the
-// P.V of tile j - 1 has landed in O_x and P_x(j - 1) has been consumed.
+//               thread; the whole S row is read from TMEM once, and P = exp2(s - m) * 2^k
+//               is written back over S in fp16 (bf16 P, relative 2^-9, is too coarse for
+//               rows with few keys; fp16 keeps 2^-12); O is rescaled in TMEM only when
+//               the running max grows by more than 2^8.
+// TMEM columns: NB S/P buffers of 128 columns (3 at head_dim 64, 2 at 128) rotate over
+// the S products of both tiles, then O_A and O_B (D columns each).  MMAs issued by
+// one thread execute in order, so the S product issued right after a P.V may reuse
+// that P.V's buffer; with three buffers S runs up to three products ahead.
 #include <float.h>
 
 #include "internal.h"
@@ -48,7 +50,7 @@ constexpr int kBM = 128;                   // query rows per tile
 constexpr int kBN = 128;                   // keys per tile
 constexpr int kThreads = 384;              // 12 warps = 3 warpgroups
 // Register split: the kernel is built for 168 registers per thread (384 x 168 =
-// 64512); warpgroup 0 (producer, MMA, two idle warps) gives up to 72 and the two
+// 64512); warpgroup 0 (producer, MMA, two converter warps) gives up to 72 and the two
 // softmax warpgroups take 216: 128 x 72 + 256 x 216 = 64512.  The build checks
 // that ptxas used exactly 168.
 constexpr uint32_t kRegsLaunch = 168, kRegsSide = 72, kRegsSoftmax = 216;
@@ -66,17 +68,19 @@ struct PrefillCfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-    static constexpr int kNumBars = 2 + 3 * kStages + 8 + 1;
+    static constexpr int kSPBufs = D == 64 ? 3 : 2;  // S/P buffers rotating over the tiles
+    static constexpr int kNumBars = 2 + 4 * kStages + 3 * kSPBufs + 2 + 1;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 3 * kLocateMax * 4;
-    static constexpr int kSmemBytes = 1024 + kOffMisc + 64;
-    static constexpr uint32_t kColSP(int x) { return 256u * x; }
-    static constexpr uint32_t kColO(int x) { return 256u * x + 128u; }
+    static constexpr int kSmemBytes = 1024 + kOffMisc + 128;
+    __host__ __device__ static constexpr uint32_t kColSP(int b) { return 128u * b; }
+    __host__ __device__ static constexpr uint32_t kColO(int x) { return 128u * kSPBufs + D * x; }
+    static_assert(128 * kSPBufs + 2 * D <= 512, "TMEM columns");
 };
 
 struct Bars {
-    uint64_t *q_full, *q_empty, *k_full, *v_full, *kv_empty, *s_full, *p_full, *pv_done, *o_free,
-        *drain;
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *kv_empty, *s_full, *p_full, *pv_done,
+        *o_free, *drain;
 };
 
 // Bounded wait that also gives up as soon as another role has given up.
@@ -240,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vpmap, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     constexpr int NS = C::kStages;
+    constexpr int NB = C::kSPBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -252,16 +257,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.q_empty = bb + 1;
     bars.k_full = bb + 2;
     bars.v_full = bars.k_full + NS;
-    bars.kv_empty = bars.v_full + NS;
-    bars.s_full = bars.kv_empty + NS;
-    bars.p_full = bars.s_full + 2;
-    bars.pv_done = bars.p_full + 2;
-    bars.o_free = bars.pv_done + 2;
+    bars.v_conv = bars.v_full + NS;     // [NS] the stage's V tile is in fp16
+    bars.kv_empty = bars.v_conv + NS;
+    // Every wait below is for the next completion of its barrier or the one before,
+    // never older: a parity wait cannot tell phases two apart.
+    bars.s_full = bars.kv_empty + NS;      // [NB] per S/P buffer: its S product is done
+    bars.p_full = bars.s_full + NB;        // [NB] per S/P buffer: its P is written
+    bars.pv_done = bars.p_full + NB;       // [NB] per S/P buffer: the P.V reading it is done
+    bars.o_free = bars.pv_done + NB;       // [2] per query tile: O was read (once per item)
     bars.drain = bars.o_free + 2;
     int *s_loc = reinterpret_cast<int *>(smem + C::kOffLoc);
     int *misc = reinterpret_cast<int *>(smem + C::kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 1;
+    int *s_vscale = misc + 16;                                 // [NS] exponent k of each V tile
+    uint32_t *s_vred = reinterpret_cast<uint32_t *>(misc + 24);  // [2] converter max per warp
+    volatile int *s_vok = misc + 26;                             // [2] converter go / stop
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -278,14 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.v_conv[s], 2);
             mbar_init(&bars.kv_empty[s], 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&bars.s_full[x], 1);
-            mbar_init(&bars.p_full[x], 4);
-            mbar_init(&bars.pv_done[x], 1);
-            mbar_init(&bars.o_free[x], 4);
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(&bars.s_full[b], 1);
+            mbar_init(&bars.p_full[b], 4);
+            mbar_init(&bars.pv_done[b], 1);
         }
+        for (int x = 0; x < 2; ++x) mbar_init(&bars.o_free[x], 4);
         mbar_init(bars.drain, 1);
         fence_mbar_init();
     }
@@ -420,95 +432,171 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         reg_dealloc<kRegsSide>();
-        if (lane == 0) {
+        {
+            // The whole warp runs this loop (waits, cursors and descriptors stay warp-
+            // uniform); one elected lane issues each group of MMAs and its commits.
+            // S products are numbered i = 0, 1, ... over the CTA's lifetime (key tile by key
+            // tile, query tile x = i % ntiles); S(i) goes to S/P buffer i % NB.  S(i + NB) is
+            // issued right after P.V(i), which read the same buffer: MMAs issued by one
+            // thread execute in order, so the buffer is free by then, and the softmax finds
+            // up to NB S tiles computed ahead.
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, true);
-            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-            int kv = 0;                   // key tiles consumed so far (ring position)
-            uint32_t tcount[2] = {0, 0};  // tiles processed per query tile x (barrier phases)
-            int k = 0;
-            bool ok = true;
-            auto issue_s = [&](int x, int s) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t adesc = tc::smem_desc_sw128(q_addr + x * C::kQBytes + off, 16, 1024);
-                    const uint64_t bdesc = tc::smem_desc_sw128(k_addr + s * C::kKVBytes + off, 16, 1024);
-                    tc::mma_f16_ss(tmem + C::kColSP(x), adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&bars.s_full[x]);
+            constexpr uint32_t idesc_o = tc::idesc_f16_f32(kBM, D, true);
+            // Descriptors are built once; an operand at byte offset `off` inside a tile
+            // only moves the start-address field (bits 0..13, address >> 4), which
+            // cannot overflow because every shared address is below 2^18.
+            const uint64_t dq = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv = tc::smem_desc_sw128(smem_u32(sV), 16384, 1024);
+            struct Cursor {
+                int rank, k, j, x, kv, n_kv;  // item rank / count, key tile, query tile, ring pos
             };
-            for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
-                const Item it = item_of(a, wl, rank);
-                const ItemGeom gm = geom_of(a, it);
-                if (!wait_or_abort(bars.q_full, (uint32_t)(k & 1), s_abort, a.status)) {
-                    ok = false;
-                    break;
-                }
-                // first key tile: S for every query tile
-                {
-                    const int s = kv % NS, u = kv / NS;
-                    if (!wait_or_abort(&bars.k_full[s], (uint32_t)(u & 1), s_abort, a.status)) {
-                        ok = false;
-                        break;
+            auto start_item = [&](Cursor &c) {
+                if (c.rank < n_items) c.n_kv = geom_of(a, item_of(a, wl, c.rank)).n_kv;
+            };
+            auto advance = [&](Cursor &c) {
+                if (++c.x == ntiles) {
+                    c.x = 0;
+                    ++c.kv;
+                    if (++c.j == c.n_kv) {
+                        c.j = 0;
+                        ++c.k;
+                        c.rank += gridDim.x;
+                        start_item(c);
                     }
+                }
+            };
+            Cursor cs = {(int)blockIdx.x, 0, 0, 0, 0, 0}, cp = cs;
+            start_item(cs);
+            start_item(cp);
+            uint32_t i_s = 0, i_p = 0;
+            bool ok = true;
+            // all lanes wait; the outcome is made warp-uniform so that no lane is left
+            // behind at the elect.sync below when a wait gives up
+            auto warp_wait = [&](uint64_t *bar, uint32_t parity, volatile int *ab, uint32_t *st) {
+                return __all_sync(0xffffffffu, wait_or_abort(bar, parity, ab, st));
+            };
+            auto issue_s = [&]() -> bool {
+                if (cs.j == 0 && cs.x == 0 &&
+                    !warp_wait(bars.q_full, (uint32_t)(cs.k & 1), s_abort, a.status))
+                    return false;
+                const int st = cs.kv % NS;
+                if (cs.x == 0 &&
+                    !warp_wait(&bars.k_full[st], (uint32_t)((cs.kv / NS) & 1), s_abort, a.status))
+                    return false;
+                const int b = i_s % NB;
+                const uint64_t q0 = dq + (uint64_t)((cs.x * C::kQBytes) >> 4);
+                const uint64_t k0 = dk + (uint64_t)((st * C::kKVBytes) >> 4);
+                const bool last = cs.j == cs.n_kv - 1 && cs.x == ntiles - 1;
+                if (elect_one()) {
                     tc::fence_after_sync();
-                    for (int x = 0; x < ntiles; ++x) issue_s(x, s);
-                    if (gm.n_kv == 1) tc::commit(bars.q_empty);
-                }
-                for (int j = 0; ok && j < gm.n_kv; ++j) {
-                    const int s = (kv + j) % NS, u = (kv + j) / NS;
-                    const int s1 = (kv + j + 1) % NS, u1 = (kv + j + 1) / NS;
-                    if (!wait_or_abort(&bars.v_full[s], (uint32_t)(u & 1), s_abort, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    for (int x = 0; x < ntiles; ++x) {
-                        if (!wait_or_abort(&bars.p_full[x], tcount[x] & 1, s_abort, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        ++tcount[x];
-                        if (j == 0 && k > 0 &&
-                            !wait_or_abort(&bars.o_free[x], (uint32_t)((k - 1) & 1), s_abort, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::fence_after_sync();
-                        // O_x += P_hi V + P_lo V; P chunk c (keys 32c..32c+31): hi in columns
-                        // 32c..32c+15, lo in 32c+16..32c+31 of the tile's S/P region
 #pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < kBN / 16; ++kk) {
-                                const uint32_t acol =
-                                    C::kColSP(x) + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * part;
-                                const uint64_t bdesc =
-                                    tc::smem_desc_sw128(v_addr + s * C::kKVBytes + kk * 2048, 16384, 1024);
-                                tc::mma_f16_ts(tmem + C::kColO(x), tmem + acol, bdesc, idesc_o,
-                                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                            }
-                        if (j == gm.n_kv - 1) tc::commit(&bars.pv_done[x]);
-                        if (j + 1 < gm.n_kv) {
-                            if (x == 0 &&
-                                !wait_or_abort(&bars.k_full[s1], (uint32_t)(u1 & 1), s_abort, a.status)) {
-                                ok = false;
-                                break;
-                            }
-                            tc::fence_after_sync();
-                            issue_s(x, s1);
-                            if (j + 1 == gm.n_kv - 1 && x == ntiles - 1) tc::commit(bars.q_empty);
-                        }
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        tc::mma_f16_ss(tmem + C::kColSP(b), q0 + off, k0 + off, idesc_s, kk > 0 ? 1u : 0u);
                     }
-                    if (!ok) break;
-                    tc::commit(&bars.kv_empty[s]);
+                    tc::commit(&bars.s_full[b]);
+                    if (last) tc::commit(bars.q_empty);  // the item's Q tiles are no longer read
                 }
-                kv += gm.n_kv;
+                __syncwarp();
+                ++i_s;
+                advance(cs);
+                return true;
+            };
+            auto issue_pv = [&]() -> bool {
+                const int b = i_p % NB, x = cp.x, st = cp.kv % NS;
+                if (!warp_wait(&bars.p_full[b], (uint32_t)((i_p / NB) & 1), s_abort, a.status))
+                    return false;
+                if (cp.j == 0 && cp.k > 0 &&
+                    !warp_wait(&bars.o_free[x], (uint32_t)((cp.k - 1) & 1), s_abort, a.status))
+                    return false;
+                if (x == 0 &&
+                    !warp_wait(&bars.v_conv[st], (uint32_t)((cp.kv / NS) & 1), s_abort, a.status))
+                    return false;
+                // O_x += P V in fp16: P (keys 2c, 2c + 1 in column c) in the first 64
+                // columns of the S/P buffer, V scaled into fp16 by the converter warps
+                const uint64_t v0 = dv + (uint64_t)((st * C::kKVBytes) >> 4);
+                const uint32_t tp = tmem + C::kColSP(b), to = tmem + C::kColO(x);
+                const uint32_t acc0 = cp.j > 0 ? 1u : 0u;
+                if (elect_one()) {
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        tc::mma_f16_ts(to, tp + 8 * kk, v0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                       kk > 0 ? 1u : acc0);
+                    tc::commit(&bars.pv_done[b]);
+                    if (x == ntiles - 1) tc::commit(&bars.kv_empty[st]);
+                }
+                __syncwarp();
+                ++i_p;
+                advance(cp);
+                return true;
+            };
+            while (ok && i_s < (uint32_t)NB && cs.rank < n_items) ok = issue_s();
+            while (ok && cp.rank < n_items) {
+                ok = issue_pv();
+                if (ok && cs.rank < n_items) ok = issue_s();
             }
         }
         __syncwarp();
     } else if (warp < 4) {
-        reg_dealloc<kRegsSide>();  // idle warps of warpgroup 0
+        // ================================================================ V converter
+        reg_dealloc<kRegsSide>();
+        // V tile, bf16 -> fp16 scaled by 2^-k, in place; k = max(0, e - 14) where 2^e <=
+        // max|v| < 2^(e+1), so the tile stays below 2^15 and P * 2^k below 2^15 (k <= 7)
+        const int ct = tid - 64;  // 0..63
+        constexpr int kVec = C::kKVBytes / 16;
+        int kv = 0;
+        bool ok = true;
+        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x) {
+            const ItemGeom gm = geom_of(a, item_of(a, wl, rank));
+            for (int j = 0; j < gm.n_kv; ++j, ++kv) {
+                const int st = kv % NS;
+                // both converter warps must take the same path through the named barriers
+                // below: they agree on a snapshot of (wait succeeded, no abort) first
+                bool good = wait_or_abort(&bars.v_full[st], (uint32_t)((kv / NS) & 1), s_abort, a.status);
+                good = __all_sync(0xffffffffu, good) && *s_abort == 0;
+                if (lane == 0) s_vok[warp - 2] = good ? 1 : 0;
+                asm volatile("bar.sync 1, 64;" ::: "memory");
+                if (!(s_vok[0] && s_vok[1])) {
+                    ok = false;
+                    break;
+                }
+                uint4 *vt = reinterpret_cast<uint4 *>(sV + st * C::kKVBytes);
+                uint32_t mx = 0;  // largest |v| as bf16 bits (monotonic for |v|)
+                for (int e = ct; e < kVec; e += 64) {
+                    const uint4 w = vt[e];
+                    const uint32_t q0 = max(w.x & 0x7FFFu, (w.x >> 16) & 0x7FFFu);
+                    const uint32_t q1 = max(w.y & 0x7FFFu, (w.y >> 16) & 0x7FFFu);
+                    const uint32_t q2 = max(w.z & 0x7FFFu, (w.z >> 16) & 0x7FFFu);
+                    const uint32_t q3 = max(w.w & 0x7FFFu, (w.w >> 16) & 0x7FFFu);
+                    mx = max(mx, max(max(q0, q1), max(q2, q3)));
+                }
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                if (lane == 0) s_vred[warp - 2] = mx;
+                asm volatile("bar.sync 1, 64;" ::: "memory");
+                mx = max(s_vred[0], s_vred[1]);
+                asm volatile("bar.sync 1, 64;" ::: "memory");
+                int kexp = max(0, (int)(mx >> 7) - 127 - 14);
+                if (mx >= 0x7F80u || kexp > 7) {
+                    if (ct == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
+                    kexp = min(kexp, 7);
+                }
+                const float sc = __uint_as_float((uint32_t)(127 - kexp) << 23);  // 2^-k
+                for (int e = ct; e < kVec; e += 64) {
+                    uint4 w = vt[e];
+                    w.x = pack_f16x2(__uint_as_float(w.x << 16) * sc, __uint_as_float(w.x & 0xFFFF0000u) * sc);
+                    w.y = pack_f16x2(__uint_as_float(w.y << 16) * sc, __uint_as_float(w.y & 0xFFFF0000u) * sc);
+                    w.z = pack_f16x2(__uint_as_float(w.z << 16) * sc, __uint_as_float(w.z & 0xFFFF0000u) * sc);
+                    w.w = pack_f16x2(__uint_as_float(w.w << 16) * sc, __uint_as_float(w.w & 0xFFFF0000u) * sc);
+                    vt[e] = w;
+                }
+                if (ct == 0) s_vscale[st] = kexp;
+                fence_proxy_async_smem();  // the P.V MMA reads these through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.v_conv[st]);
+            }
+        }
     } else {
         // ================================================================ softmax
         reg_alloc<kRegsSoftmax>();
@@ -516,9 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // tile row of this thread
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tsp = tmem + lane_base + C::kColSP(x);
         const uint32_t tO = tmem + lane_base + C::kColO(x);
-        uint32_t tcount = 0;
+        uint32_t tcount = 0;  // key tiles this query tile has processed (over all items)
         int k = 0;
         bool ok = x < ntiles;
         for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
@@ -530,7 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = sink2;                      // running max, seeded with the sink
             float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
             for (int j = 0; j < gm.n_kv; ++j) {
-                if (!wait_or_abort(&bars.s_full[x], tcount & 1, s_abort, a.status)) {
+                const uint32_t i = tcount * ntiles + x;  // number of this S product
+                const int b = i % NB;
+                const uint32_t tsp = tmem + lane_base + C::kColSP(b);
+                if (!wait_or_abort(&bars.s_full[b], (i / NB) & 1, s_abort, a.status)) {
                     ok = false;
                     break;
                 }
@@ -569,7 +659,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     const bool need = mt > m_used + kRescaleThreshold;
                     if (__any_sync(0xffffffffu, need)) {
-                        // O_x holds every earlier P.V: S_x(j) was issued after them
+                        // O_x must hold the P.V of this query tile's previous key tile,
+                        // S product i - ntiles (its buffer's previous use is long done)
+                        const uint32_t ip = i - ntiles;
+                        if (!wait_or_abort(&bars.pv_done[ip % NB], (ip / NB) & 1, s_abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
                         const float mn = fmaxf(m_used, mt);
                         const float alpha = need ? fast_exp2(m_used - mn) : 1.f;
                         if (need) {
@@ -587,13 +684,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // P = exp2(s * scale - m), written back over S: per 32 keys, 16 columns of
-                // P_hi = P with its low 16 bits cleared, then 16 columns of P_lo = bf16(P - P_hi)
-                const float neg = m_used == -INFINITY ? 0.f : -m_used;
+                // P * 2^k = exp2(s * scale - m + k) in fp16 over the first 64 columns of the
+                // buffer (keys 2c, 2c + 1 in column c); 2^-k is the V tile's scale
+                const int vst = (tcount - 1) % NS;
+                if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const int kexp = s_vscale[vst];
+                const float neg = (m_used == -INFINITY ? 0.f : -m_used) + (float)kexp;
                 float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ch = 0; ch < kBN / 32; ++ch) {
-                    uint32_t hi[16], lo[16];
+                    uint32_t pp[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int c = ch * 32 + 2 * e;
@@ -601,23 +704,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, neg));
                         sum8[(2 * e) & 7] += p0;
                         sum8[(2 * e + 1) & 7] += p1;
-                        const uint32_t t0 = __float_as_uint(p0) & 0xFFFF0000u;
-                        const uint32_t t1 = __float_as_uint(p1) & 0xFFFF0000u;
-                        hi[e] = (t0 >> 16) | t1;  // exact: both are bf16 values already
-                        lo[e] = pack_bf16x2(p0 - __uint_as_float(t0), p1 - __uint_as_float(t1));
+                        pp[e] = pack_f16x2(p0, p1);
                     }
-                    tc::st_32x32b_x16(tsp + ch * 32, hi);
-                    tc::st_32x32b_x16(tsp + ch * 32 + 16, lo);
+                    tc::st_32x32b_x16(tsp + ch * 16, pp);
                 }
-                l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
+                     __uint_as_float((uint32_t)(127 - kexp) << 23);
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p_full[x]);
+                if (lane == 0) mbar_arrive(&bars.p_full[b]);
             }
             if (!ok) break;
             // epilogue: O / l for this row, once the item's last P.V has landed
-            if (!wait_or_abort(&bars.pv_done[x], (uint32_t)(k & 1), s_abort, a.status)) {
+            const uint32_t il = (tcount - 1) * ntiles + x;  // S product of the last key tile
+            if (!wait_or_abort(&bars.pv_done[il % NB], (il / NB) & 1, s_abort, a.status)) {
                 ok = false;
                 break;
             }

@@ -144,6 +144,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// One lane of a converged warp is elected (true there, false elsewhere).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Re-balance registers between warpgroups (all four warps of a warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void reg_alloc() {
@@ -157,6 +168,12 @@ __device__ __forceinline__ void reg_dealloc() {
 // Sum of the two bf16 halves of a packed pair, as float (exact).
 __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
     return __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -286,6 +303,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Same for fp16 A and B (A and B of one kind::f16 MMA always share their type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4)                         // D format: f32
+           | (0u << 7)                       // A format: f16
+           | (0u << 10)                      // B format: f16
+           | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
+           | ((uint32_t)(N >> 3) << 17)      // N / 8
+           | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator,

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
 STATUS_BAD_PAGE, STATUS_BAD_LENGTH, STATUS_BAD_CU_SEQLENS, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
+STATUS_VALUE_RANGE = 16
 PAGE_SIZE = 16
 
 # every symbol the header declares, with (restype, argtypes)
