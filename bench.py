@@ -60,7 +60,7 @@ def traffic_for(kernel: str, sources: list[str]):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel)
-    if not d or d.get("source_sha") != file_sha(*sources):
+    if not d or d.get("source_sha") != file_sha(*d.get("source_files", sources)):
         return None
     return d.get("bytes_per_launch")
 
@@ -248,8 +248,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": round(ach, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "traffic": traffic_for("decode_splitkv_kernel",
-                                            ["paged_gqa_attention_head_gb300/csrc/decode.cu"]),
+                     "traffic": traffic_for("decode_splitkv_kernel", []),
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "kernel_ms": round(split_ms, 5)},
         "clocks": clocks,
@@ -324,7 +323,8 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
         tf = p.flops() / (ms * 1e-3) / 1e12
         rows[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
                       "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": p.flops(),
-                      "peak_source": f"{peak_src} bf16_tflops"}
+                      "peak_source": f"{peak_src} bf16_tflops (burst)",
+                      "traffic": traffic_for("prefill_kernel", []) if name == "gptoss_prefill" else None}
     return rows
 
 
