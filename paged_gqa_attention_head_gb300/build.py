@@ -24,7 +24,7 @@ NVCC = os.environ.get("NVCC", "nvcc")
 # split adds up to exactly the registers it is launched with (384 threads x 168), so
 # the build refuses any other register count (a larger split than the launch
 # budget would make setmaxnreg wait forever).
-PREFILL_LAUNCH_REGS = 168
+PREFILL_LAUNCH_REGS = 128
 
 
 def _check_prefill_regs(ptxas_log: str) -> None:

@@ -21,19 +21,22 @@
 //               of stages (new tokens: one 3-D box of 128 rows; prefix: 16-row page
 //               boxes through the block table; a ragged or invalid page is copied
 //               by the warp and zero-filled)
-//   warp 1      owns TMEM; one thread issues S_x = Q_x K^T (M=128, N=128) and
-//               O_x += P_x V (M=128, N=D, P read from TMEM)
-//   warps 2..3  convert each V tile in shared memory from bf16 to fp16, scaled by a
-//               power of two 2^-k that keeps it in fp16 range (k = 0 unless |v| >= 2^15)
+//   warp 1      owns TMEM; issues O_x += P_x V (M=128, N=D, P read from TMEM, fp16)
+//   warp 2      issues S_x = Q_x K^T (M=128, N=128, bf16) into the next free S/P buffer
+//   warp 3      idle
 //   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B: one query row per
 //               thread; the whole S row is read from TMEM once, and P = exp2(s - m) * 2^k
 //               is written back over S in fp16 (bf16 P, relative 2^-9, is too coarse for
 //               rows with few keys; fp16 keeps 2^-12); O is rescaled in TMEM only when
 //               the running max grows by more than 2^8.
+//   warps 12..15 convert each V tile in shared memory from bf16 to fp16, one 32-key
+//               quarter per warp (one warp per SM sub-partition), each quarter scaled by
+//               its own power of two 2^-k that keeps it in fp16 range (k = 0 unless
+//               |v| >= 2^15); the softmax multiplies P by 2^k over the same 32 keys.
 // TMEM columns: NB S/P buffers of 128 columns (3 at head_dim 64, 2 at 128) rotate over
-// the S products of both tiles, then O_A and O_B (D columns each).  MMAs issued by
-// one thread execute in order, so the S product issued right after a P.V may reuse
-// that P.V's buffer; with three buffers S runs up to three products ahead.
+// the S products of both tiles, then O_A and O_B (D columns each).  S product i goes to
+// buffer i % NB once the P.V of product i - NB (which read that buffer) has completed,
+// so S runs up to NB products ahead of the softmax.
 #include <float.h>
 
 #include "internal.h"
@@ -48,13 +51,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
 constexpr int kBM = 128;                   // query rows per tile
 constexpr int kBN = 128;                   // keys per tile
-constexpr int kThreads = 384;              // 12 warps = 3 warpgroups
-// Register split: the kernel is built for 168 registers per thread (384 x 168 =
-// 64512); warpgroup 0 (producer, MMA, two converter warps) gives up to 72 and the two
-// softmax warpgroups take 216: 128 x 72 + 256 x 216 = 64512.  The build checks
-// that ptxas used exactly 168.
-constexpr uint32_t kRegsLaunch = 168, kRegsSide = 72, kRegsSoftmax = 216;
-static_assert(128 * kRegsSide + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+constexpr int kThreads = 512;              // 16 warps = 4 warpgroups
+// Register split: the kernel is built for 128 registers per thread (512 x 128 =
+// 65536); warpgroup 0 (producer, MMA issuers) drops to 48, warpgroup 3 (V converters)
+// to 32, and the two softmax warpgroups take 216: 128 x 48 + 128 x 32 + 256 x 216 =
+// 65536.  The build checks that ptxas used exactly 128.
+constexpr uint32_t kRegsLaunch = 128, kRegsSide = 48, kRegsConvert = 32, kRegsSoftmax = 216;
+static_assert(128 * kRegsSide + 128 * kRegsConvert + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLocateMax = 1024;  // requests / levels of the shared-memory tile lookup
 
@@ -72,7 +76,7 @@ struct PrefillCfg {
     static constexpr int kNumBars = 2 + 4 * kStages + 3 * kSPBufs + 2 + 1;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 3 * kLocateMax * 4;
-    static constexpr int kSmemBytes = 1024 + kOffMisc + 128;
+    static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
     __host__ __device__ static constexpr uint32_t kColSP(int b) { return 128u * b; }
     __host__ __device__ static constexpr uint32_t kColO(int x) { return 128u * kSPBufs + D * x; }
     static_assert(128 * kSPBufs + 2 * D <= 512, "TMEM columns");
@@ -270,9 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *misc = reinterpret_cast<int *>(smem + C::kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 1;
-    int *s_vscale = misc + 16;                                 // [NS] exponent k of each V tile
-    uint32_t *s_vred = reinterpret_cast<uint32_t *>(misc + 24);  // [2] converter max per warp
-    volatile int *s_vok = misc + 26;                             // [2] converter go / stop
+    int *s_vscale = misc + 32;  // [NS][4] exponent k of each 32-key quarter of each V tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.v_conv[s], 2);
+            mbar_init(&bars.v_conv[s], 4);  // one arrive per converter warp
             mbar_init(&bars.kv_empty[s], 1);
         }
         for (int b = 0; b < NB; ++b) {
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.pv_done[b], 1);
         }
         for (int x = 0; x < 2; ++x) mbar_init(&bars.o_free[x], 4);
-        mbar_init(bars.drain, 1);
+        mbar_init(bars.drain, 2);  // one commit from each MMA-issuing warp
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(s_tmem, kTmemCols);
@@ -341,6 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int s = kv % NS, u = kv / NS;
+                // prefix tile: lane p < 8 looks up page 8j + p (issued before the wait below so
+                // the load overlaps it); nrow = its valid rows, pg = -1 for a missing page
+                int nrow = 0, pg = -1;
+                if (j < gm.n_pre && lane < 8) {
+                    const int page = j * 8 + lane;
+                    nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
+                    if (nrow > 0) {
+                        pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
+                        if (pg < 0 || pg >= a.num_pages) {
+                            set_status(a.status, SINKATTN_STATUS_BAD_PAGE);
+                            pg = -1;
+                        }
+                    }
+                }
                 if (u > 0 &&
                     !wait_or_abort(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status)) {
                     ok = false;
@@ -349,64 +365,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *kt = sK + s * C::kKVBytes;
                 uint8_t *vt = sV + s * C::kKVBytes;
                 if (j < gm.n_pre) {
-                    // eight pages of 16 tokens; whole valid pages by TMA, the rest by the warp
-                    uint32_t nfull = 0;
-#pragma unroll
-                    for (int pp = 0; pp < 8; ++pp) {
-                        const int page = j * 8 + pp;
-                        const int nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
-                        if (nrow > 0) {
-                            const int pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
-                            if (pg < 0 || pg >= a.num_pages) {
-                                if (lane == 0) set_status(a.status, SINKATTN_STATUS_BAD_PAGE);
-                            } else if (nrow == kPageSize) {
-                                ++nfull;
-                            }
-                        }
-                    }
+                    // eight pages of 16 tokens: each whole valid page by a TMA issued from its
+                    // own lane, the others (ragged tail, missing page) by the warp
+                    const bool full = nrow == kPageSize && pg >= 0;
+                    const uint32_t full_mask = __ballot_sync(0xffffffffu, full);
+                    const uint32_t other_mask = __ballot_sync(0xffffffffu, lane < 8 && !full);
                     if (lane == 0) {
-                        mbar_expect_tx(&bars.k_full[s], nfull * kPageSize * D * 2);
-                        mbar_expect_tx(&bars.v_full[s], nfull * kPageSize * D * 2);
+                        const uint32_t bytes = (uint32_t)__popc(full_mask) * kPageSize * D * 2;
+                        mbar_expect_tx(&bars.k_full[s], bytes);
+                        mbar_expect_tx(&bars.v_full[s], bytes);
                     }
-#pragma unroll 1
-                    for (int pp = 0; pp < 8; ++pp) {
-                        const int page = j * 8 + pp;
-                        const int nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
-                        int pg = -1;
-                        if (nrow > 0) {
-                            pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
-                            if (pg < 0 || pg >= a.num_pages) pg = -1;
-                        }
-                        if (nrow == kPageSize && pg >= 0) {
-                            if (lane == 0) {
+                    if (full) {
 #pragma unroll
-                                for (int hf = 0; hf < C::kHalves; ++hf) {
-                                    tma_load_4d(kt + hf * 16384 + pp * 2048, &kpmap, &bars.k_full[s],
-                                                hf * 64, 0, gm.g, pg);
-                                    tma_load_4d(vt + hf * 16384 + pp * 2048, &vpmap, &bars.v_full[s],
-                                                hf * 64, 0, gm.g, pg);
-                                }
+                        for (int hf = 0; hf < C::kHalves; ++hf) {
+                            tma_load_4d(kt + hf * 16384 + lane * 2048, &kpmap, &bars.k_full[s], hf * 64, 0,
+                                        gm.g, pg);
+                            tma_load_4d(vt + hf * 16384 + lane * 2048, &vpmap, &bars.v_full[s], hf * 64, 0,
+                                        gm.g, pg);
+                        }
+                    }
+                    for (uint32_t om = other_mask; om; om &= om - 1) {
+                        // copy the valid rows of page pp (none if missing), zero the rest
+                        const int pp = __ffs(om) - 1;
+                        const int pgp = __shfl_sync(0xffffffffu, pg, pp);
+                        const int nv = pgp >= 0 ? __shfl_sync(0xffffffffu, nrow, pp) : 0;
+                        const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
+                        const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+                        for (int e = lane; e < kPageSize * C::kHalves * 8; e += 32) {
+                            const int slot = e / (C::kHalves * 8);
+                            const int hf = (e / 8) % C::kHalves;
+                            const int c = e % 8;
+                            uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
+                            if (slot < nv) {
+                                const int64_t off =
+                                    (((int64_t)pgp * a.Hkv + gm.g) * kPageSize + slot) * D + hf * 64 + c * 8;
+                                kx = *reinterpret_cast<const uint4 *>(kg + off);
+                                vx = *reinterpret_cast<const uint4 *>(vg + off);
                             }
-                        } else {
-                            // ragged or invalid page: copy the valid rows, zero the rest
-                            const int nv = pg >= 0 ? nrow : 0;
-                            const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-                            const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-                            for (int e = lane; e < kPageSize * C::kHalves * 8; e += 32) {
-                                const int slot = e / (C::kHalves * 8);
-                                const int hf = (e / 8) % C::kHalves;
-                                const int c = e % 8;
-                                uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
-                                if (slot < nv) {
-                                    const int64_t off =
-                                        (((int64_t)pg * a.Hkv + gm.g) * kPageSize + slot) * D + hf * 64 + c * 8;
-                                    kx = *reinterpret_cast<const uint4 *>(kg + off);
-                                    vx = *reinterpret_cast<const uint4 *>(vg + off);
-                                }
-                                const uint32_t o = hf * 16384 + sw128(pp * kPageSize + slot, c);
-                                *reinterpret_cast<uint4 *>(kt + o) = kx;
-                                *reinterpret_cast<uint4 *>(vt + o) = vx;
-                            }
+                            const uint32_t o = hf * 16384 + sw128(pp * kPageSize + slot, c);
+                            *reinterpret_cast<uint4 *>(kt + o) = kx;
+                            *reinterpret_cast<uint4 *>(vt + o) = vx;
                         }
                     }
                     fence_proxy_async_smem();
@@ -429,65 +427,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ================================================================ MMA issuers
         reg_dealloc<kRegsSide>();
-        {
-            // The whole warp runs this loop (waits, cursors and descriptors stay warp-
-            // uniform); one elected lane issues each group of MMAs and its commits.
-            // S products are numbered i = 0, 1, ... over the CTA's lifetime (key tile by key
-            // tile, query tile x = i % ntiles); S(i) goes to S/P buffer i % NB.  S(i + NB) is
-            // issued right after P.V(i), which read the same buffer: MMAs issued by one
-            // thread execute in order, so the buffer is free by then, and the softmax finds
-            // up to NB S tiles computed ahead.
-            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
-            constexpr uint32_t idesc_o = tc::idesc_f16_f32(kBM, D, true);
-            // Descriptors are built once; an operand at byte offset `off` inside a tile
-            // only moves the start-address field (bits 0..13, address >> 4), which
-            // cannot overflow because every shared address is below 2^18.
-            const uint64_t dq = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dk = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
-            const uint64_t dv = tc::smem_desc_sw128(smem_u32(sV), 16384, 1024);
-            struct Cursor {
-                int rank, k, j, x, kv, n_kv;  // item rank / count, key tile, query tile, ring pos
-            };
-            auto start_item = [&](Cursor &c) {
-                if (c.rank < n_items) c.n_kv = geom_of(a, item_of(a, wl, c.rank)).n_kv;
-            };
-            auto advance = [&](Cursor &c) {
-                if (++c.x == ntiles) {
-                    c.x = 0;
-                    ++c.kv;
-                    if (++c.j == c.n_kv) {
-                        c.j = 0;
-                        ++c.k;
-                        c.rank += gridDim.x;
-                        start_item(c);
-                    }
+        // Warp 1 issues the P.V products, warp 2 the S products; each runs its loop warp-
+        // uniformly and one elected lane issues each MMA group.  S products are numbered
+        // i = 0, 1, ... over the CTA's lifetime (key tile by key tile, query tile x = i %
+        // ntiles); S(i) goes to S/P buffer i % NB.
+        const bool pv_role = warp == 1;
+        constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
+        constexpr uint32_t idesc_o = tc::idesc_f16_f32(kBM, D, true);
+        // Descriptors are built once; an operand at byte offset `off` inside a tile only
+        // moves the start-address field (bits 0..13, address >> 4), which cannot overflow
+        // because every shared address is below 2^18.
+        const uint64_t dq = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dv = tc::smem_desc_sw128(smem_u32(sV), 16384, 1024);
+        // all lanes wait; the outcome is made warp-uniform so that no lane is left behind
+        // at the elect.sync below when a wait gives up
+        auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort, a.status));
+        };
+        int rank = blockIdx.x, k = 0, j = 0, x = 0, kv = 0;
+        int n_kv = rank < n_items ? geom_of(a, item_of(a, wl, rank)).n_kv : 0;
+        uint32_t i = 0;
+        int b = 0;           // i % NB
+        uint32_t use = 0;    // i / NB
+        bool ok = true;
+        while (ok && rank < n_items) {
+            const int st = kv % NS;
+            const uint32_t sp = (uint32_t)((kv / NS) & 1);
+            if (pv_role) {
+                // O_x += P V in fp16: P (keys 2c, 2c + 1 in column c) in the first 64 columns
+                // of the S/P buffer, V scaled into fp16 by the converter warp
+                if (!warp_wait(&bars.p_full[b], use & 1)) break;
+                if (j == 0 && k > 0 && !warp_wait(&bars.o_free[x], (uint32_t)((k - 1) & 1))) break;
+                if (x == 0 && !warp_wait(&bars.v_conv[st], sp)) break;
+                const uint64_t v0 = dv + (uint64_t)((st * C::kKVBytes) >> 4);
+                const uint32_t tp = tmem + C::kColSP(b), to = tmem + C::kColO(x);
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+                if (elect_one()) {
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        tc::mma_f16_ts(to, tp + 8 * kk, v0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                       kk > 0 ? 1u : acc0);
+                    tc::commit(&bars.pv_done[b]);
+                    if (x == ntiles - 1) tc::commit(&bars.kv_empty[st]);
                 }
-            };
-            Cursor cs = {(int)blockIdx.x, 0, 0, 0, 0, 0}, cp = cs;
-            start_item(cs);
-            start_item(cp);
-            uint32_t i_s = 0, i_p = 0;
-            bool ok = true;
-            // all lanes wait; the outcome is made warp-uniform so that no lane is left
-            // behind at the elect.sync below when a wait gives up
-            auto warp_wait = [&](uint64_t *bar, uint32_t parity, volatile int *ab, uint32_t *st) {
-                return __all_sync(0xffffffffu, wait_or_abort(bar, parity, ab, st));
-            };
-            auto issue_s = [&]() -> bool {
-                if (cs.j == 0 && cs.x == 0 &&
-                    !warp_wait(bars.q_full, (uint32_t)(cs.k & 1), s_abort, a.status))
-                    return false;
-                const int st = cs.kv % NS;
-                if (cs.x == 0 &&
-                    !warp_wait(&bars.k_full[st], (uint32_t)((cs.kv / NS) & 1), s_abort, a.status))
-                    return false;
-                const int b = i_s % NB;
-                const uint64_t q0 = dq + (uint64_t)((cs.x * C::kQBytes) >> 4);
+                __syncwarp();
+            } else {
+                // buffer b is free once the P.V of product i - NB has completed
+                if (use > 0 && !warp_wait(&bars.pv_done[b], (use - 1) & 1)) break;
+                if (j == 0 && x == 0 && !warp_wait(bars.q_full, (uint32_t)(k & 1))) break;
+                if (x == 0 && !warp_wait(&bars.k_full[st], sp)) break;
+                const uint64_t q0 = dq + (uint64_t)((x * C::kQBytes) >> 4);
                 const uint64_t k0 = dk + (uint64_t)((st * C::kKVBytes) >> 4);
-                const bool last = cs.j == cs.n_kv - 1 && cs.x == ntiles - 1;
+                const bool last = j == n_kv - 1 && x == ntiles - 1;
                 if (elect_one()) {
                     tc::fence_after_sync();
 #pragma unroll
@@ -499,99 +495,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (last) tc::commit(bars.q_empty);  // the item's Q tiles are no longer read
                 }
                 __syncwarp();
-                ++i_s;
-                advance(cs);
-                return true;
-            };
-            auto issue_pv = [&]() -> bool {
-                const int b = i_p % NB, x = cp.x, st = cp.kv % NS;
-                if (!warp_wait(&bars.p_full[b], (uint32_t)((i_p / NB) & 1), s_abort, a.status))
-                    return false;
-                if (cp.j == 0 && cp.k > 0 &&
-                    !warp_wait(&bars.o_free[x], (uint32_t)((cp.k - 1) & 1), s_abort, a.status))
-                    return false;
-                if (x == 0 &&
-                    !warp_wait(&bars.v_conv[st], (uint32_t)((cp.kv / NS) & 1), s_abort, a.status))
-                    return false;
-                // O_x += P V in fp16: P (keys 2c, 2c + 1 in column c) in the first 64
-                // columns of the S/P buffer, V scaled into fp16 by the converter warps
-                const uint64_t v0 = dv + (uint64_t)((st * C::kKVBytes) >> 4);
-                const uint32_t tp = tmem + C::kColSP(b), to = tmem + C::kColO(x);
-                const uint32_t acc0 = cp.j > 0 ? 1u : 0u;
-                if (elect_one()) {
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        tc::mma_f16_ts(to, tp + 8 * kk, v0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                       kk > 0 ? 1u : acc0);
-                    tc::commit(&bars.pv_done[b]);
-                    if (x == ntiles - 1) tc::commit(&bars.kv_empty[st]);
-                }
-                __syncwarp();
-                ++i_p;
-                advance(cp);
-                return true;
-            };
-            while (ok && i_s < (uint32_t)NB && cs.rank < n_items) ok = issue_s();
-            while (ok && cp.rank < n_items) {
-                ok = issue_pv();
-                if (ok && cs.rank < n_items) ok = issue_s();
             }
+            // next product
+            ++i;
+            if (++b == NB) {
+                b = 0;
+                ++use;
+            }
+            if (++x == ntiles) {
+                x = 0;
+                ++kv;
+                if (++j == n_kv) {
+                    j = 0;
+                    ++k;
+                    rank += gridDim.x;
+                    if (rank < n_items) n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
+                }
+            }
+            continue;
         }
-        __syncwarp();
-    } else if (warp < 4) {
-        // ================================================================ V converter
+        ok = false;
+        (void)ok;
+    } else if (warp == 3) {
         reg_dealloc<kRegsSide>();
-        // V tile, bf16 -> fp16 scaled by 2^-k, in place; k = max(0, e - 14) where 2^e <=
-        // max|v| < 2^(e+1), so the tile stays below 2^15 and P * 2^k below 2^15 (k <= 7)
-        const int ct = tid - 64;  // 0..63
-        constexpr int kVec = C::kKVBytes / 16;
+    } else if (warp >= 12) {
+        // ================================================================ V converters
+        reg_dealloc<kRegsConvert>();
+        // Keys 32q..32q+31 of the V tile, bf16 -> fp16 scaled by 2^-k, in place;
+        // k = max(0, e - 14) where 2^e <= max|v| < 2^(e+1) over the quarter, so the
+        // quarter stays below 2^15 and P * 2^k below 2^15 (k <= 7).  The quarter is
+        // 32 rows x 128 bytes of each 64-column half of the tile.
+        const int q = warp - 12;
         int kv = 0;
         bool ok = true;
         for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x) {
-            const ItemGeom gm = geom_of(a, item_of(a, wl, rank));
-            for (int j = 0; j < gm.n_kv; ++j, ++kv) {
+            const int n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
+            for (int j = 0; j < n_kv; ++j, ++kv) {
                 const int st = kv % NS;
-                // both converter warps must take the same path through the named barriers
-                // below: they agree on a snapshot of (wait succeeded, no abort) first
-                bool good = wait_or_abort(&bars.v_full[st], (uint32_t)((kv / NS) & 1), s_abort, a.status);
-                good = __all_sync(0xffffffffu, good) && *s_abort == 0;
-                if (lane == 0) s_vok[warp - 2] = good ? 1 : 0;
-                asm volatile("bar.sync 1, 64;" ::: "memory");
-                if (!(s_vok[0] && s_vok[1])) {
+                if (!__all_sync(0xffffffffu, wait_or_abort(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
+                                                            s_abort, a.status))) {
                     ok = false;
                     break;
                 }
-                uint4 *vt = reinterpret_cast<uint4 *>(sV + st * C::kKVBytes);
-                uint32_t mx = 0;  // largest |v| as bf16 bits (monotonic for |v|)
-                for (int e = ct; e < kVec; e += 64) {
-                    const uint4 w = vt[e];
-                    const uint32_t q0 = max(w.x & 0x7FFFu, (w.x >> 16) & 0x7FFFu);
-                    const uint32_t q1 = max(w.y & 0x7FFFu, (w.y >> 16) & 0x7FFFu);
-                    const uint32_t q2 = max(w.z & 0x7FFFu, (w.z >> 16) & 0x7FFFu);
-                    const uint32_t q3 = max(w.w & 0x7FFFu, (w.w >> 16) & 0x7FFFu);
-                    mx = max(mx, max(max(q0, q1), max(q2, q3)));
+                uint4 *vt = reinterpret_cast<uint4 *>(sV + st * C::kKVBytes + q * 4096) + lane;
+                // this lane's vectors: 8 per 64-column half, 512 bytes apart
+                uint32_t mx = 0;  // largest |v| per 16-bit half, as bf16 bits (monotonic in |v|)
+#pragma unroll 1
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint4 w = vt[hf * 1024 + e * 32];
+                        mx = __vmaxu2(mx, w.x & 0x7FFF7FFFu);
+                        mx = __vmaxu2(mx, w.y & 0x7FFF7FFFu);
+                        mx = __vmaxu2(mx, w.z & 0x7FFF7FFFu);
+                        mx = __vmaxu2(mx, w.w & 0x7FFF7FFFu);
+                    }
                 }
-                mx = __reduce_max_sync(0xffffffffu, mx);
-                if (lane == 0) s_vred[warp - 2] = mx;
-                asm volatile("bar.sync 1, 64;" ::: "memory");
-                mx = max(s_vred[0], s_vred[1]);
-                asm volatile("bar.sync 1, 64;" ::: "memory");
+                mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
                 int kexp = max(0, (int)(mx >> 7) - 127 - 14);
                 if (mx >= 0x7F80u || kexp > 7) {
-                    if (ct == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
+                    if (lane == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
                     kexp = min(kexp, 7);
                 }
                 const float sc = __uint_as_float((uint32_t)(127 - kexp) << 23);  // 2^-k
-                for (int e = ct; e < kVec; e += 64) {
-                    uint4 w = vt[e];
-                    w.x = pack_f16x2(__uint_as_float(w.x << 16) * sc, __uint_as_float(w.x & 0xFFFF0000u) * sc);
-                    w.y = pack_f16x2(__uint_as_float(w.y << 16) * sc, __uint_as_float(w.y & 0xFFFF0000u) * sc);
-                    w.z = pack_f16x2(__uint_as_float(w.z << 16) * sc, __uint_as_float(w.z & 0xFFFF0000u) * sc);
-                    w.w = pack_f16x2(__uint_as_float(w.w << 16) * sc, __uint_as_float(w.w & 0xFFFF0000u) * sc);
-                    vt[e] = w;
+#pragma unroll 1
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    if (kexp == 0) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            uint4 *pw = vt + hf * 1024 + e * 32;
+                            uint4 w = *pw;
+                            w.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+                            w.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+                            w.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+                            w.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+                            *pw = w;
+                        }
+                    } else {
+#pragma unroll 2
+                        for (int e = 0; e < 8; ++e) {
+                            uint4 *pw = vt + hf * 1024 + e * 32;
+                            uint4 w = *pw;
+                            w.x = pack_f16x2(__uint_as_float(w.x << 16) * sc, __uint_as_float(w.x & 0xFFFF0000u) * sc);
+                            w.y = pack_f16x2(__uint_as_float(w.y << 16) * sc, __uint_as_float(w.y & 0xFFFF0000u) * sc);
+                            w.z = pack_f16x2(__uint_as_float(w.z << 16) * sc, __uint_as_float(w.z & 0xFFFF0000u) * sc);
+                            w.w = pack_f16x2(__uint_as_float(w.w << 16) * sc, __uint_as_float(w.w & 0xFFFF0000u) * sc);
+                            *pw = w;
+                        }
+                    }
                 }
-                if (ct == 0) s_vscale[st] = kexp;
+                if (lane == 0) s_vscale[st * 4 + q] = kexp;
                 fence_proxy_async_smem();  // the P.V MMA reads these through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.v_conv[st]);
@@ -685,17 +678,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // P * 2^k = exp2(s * scale - m + k) in fp16 over the first 64 columns of the
-                // buffer (keys 2c, 2c + 1 in column c); 2^-k is the V tile's scale
+                // buffer (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter
+                // holding keys 32ch..32ch+31
                 const int vst = (tcount - 1) % NS;
                 if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status)) {
                     ok = false;
                     break;
                 }
-                const int kexp = s_vscale[vst];
-                const float neg = (m_used == -INFINITY ? 0.f : -m_used) + (float)kexp;
+                const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
+                const bool k_uniform = kq.x == kq.y && kq.y == kq.z && kq.z == kq.w;  // warp-uniform
+                const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
                 float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ch = 0; ch < kBN / 32; ++ch) {
+                    const int kc = ch == 0 ? kq.x : ch == 1 ? kq.y : ch == 2 ? kq.z : kq.w;
+                    const float neg = neg0 + (float)kc;
                     uint32_t pp[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -707,9 +704,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pp[e] = pack_f16x2(p0, p1);
                     }
                     tc::st_32x32b_x16(tsp + ch * 16, pp);
+                    if (!k_uniform) {  // quarters scaled differently: fold this chunk into l now
+                        l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
+                             __uint_as_float((uint32_t)(127 - kc) << 23);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+                    }
                 }
-                l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
-                     __uint_as_float((uint32_t)(127 - kexp) << 23);
+                if (k_uniform)
+                    l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
+                         __uint_as_float((uint32_t)(127 - kq.x) << 23);
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
@@ -755,12 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all roles done: after an abort wait for MMAs still in flight, then free TMEM
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
-        if (*s_abort && lane == 0) {
+    if ((warp == 1 || warp == 2) && *s_abort) {
+        // a commit arrives once every MMA this warp issued has completed
+        if (lane == 0) {
             tc::commit(bars.drain);
             mbar_wait(bars.drain, 0, 100000000ull);
         }
         __syncwarp();
+    }
+    if (*s_abort) __syncthreads();
+    if (warp == 1) {
         tc::fence_after_sync();
         tc::dealloc(tmem, kTmemCols);
     }
