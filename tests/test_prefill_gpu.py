@@ -105,6 +105,63 @@ def test_prefill_row_equals_decode(sa, cuda_dev):
     check_lse(dlse, lse[ts].double().cpu().numpy())
 
 
+def _large_rows(n, lo_exp, seed):
+    """n x D-independent positive bf16 magnitudes in [2^lo_exp, 2^(lo_exp + 1))."""
+    g = torch.Generator().manual_seed(seed)
+    return (2.0 ** lo_exp) * (1.0 + torch.rand(n, generator=g))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_v_quarters_with_different_scales(sa, oracle_mod, cuda_dev, D):
+    """V rows at key positions 32..63 of each 128-key tile in [2^17, 2^18) and 96..127 in
+    [2^20, 2^21): the kernel scales those 32-key quarters into fp16 range with different
+    powers of two (k = 3 and 6) and the other quarters not at all.  No status is raised
+    below 2^22."""
+    p = inputs.make_prefill([300, 129, 64], 8, 2, D, seed=40 + D, sinks=True)
+    cu = p.cu_seqlens.tolist()
+    for i in range(len(cu) - 1):
+        for t in range(cu[i], cu[i + 1]):
+            pos = (t - cu[i]) % 128
+            if 32 <= pos < 64:
+                p.v[t] = _large_rows(D, 17, t).to(torch.bfloat16).expand(p.v.shape[1], D)
+            elif pos >= 96:
+                p.v[t] = _large_rows(D, 20, t).to(torch.bfloat16).expand(p.v.shape[1], D)
+    ws = sa.workspace(0, cuda_dev, "prefill")
+    sa.get_status(ws)
+    out, lse = run_prefill(sa, p, cuda_dev)
+    ro, rl = oracle_prefill(oracle_mod, p)
+    check_out(out, ro)
+    check_lse(lse, rl)
+    assert sa.get_status(ws) == 0
+
+
+def test_chunked_prefill_prefix_v_quarters_with_different_scales(sa, oracle_mod, cuda_dev):
+    """The same scaling for prefix tiles read through the block table."""
+    p = inputs.make_prefill([40, 3], 8, 2, 64, seed=52, sinks=True, prefix_lens=[300, 150])
+    pre = p.prefix
+    for i, P in enumerate(pre.lens.tolist()):
+        for pos in range(P):
+            page = int(pre.block_table[i, pos // 16])
+            if 32 <= pos % 128 < 64:
+                pre.v_pages[page, :, pos % 16] = _large_rows(64, 16, pos).to(torch.bfloat16)
+    ws = sa.workspace(0, cuda_dev, "prefill")
+    sa.get_status(ws)
+    out, lse = run_prefill(sa, p, cuda_dev)
+    ro, rl = oracle_prefill(oracle_mod, p)
+    check_out(out, ro)
+    check_lse(lse, rl)
+    assert sa.get_status(ws) == 0
+
+
+def test_prefill_v_beyond_fp16_range_sets_status(sa, cuda_dev):
+    p = inputs.make_prefill([50], 8, 2, 64, seed=9, sinks=True)
+    p.v[10, 1, 5] = 2.0 ** 23
+    ws = sa.workspace(0, cuda_dev, "prefill")
+    sa.get_status(ws)
+    run_prefill(sa, p, cuda_dev)
+    assert sa.get_status(ws) & sa.STATUS_VALUE_RANGE
+
+
 def test_prefill_bad_prefix_page_sets_status(sa, cuda_dev):
     p = inputs.make_prefill([20, 20], 8, 2, 64, seed=7, sinks=True, prefix_lens=[64, 64])
     p.prefix.block_table[1, 1] = p.prefix.num_pages + 99
