@@ -33,10 +33,13 @@
 //               quarter per warp (one warp per SM sub-partition), each quarter scaled by
 //               its own power of two 2^-k that keeps it in fp16 range (k = 0 unless
 //               |v| >= 2^15); the softmax multiplies P by 2^k over the same 32 keys.
-// TMEM columns: NB S/P buffers of 128 columns (3 at head_dim 64, 2 at 128) rotate over
-// the S products of both tiles, then O_A and O_B (D columns each).  S product i goes to
-// buffer i % NB once the P.V of product i - NB (which read that buffer) has completed,
-// so S runs up to NB products ahead of the softmax.
+// TMEM columns.  S products are numbered i = 0, 1, ... over the CTA's lifetime (key tile
+// by key tile, query tile x = i % ntiles).  At head_dim 64: two S buffers of 128 columns,
+// two P buffers of 64 (fp16 pairs), O_A and O_B of 64.  S(i) goes to S buffer i % 2 as
+// soon as the softmax has copied S(i - 2) into registers, and P(i) to P buffer i % 2 once
+// the P.V of product i - 2 has completed, so the tensor core computes the next S products
+// while the softmax works.  At head_dim 128 (O_A and O_B take 256 columns) P is written
+// over S in two S/P buffers, and S(i) waits for the P.V of product i - 2.
 #include <float.h>
 
 #include "internal.h"
@@ -72,19 +75,27 @@ struct PrefillCfg {
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-    static constexpr int kSPBufs = D == 64 ? 3 : 2;  // S/P buffers rotating over the tiles
-    static constexpr int kNumBars = 2 + 4 * kStages + 3 * kSPBufs + 2 + 1;
+    static constexpr bool kSplitP = D == 64;         // P in buffers of its own (else over S)
+    static constexpr int kSBufs = 2;                 // S buffers (128 columns, fp32)
+    static constexpr int kPBufs = 2;                 // P buffers (64 columns of fp16 pairs)
+    static constexpr int kNumBars = 2 + 4 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 3 * kLocateMax * 4;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
-    __host__ __device__ static constexpr uint32_t kColSP(int b) { return 128u * b; }
-    __host__ __device__ static constexpr uint32_t kColO(int x) { return 128u * kSPBufs + D * x; }
-    static_assert(128 * kSPBufs + 2 * D <= 512, "TMEM columns");
+    __host__ __device__ static constexpr uint32_t kColS(int b) { return 128u * b; }
+    __host__ __device__ static constexpr uint32_t kColP(int p) {
+        return kSplitP ? 128u * kSBufs + 64u * p : 128u * p;
+    }
+    __host__ __device__ static constexpr uint32_t kColO(int x) {
+        return (kSplitP ? 128u * kSBufs + 64u * kPBufs : 128u * kSBufs) + D * x;
+    }
+    static_assert(kSplitP || kSBufs == kPBufs, "P over S needs one P buffer per S buffer");
+    static_assert(kColO(2) <= 512, "TMEM columns");
 };
 
 struct Bars {
-    uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *kv_empty, *s_full, *p_full, *pv_done,
-        *o_free, *drain;
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *kv_empty, *s_full, *s_free, *p_full,
+        *pv_done, *o_free, *drain;
 };
 
 // Bounded wait that also gives up as soon as another role has given up.
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vpmap, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     constexpr int NS = C::kStages;
-    constexpr int NB = C::kSPBufs;
+    constexpr int NBS = C::kSBufs, NBP = C::kPBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -265,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.kv_empty = bars.v_conv + NS;
     // Every wait below is for the next completion of its barrier or the one before,
     // never older: a parity wait cannot tell phases two apart.
-    bars.s_full = bars.kv_empty + NS;      // [NB] per S/P buffer: its S product is done
-    bars.p_full = bars.s_full + NB;        // [NB] per S/P buffer: its P is written
-    bars.pv_done = bars.p_full + NB;       // [NB] per S/P buffer: the P.V reading it is done
-    bars.o_free = bars.pv_done + NB;       // [2] per query tile: O was read (once per item)
+    bars.s_full = bars.kv_empty + NS;      // [NBS] per S buffer: its S product is done
+    bars.s_free = bars.s_full + NBS;       // [NBS] per S buffer: the softmax has read it
+    bars.p_full = bars.s_free + NBS;       // [NBP] per P buffer: its P is written
+    bars.pv_done = bars.p_full + NBP;      // [NBP] per P buffer: the P.V reading it is done
+    bars.o_free = bars.pv_done + NBP;      // [2] per query tile: O was read (once per item)
     bars.drain = bars.o_free + 2;
     int *s_loc = reinterpret_cast<int *>(smem + C::kOffLoc);
     int *misc = reinterpret_cast<int *>(smem + C::kOffMisc);
@@ -294,10 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.v_conv[s], 4);  // one arrive per converter warp
             mbar_init(&bars.kv_empty[s], 1);
         }
-        for (int b = 0; b < NB; ++b) {
+        for (int b = 0; b < NBS; ++b) {
             mbar_init(&bars.s_full[b], 1);
-            mbar_init(&bars.p_full[b], 4);
-            mbar_init(&bars.pv_done[b], 1);
+            mbar_init(&bars.s_free[b], 4);
+        }
+        for (int p = 0; p < NBP; ++p) {
+            mbar_init(&bars.p_full[p], 4);
+            mbar_init(&bars.pv_done[p], 1);
         }
         for (int x = 0; x < 2; ++x) mbar_init(&bars.o_free[x], 4);
         mbar_init(bars.drain, 2);  // one commit from each MMA-issuing warp
@@ -433,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Warp 1 issues the P.V products, warp 2 the S products; each runs its loop warp-
         // uniformly and one elected lane issues each MMA group.  S products are numbered
         // i = 0, 1, ... over the CTA's lifetime (key tile by key tile, query tile x = i %
-        // ntiles); S(i) goes to S/P buffer i % NB.
+        // ntiles); S(i) goes to S buffer i % NBS and P(i) is read from P buffer i % NBP.
         const bool pv_role = warp == 1;
         constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false);
         constexpr uint32_t idesc_o = tc::idesc_f16_f32(kBM, D, true);
@@ -451,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rank = blockIdx.x, k = 0, j = 0, x = 0, kv = 0;
         int n_kv = rank < n_items ? geom_of(a, item_of(a, wl, rank)).n_kv : 0;
         uint32_t i = 0;
-        int b = 0;           // i % NB
-        uint32_t use = 0;    // i / NB
+        int b = 0, pb = 0;            // i % NBS, i % NBP
+        uint32_t use = 0, use_p = 0;  // i / NBS, i / NBP
         bool ok = true;
         while (ok && rank < n_items) {
             const int st = kv % NS;
@@ -460,11 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pv_role) {
                 // O_x += P V in fp16: P (keys 2c, 2c + 1 in column c) in the first 64 columns
                 // of the S/P buffer, V scaled into fp16 by the converter warp
-                if (!warp_wait(&bars.p_full[b], use & 1)) break;
+                if (!warp_wait(&bars.p_full[pb], use_p & 1)) break;
                 if (j == 0 && k > 0 && !warp_wait(&bars.o_free[x], (uint32_t)((k - 1) & 1))) break;
                 if (x == 0 && !warp_wait(&bars.v_conv[st], sp)) break;
                 const uint64_t v0 = dv + (uint64_t)((st * C::kKVBytes) >> 4);
-                const uint32_t tp = tmem + C::kColSP(b), to = tmem + C::kColO(x);
+                const uint32_t tp = tmem + C::kColP(pb), to = tmem + C::kColO(x);
                 const uint32_t acc0 = j > 0 ? 1u : 0u;
                 if (elect_one()) {
                     tc::fence_after_sync();
@@ -472,13 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         tc::mma_f16_ts(to, tp + 8 * kk, v0 + (uint64_t)((kk * 2048) >> 4), idesc_o,
                                        kk > 0 ? 1u : acc0);
-                    tc::commit(&bars.pv_done[b]);
+                    tc::commit(&bars.pv_done[pb]);
                     if (x == ntiles - 1) tc::commit(&bars.kv_empty[st]);
                 }
                 __syncwarp();
             } else {
-                // buffer b is free once the P.V of product i - NB has completed
-                if (use > 0 && !warp_wait(&bars.pv_done[b], (use - 1) & 1)) break;
+                // S buffer b is free once the softmax has read S(i - NBS) (with P over S:
+                // once the P.V of product i - NBS has completed)
+                if (use > 0 &&
+                    !warp_wait(C::kSplitP ? &bars.s_free[b] : &bars.pv_done[b], (use - 1) & 1))
+                    break;
                 if (j == 0 && x == 0 && !warp_wait(bars.q_full, (uint32_t)(k & 1))) break;
                 if (x == 0 && !warp_wait(&bars.k_full[st], sp)) break;
                 const uint64_t q0 = dq + (uint64_t)((x * C::kQBytes) >> 4);
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        tc::mma_f16_ss(tmem + C::kColSP(b), q0 + off, k0 + off, idesc_s, kk > 0 ? 1u : 0u);
+                        tc::mma_f16_ss(tmem + C::kColS(b), q0 + off, k0 + off, idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc::commit(&bars.s_full[b]);
                     if (last) tc::commit(bars.q_empty);  // the item's Q tiles are no longer read
@@ -498,9 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // next product
             ++i;
-            if (++b == NB) {
+            if (++b == NBS) {
                 b = 0;
                 ++use;
+            }
+            if (++pb == NBP) {
+                pb = 0;
+                ++use_p;
             }
             if (++x == ntiles) {
                 x = 0;
@@ -611,9 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
             for (int j = 0; j < gm.n_kv; ++j) {
                 const uint32_t i = tcount * ntiles + x;  // number of this S product
-                const int b = i % NB;
-                const uint32_t tsp = tmem + lane_base + C::kColSP(b);
-                if (!wait_or_abort(&bars.s_full[b], (i / NB) & 1, s_abort, a.status)) {
+                const int b = i % NBS, pb = i % NBP;
+                const uint32_t ts = tmem + lane_base + C::kColS(b);
+                const uint32_t tp = tmem + lane_base + C::kColP(pb);
+                if (!wait_or_abort(&bars.s_full[b], (i / NBS) & 1, s_abort, a.status)) {
                     ok = false;
                     break;
                 }
@@ -630,20 +653,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t sv[kBN];
 #pragma unroll
                 for (int c = 0; c < kBN / 32; ++c)
-                    tc::ld_32x32b_x32(tsp + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                    tc::ld_32x32b_x32(ts + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
                 tc::wait_ld();
+                if (C::kSplitP) {  // S is in registers: its buffer may take the next S product
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.s_free[b]);
+                }
                 if (ncols < kBN) {  // diagonal, ragged or prefix-tail tile: hide invisible keys
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (c >= ncols) sv[c] = 0xFF800000u;  // -inf
                 }
+                // row max: eight chains of three-input maxima over 16 keys each
                 float mx8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sv[e]);
+                for (int e = 0; e < 8; ++e) {
+                    const float *sf = reinterpret_cast<const float *>(sv) + 16 * e;
+                    float m = fmax3(sf[0], sf[1], sf[2]);
 #pragma unroll
-                for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sv[c]));
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    for (int t = 3; t < 15; t += 2) m = fmax3(m, sf[t], sf[t + 1]);
+                    mx8[e] = fmaxf(m, sf[15]);
+                }
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float mt = mx * a.scale_log2;
                 if (j == 0) {
                     const float mn = fmaxf(m_used, mt);
@@ -653,9 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool need = mt > m_used + kRescaleThreshold;
                     if (__any_sync(0xffffffffu, need)) {
                         // O_x must hold the P.V of this query tile's previous key tile,
-                        // S product i - ntiles (its buffer's previous use is long done)
+                        // product i - ntiles (its P buffer's previous use is long done)
                         const uint32_t ip = i - ntiles;
-                        if (!wait_or_abort(&bars.pv_done[ip % NB], (ip / NB) & 1, s_abort, a.status)) {
+                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status)) {
                             ok = false;
                             break;
                         }
@@ -677,53 +710,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // P * 2^k = exp2(s * scale - m + k) in fp16 over the first 64 columns of the
-                // buffer (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter
-                // holding keys 32ch..32ch+31
+                // P * 2^k = exp2(s * scale - m + k) in fp16 in the 64 columns of the P buffer
+                // (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter holding
+                // keys 32ch..32ch+31
                 const int vst = (tcount - 1) % NS;
                 if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status)) {
                     ok = false;
                     break;
                 }
+                if (C::kSplitP && i >= (uint32_t)NBP) {
+                    // the P buffer is free once the P.V of product i - NBP has completed
+                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                }
                 const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
                 const bool k_uniform = kq.x == kq.y && kq.y == kq.z && kq.z == kq.w;  // warp-uniform
                 const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
-                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                // running sums of keys c with c % 8 = 2q (.x) and 2q + 1 (.y)
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                uint32_t pp[kBN / 2];
 #pragma unroll
                 for (int ch = 0; ch < kBN / 32; ++ch) {
                     const int kc = ch == 0 ? kq.x : ch == 1 ? kq.y : ch == 2 ? kq.z : kq.w;
                     const float neg = neg0 + (float)kc;
-                    uint32_t pp[16];
+                    const float2 ng2 = make_float2(neg, neg);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int c = ch * 32 + 2 * e;
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), a.scale_log2, neg));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, neg));
-                        sum8[(2 * e) & 7] += p0;
-                        sum8[(2 * e + 1) & 7] += p1;
-                        pp[e] = pack_f16x2(p0, p1);
+                        const float2 t2 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                                sc2, ng2);
+                        const float p0 = fast_exp2(t2.x);
+                        const float p1 = fast_exp2(t2.y);
+                        acc[e & 3] = fadd2(acc[e & 3], make_float2(p0, p1));
+                        pp[ch * 16 + e] = pack_f16x2(p0, p1);
                     }
-                    tc::st_32x32b_x16(tsp + ch * 16, pp);
+                    tc::st_32x32b_x16(tp + ch * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[ch * 16]));
                     if (!k_uniform) {  // quarters scaled differently: fold this chunk into l now
-                        l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                              ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
+                        l += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                              ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
                              __uint_as_float((uint32_t)(127 - kc) << 23);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+                        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
                     }
                 }
                 if (k_uniform)
-                    l += (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]))) *
+                    l += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
                          __uint_as_float((uint32_t)(127 - kq.x) << 23);
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p_full[b]);
+                if (lane == 0) mbar_arrive(&bars.p_full[pb]);
             }
             if (!ok) break;
             // epilogue: O / l for this row, once the item's last P.V has landed
             const uint32_t il = (tcount - 1) * ntiles + x;  // S product of the last key tile
-            if (!wait_or_abort(&bars.pv_done[il % NB], (il / NB) & 1, s_abort, a.status)) {
+            if (!wait_or_abort(&bars.pv_done[il % NBP], (il / NBP) & 1, s_abort, a.status)) {
                 ok = false;
                 break;
             }
