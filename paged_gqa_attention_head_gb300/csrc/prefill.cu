@@ -122,7 +122,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 
 // Work list.  Query blocks are ordered by their index inside the request (the
 // number of causal key tiles they see), largest first, then by request, then by
-// head (pair); items are dealt round-robin to the persistent CTAs.  Set-up, once
+// head (pair); items are dealt to the persistent CTAs in rounds (see item_rank).  Set-up, once
 // per CTA: s_nq[i] = query blocks of request i; s_cnt[lev] = requests with more
 // than lev query blocks; s_cum[lev] = query blocks at levels above lev.
 struct WorkList {
@@ -232,6 +232,15 @@ __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
     return it;
 }
 
+// Rank of this CTA's k-th item: items are dealt in rounds of gridDim.x, in alternating
+// direction, so that with items sorted by size the CTAs' totals come out close.  Every
+// rank below n_items belongs to exactly one (CTA, k), and a CTA's ranks only grow, so
+// its items end at the first rank >= n_items.
+__device__ __forceinline__ int item_rank(int k) {
+    const int G = gridDim.x, b = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - b : b);
+}
+
 struct ItemGeom {
     int row0, L, P, n_pre, n_kv, g;
 };
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kv = 0;  // key tiles loaded so far (ring position)
         int k = 0;   // items so far
         bool ok = true;
-        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
+        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
             const ItemGeom gm = geom_of(a, it);
             if (lane == 0 && a.prefix_lens) {
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
             return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort, a.status));
         };
-        int rank = blockIdx.x, k = 0, j = 0, x = 0, kv = 0;
+        int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
         int n_kv = rank < n_items ? geom_of(a, item_of(a, wl, rank)).n_kv : 0;
         uint32_t i = 0;
         int b = 0, pb = 0;            // i % NBS, i % NBP
@@ -529,8 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++kv;
                 if (++j == n_kv) {
                     j = 0;
-                    ++k;
-                    rank += gridDim.x;
+                    rank = item_rank(++k);
                     if (rank < n_items) n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
                 }
             }
@@ -548,9 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // quarter stays below 2^15 and P * 2^k below 2^15 (k <= 7).  The quarter is
         // 32 rows x 128 bytes of each 64-column half of the tile.
         const int q = warp - 12;
-        int kv = 0;
+        int kv = 0, k = 0;
         bool ok = true;
-        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x) {
+        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const int n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
             for (int j = 0; j < n_kv; ++j, ++kv) {
                 const int st = kv % NS;
@@ -623,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tcount = 0;  // key tiles this query tile has processed (over all items)
         int k = 0;
         bool ok = x < ntiles;
-        for (int rank = blockIdx.x; ok && rank < n_items; rank += gridDim.x, ++k) {
+        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
             const ItemGeom gm = geom_of(a, it);
             const int h = it.h0 + x;
