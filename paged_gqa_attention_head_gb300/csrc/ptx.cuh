@@ -209,30 +209,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// 2^x for two values at once on the FMA and integer pipes instead of the special
-// function unit (which ex2.approx uses), for x <= 15; x is clamped below at -125, whose
-// power of two (~2.4e-38) stands in for 0.  Method: x = j + f with j = round(x) (the
-// 1.5 * 2^23 addition rounds to an integer) and |f| <= 1/2; 2^f from a degree-4
-// polynomial fitted to 2^f on [-1/2, 1/2] in relative error (max 2.7e-6 in fp32
-// arithmetic); 2^j enters by adding j to the exponent field.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = fadd2(x, make_float2(kRound, kRound));
-    const float2 j = fadd2(t, make_float2(-kRound, -kRound));
-    const float2 f = ffma2(j, make_float2(-1.f, -1.f), x);  // x - j, exact
-    float2 p = ffma2(make_float2(9.570087306201458e-3f, 9.570087306201458e-3f), f,
-                     make_float2(5.5917855352163315e-2f, 5.5917855352163315e-2f));
-    p = ffma2(p, f, make_float2(2.40247443318367e-1f, 2.40247443318367e-1f));
-    p = ffma2(p, f, make_float2(6.931217908859253e-1f, 6.931217908859253e-1f));
-    p = ffma2(p, f, make_float2(9.999992847442627e-1f, 9.999992847442627e-1f));
-    // t's low mantissa bits hold 0x400000 + j; shifted into the exponent field the
-    // constant part leaves the 32-bit word, so this adds j to p's exponent
-    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile whose rows are
 // 128 bytes and whose chunks are XOR-swizzled by (row % 8) - the layout TMA
 // writes with CU_TENSOR_MAP_SWIZZLE_128B into a 1024-byte aligned buffer.
