@@ -98,14 +98,21 @@ struct Bars {
         *pv_done, *o_free, *drain;
 };
 
-// Bounded wait that also gives up as soon as another role has given up.
+// Bounded wait that also gives up as soon as another role has given up.  With kSleep
+// the thread sleeps in the wait (for warps off the critical path: it leaves the issue
+// slots to the softmax warps, at ~50 cycles more wake-up latency).
+template <bool kSleep = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort,
                                               uint32_t *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        for (int i = 0; i < 128; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (kSleep) {
+            if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        } else {
+            for (int i = 0; i < 128; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+        }
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
@@ -353,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
             }
             // Q tiles of this item, once the previous item's last S products are done
-            if (k > 0 && !wait_or_abort(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status)) {
+            if (k > 0 && !wait_or_abort<true>(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status)) {
                 ok = false;
                 break;
             }
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (u > 0 &&
-                    !wait_or_abort(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status)) {
+                    !wait_or_abort<true>(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status)) {
                     ok = false;
                     break;
                 }
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all lanes wait; the outcome is made warp-uniform so that no lane is left behind
         // at the elect.sync below when a wait gives up
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort, a.status));
+            return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status));
         };
         int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
         int n_kv = rank < n_items ? geom_of(a, item_of(a, wl, rank)).n_kv : 0;
@@ -562,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
             for (int j = 0; j < n_kv; ++j, ++kv) {
                 const int st = kv % NS;
-                if (!__all_sync(0xffffffffu, wait_or_abort(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
+                if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
                                                             s_abort, a.status))) {
                     ok = false;
                     break;

@@ -52,6 +52,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not yet complete sleeps until it
+// completes or `sleep_ns` have passed, instead of returning after a short fixed time
+// (so a waiting warp stops taking issue slots from the warps that work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t sleep_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // A wait that gives up after about `limit_ns` of wall time (checked every 256
 // polls) instead of spinning forever.  Returns false on timeout.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
