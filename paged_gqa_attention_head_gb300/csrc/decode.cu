@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
 
     for (int u = 0; u < n_units; ++u) {
         const int stage = u % S;
-        if (!mbar_wait(&wbar[stage], (uint32_t)((u / S) & 1))) {
+        if (!mbar_wait_sleep(&wbar[stage], (uint32_t)((u / S) & 1))) {
             // give up: record it, let the copies already issued land, leave
             if (lane == 0) set_status(a.status, SINKATTN_STATUS_WAIT_TIMEOUT);
             for (int v = u; v < min(n_units, u + S); ++v)

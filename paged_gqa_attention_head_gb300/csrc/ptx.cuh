@@ -82,6 +82,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// As mbar_wait, sleeping in the wait (see mbar_try_wait_sleep) after one poll.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tensor core) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
