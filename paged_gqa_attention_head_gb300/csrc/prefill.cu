@@ -80,7 +80,7 @@ struct PrefillCfg {
     static constexpr int kPBufs = 2;                 // P buffers (64 columns of fp16 pairs)
     static constexpr int kNumBars = 2 + 4 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
-    static constexpr int kOffMisc = kOffLoc + 3 * kLocateMax * 4;
+    static constexpr int kOffMisc = kOffLoc + 4 * kLocateMax * 4;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
     __host__ __device__ static constexpr uint32_t kColS(int b) { return 128u * b; }
     __host__ __device__ static constexpr uint32_t kColP(int p) {
@@ -127,34 +127,68 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Work list.  Query blocks are ordered by their index inside the request (the
-// number of causal key tiles they see), largest first, then by request, then by
-// head (pair); items are dealt to the persistent CTAs in rounds (see item_rank).  Set-up, once
-// per CTA: s_nq[i] = query blocks of request i; s_cnt[lev] = requests with more
-// than lev query blocks; s_cum[lev] = query blocks at levels above lev.
+// Work list, in two parts.  (A) Requests with a paged prefix, request by request (each
+// request's query blocks from the last to the first, then by head pair): the items that
+// read one request's prefix run close together in time and share its pages in L2.
+// (B) Requests without a prefix: query blocks ordered by their index inside the request
+// (the number of causal key tiles they see), largest first, then by request, then by head
+// pair.  Items are dealt to the persistent CTAs in rounds (see item_rank).
+// Set-up, once per CTA: s_nq[i] = query blocks of request i if it is in part B, else 0;
+// s_aend[i] = part-A query blocks of requests 0..i; s_cnt[lev] = part-B requests with more
+// than lev query blocks; s_cum[lev] = part-B query blocks at levels above lev.
 struct WorkList {
-    const int *nq, *cnt, *cum;
-    int n, levels, tiles, heads_per_item, groups;  // groups = items per query block
+    const int *nq, *cnt, *cum, *aend;
+    int n, levels, tiles, tiles_a, heads_per_item, groups;  // groups = items per query block
     bool fast;
 };
 
-__device__ void worklist_setup(const PrefillArgs &a, int *s_nq, int *s_cnt, int *s_cum, int *s_misc,
-                               WorkList *wl) {
+__device__ __forceinline__ int query_blocks(const PrefillArgs &a, int i) {
+    const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
+    return L > 0 ? (L + kBM - 1) / kBM : 0;
+}
+
+__device__ __forceinline__ bool has_prefix(const PrefillArgs &a, int i) {
+    return a.prefix_lens != nullptr && a.prefix_lens[i] > 0;
+}
+
+__device__ void worklist_setup(const PrefillArgs &a, int *s_nq, int *s_cnt, int *s_cum, int *s_aend,
+                               int *s_misc, WorkList *wl) {
     const int tid = threadIdx.x;
     const bool fast = a.n <= kLocateMax;
     if (tid == 0) s_misc[0] = 0;
     __syncthreads();
     int mx = 0;
     for (int i = tid; i < a.n; i += blockDim.x) {
-        const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-        const int q = L > 0 ? (L + kBM - 1) / kBM : 0;
-        if (fast) s_nq[i] = q;
-        mx = max(mx, q);
+        const int q = query_blocks(a, i);
+        const bool pa = has_prefix(a, i);
+        if (fast) {
+            s_nq[i] = pa ? 0 : q;
+            s_aend[i] = pa ? q : 0;  // made inclusive below
+        }
+        mx = max(mx, pa ? 0 : q);
     }
     atomicMax(&s_misc[0], mx);
     __syncthreads();
     const int levels = s_misc[0];
     const bool fast_lv = fast && levels <= kLocateMax;
+    if (fast && tid < 32) {
+        // inclusive prefix sum of s_aend by warp 0: lane l sums a contiguous chunk, the
+        // chunk totals are scanned across the warp, then each lane adds its offset
+        const int per = (a.n + 31) / 32, i0 = min(a.n, tid * per), i1 = min(a.n, i0 + per);
+        int run = 0;
+        for (int i = i0; i < i1; ++i) {
+            run += s_aend[i];
+            s_aend[i] = run;
+        }
+        int incl = run;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (tid >= d) incl += v;
+        }
+        const int off = incl - run;
+        for (int i = i0; i < i1; ++i) s_aend[i] += off;
+    }
     if (fast_lv)
         for (int lev = tid; lev < levels; lev += blockDim.x) {
             int c = 0;
@@ -163,27 +197,33 @@ __device__ void worklist_setup(const PrefillArgs &a, int *s_nq, int *s_cnt, int 
         }
     __syncthreads();
     if (tid == 0) {
-        int tiles = 0;
+        int tiles_a = 0, tiles_b = 0;
         if (fast_lv) {
+            tiles_a = a.n > 0 ? s_aend[a.n - 1] : 0;
             for (int lev = levels - 1; lev >= 0; --lev) {
-                s_cum[lev] = tiles;
-                tiles += s_cnt[lev];
+                s_cum[lev] = tiles_b;
+                tiles_b += s_cnt[lev];
             }
         } else {
             for (int i = 0; i < a.n; ++i) {
-                const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-                tiles += L > 0 ? (L + kBM - 1) / kBM : 0;
+                if (has_prefix(a, i))
+                    tiles_a += query_blocks(a, i);
+                else
+                    tiles_b += query_blocks(a, i);
             }
         }
-        s_misc[1] = tiles;
+        s_misc[1] = tiles_a + tiles_b;
+        s_misc[2] = tiles_a;
     }
     __syncthreads();
     wl->nq = s_nq;
     wl->cnt = s_cnt;
     wl->cum = s_cum;
+    wl->aend = s_aend;
     wl->n = a.n;
     wl->levels = levels;
     wl->tiles = s_misc[1];
+    wl->tiles_a = s_misc[2];
     wl->heads_per_item = a.G >= 2 ? 2 : 1;
     wl->groups = a.Hq / wl->heads_per_item;
     wl->fast = fast_lv;
@@ -196,10 +236,39 @@ struct Item {
 // Item of a given rank (any thread; reads the set-up tables).
 __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
     Item it;
-    const int tr = rank / wl.groups;
+    int tr = rank / wl.groups;
     it.h0 = (rank % wl.groups) * wl.heads_per_item;
     it.req = 0;
     it.qb = 0;
+    if (tr < wl.tiles_a) {
+        // part A: the request whose query blocks hold tile rank tr, then its blocks from
+        // the last one down
+        int i = 0, before = 0;
+        if (wl.fast) {
+            // smallest i with aend[i] > tr (aend does not decrease)
+            int lo = 0, hi = wl.n - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (wl.aend[mid] > tr)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            i = lo;
+            before = i > 0 ? wl.aend[i - 1] : 0;
+            it.qb = wl.aend[i] - 1 - tr;  // blocks of request i: aend[i] - before
+        } else {
+            for (i = 0; i < a.n; ++i) {
+                const int q = has_prefix(a, i) ? query_blocks(a, i) : 0;
+                if (tr < before + q) break;
+                before += q;
+            }
+            it.qb = before + query_blocks(a, i) - 1 - tr;
+        }
+        it.req = i;
+        return it;
+    }
+    tr -= wl.tiles_a;
     if (wl.fast) {
         // the level holding tile rank tr: cum[lev] <= tr < cum[lev] + cnt[lev]; cum
         // decreases as lev grows, so this is the smallest lev with cum[lev] <= tr
@@ -220,22 +289,18 @@ __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
         it.qb = lo;
         return it;
     }
-    // slow path: walk levels from the top over global memory
+    // slow path: walk the levels of part B from the top over global memory
     int mq = 0;
-    for (int i = 0; i < a.n; ++i) {
-        const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-        mq = max(mq, L > 0 ? (L + kBM - 1) / kBM : 0);
-    }
+    for (int i = 0; i < a.n; ++i)
+        if (!has_prefix(a, i)) mq = max(mq, query_blocks(a, i));
     int r = tr;
     for (int lev = mq - 1; lev >= 0; --lev)
-        for (int i = 0; i < a.n; ++i) {
-            const int L = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
-            if (L > 0 && (L + kBM - 1) / kBM > lev && r-- == 0) {
+        for (int i = 0; i < a.n; ++i)
+            if (!has_prefix(a, i) && query_blocks(a, i) > lev && r-- == 0) {
                 it.req = i;
                 it.qb = lev;
                 return it;
             }
-        }
     return it;
 }
 
@@ -307,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     WorkList wl;
-    worklist_setup(a, s_loc, s_loc + kLocateMax, s_loc + 2 * kLocateMax, misc + 4, &wl);
+    worklist_setup(a, s_loc, s_loc + kLocateMax, s_loc + 2 * kLocateMax, s_loc + 3 * kLocateMax, misc + 4,
+                   &wl);
     const int n_items = wl.tiles * wl.groups;
     if ((int)blockIdx.x >= n_items) return;  // CTA-uniform, before any allocation
     const int ntiles = wl.heads_per_item;    // query tiles per item (1 or 2)
