@@ -141,6 +141,23 @@ def time_loop(torch, fn, steps: int, stream, marks=None):
     return start.elapsed_time(end)
 
 
+def reduce_step_time(dist, ms: float, device) -> float:
+    """The slowest rank's timed region, in ms, on every rank (all-reduce MAX); the
+    value itself when there is a single process (dist is None)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput in units/s / 1e9: every rank processes units_per_rank per step
+    (replicas: weak scaling), timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -199,12 +216,9 @@ def run_ours(args, rank, world, local_rank):
     t_load1 = time.time()
     clocks = sampler.stop(t_load0, t_load1)
     split_ms = sum(a.elapsed_time(b) for a, b in phase_events) / len(phase_events)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_step_time(dist, ms, dev)
     ms_step = ms / args.steps
-    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_value(kv_bytes, world, ms_step)
     ach = kv_bytes / (split_ms * 1e-3) / 1e9
     assert sa.get_status(sa.workspace(0, dev)) == 0, "device status reported a problem"
 
@@ -224,13 +238,16 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(3):
         e2e_step()
-    e2e_ms = time_loop(torch, e2e_step, args.steps, stream) / args.steps
+    if dist:
+        dist.barrier()
+    e2e_ms = reduce_step_time(dist, time_loop(torch, e2e_step, args.steps, stream), dev) / args.steps
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = host_out.numel() * 2 + host_lse.numel() * 4
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": nwarm, "ms_per_step": round(ms_step, 5),
+        "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": nwarm,
+        "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
         "config": {"workload": "gpt-oss-shape decode: B=64, 64 q / 8 KV heads, head_dim 64, "
@@ -239,7 +256,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 "
                    f"({kv_bytes / 1e6:.0f} MB of KV per step vs 129 MB L2)"},
         "tokens_per_s": round(world * 64 / (ms_step * 1e-3), 1),
-        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_value(kv_bytes, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "q, block table, lengths and sinks copied from pinned host memory and "

@@ -1,0 +1,73 @@
+"""The N-process path of bench.py on CPU: two gloo ranks (world size 2) run the same
+cross-rank reduction the GPU replicas use (slowest rank's time, whole-job value), and
+the reference arm's non-zero ranks leave without work or output.  Decode and prefill
+do not shard (independent replicas), so this reduction is the only cross-rank step."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, q) -> None:
+    sys.path.insert(0, ROOT)
+    import bench
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        ms = 10.0 + 5.0 * rank  # rank 1 is the slower one
+        slowest = bench.reduce_step_time(dist, ms, torch.device("cpu"))
+        dist.barrier()
+        value = bench.whole_job_value(548_345_856, world, slowest / 20)
+        q.put((rank, slowest, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time_and_whole_job_value():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    assert [g[0] for g in got] == [0, 1]
+    for _, slowest, value in got:
+        assert slowest == 15.0
+        # 2 replicas x 548 MB each per 0.75 ms step
+        assert value == pytest.approx(2 * 548_345_856 / 0.75e-3 / 1e9)
+
+
+def test_single_process_reduction_is_the_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.reduce_step_time(None, 3.25, torch.device("cpu")) == 3.25
+    assert bench.whole_job_value(1e9, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1",
+               MASTER_PORT=str(_free_port()))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
