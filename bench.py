@@ -53,14 +53,14 @@ def file_sha(*rel):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel: str, sources: list[str]):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current source of the kernel (else None)."""
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu summary, if it
+    was taken on the kernel's current source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
-    if not d or d.get("source_sha") != file_sha(*d.get("source_files", sources)):
+    d = json.load(open(p)).get(f"{kernel}:{workload}")
+    if not d or d.get("source_sha") != file_sha(*d.get("source_files", [])):
         return None
     return d.get("bytes_per_launch")
 
@@ -265,7 +265,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": round(ach, 1),
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "traffic": traffic_for("decode_splitkv_kernel", []),
+                     "traffic": traffic_for("decode_splitkv_kernel", HEADLINE),
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "kernel_ms": round(split_ms, 5)},
         "clocks": clocks,
@@ -341,7 +341,7 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
         rows[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
                       "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": p.flops(),
                       "peak_source": f"{peak_src} bf16_tflops (burst)",
-                      "traffic": traffic_for("prefill_kernel", []) if name == "gptoss_prefill" else None}
+                      "traffic": traffic_for("prefill_kernel", name)}
     return rows
 
 
