@@ -39,9 +39,9 @@ def _load():
         build()
         lib = ctypes.CDLL(_LIB_PATH)
         P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        lib.oracle_decode.argtypes = [P, P, P, P, P, P, D, I, I, I, I, I, I64, I, P, P, P]
+        lib.oracle_decode.argtypes = [P, P, P, P, P, P, D, I, I, I, I, I, I64, I, I, P, P, P]
         lib.oracle_decode.restype = I
-        lib.oracle_prefill.argtypes = [P, P, P, P, I, P, P, P, P, I64, I, P, D, I, I, I, I, P, P, P]
+        lib.oracle_prefill.argtypes = [P, P, P, P, I, P, P, P, P, I64, I, P, D, I, I, I, I, I, P, P, P]
         lib.oracle_prefill.restype = I
         lib.oracle_append_kv.argtypes = [P, P, P, I, P, P, I, I64, I, I, I, P, P]
         lib.oracle_append_kv.restype = I
@@ -90,9 +90,10 @@ def max_threads() -> int:
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, sinks, scale: float,
-           select: Optional[np.ndarray] = None):
+           select: Optional[np.ndarray] = None, window: int = 0):
     """Decode attention.  q [B,Hq,D]; pages [num_pages,Hkv,P,D]; returns (out [B,Hq,D], lse [B,Hq])
-    in float64.  select: bool [B,Hq] restricting which rows are computed (others NaN)."""
+    in float64.  select: bool [B,Hq] restricting which rows are computed (others NaN).
+    window > 0: only the last `window` cached tokens are seen (sliding window)."""
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
     B, Hq, D = qb.shape
@@ -103,7 +104,8 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, sinks, scale: float,
     lse = np.full((B, Hq), np.nan)
     sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
     rc = lib.oracle_decode(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(sl), _ptr(sk), float(scale),
-                           B, Hq, Hkv, D, P, num_pages, bt.shape[1], _ptr(sel), _ptr(out), _ptr(lse))
+                           B, Hq, Hkv, D, P, num_pages, bt.shape[1], int(window), _ptr(sel), _ptr(out),
+                           _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_decode rejected its inputs ({rc})")
     return out, lse
@@ -111,8 +113,9 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, sinks, scale: float,
 
 def prefill(q, k, v, cu_seqlens, sinks, scale: float, k_pages=None, v_pages=None,
             prefix_block_table=None, prefix_lens=None, select: Optional[np.ndarray] = None,
-            page_size: int = 16):
-    """Causal ragged prefill, optionally over a paged prefix.  Returns (out [T,Hq,D], lse [T,Hq])."""
+            page_size: int = 16, window: int = 0):
+    """Causal ragged prefill, optionally over a paged prefix.  Returns (out [T,Hq,D], lse [T,Hq]).
+    window > 0: each query sees only the keys at its last `window` absolute positions."""
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     T, Hq, D = qb.shape
@@ -132,7 +135,7 @@ def prefill(q, k, v, cu_seqlens, sinks, scale: float, k_pages=None, v_pages=None
     sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
     rc = lib.oracle_prefill(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), n, _ptr(kp), _ptr(vp), _ptr(pbt),
                             _ptr(pl), num_pages, maxp, _ptr(_f32(sinks)), float(scale), Hq, Hkv, D,
-                            page_size, _ptr(sel), _ptr(out), _ptr(lse))
+                            page_size, int(window), _ptr(sel), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_prefill rejected its inputs ({rc})")
     return out, lse

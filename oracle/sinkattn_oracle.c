@@ -27,6 +27,11 @@
  *   same sequence; chunked prefill - all P_i prefix tokens plus new tokens 0..t,
  *   the new token t sitting at absolute position P_i + t.
  *
+ *   Sliding window W > 0 (gptoss.md section 4: even layers attend a local window of
+ *   128 positions, odd layers the full causal range; the window is passed per call to
+ *   the paged kernel): J keeps only the keys at absolute positions pos - W < j <= pos,
+ *   pos being the query's own position (decode: L_b - 1).  W <= 0: no window.
+ *
  *   KV pages are HND: [num_pages, Hkv, page_size, head_dim], the tokens of one
  *   (page, head) contiguous (Hosting Qwen on Blackwell, KV-cache layout paragraph).
  *   Token j of sequence b lives in page block_table[b][j / page_size], slot
@@ -117,7 +122,7 @@ int oracle_max_threads(void) {
 int oracle_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                   const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
                   double scale, int B, int Hq, int Hkv, int D, int P, int64_t num_pages,
-                  int max_pages, const uint8_t *select, double *out, double *lse) {
+                  int max_pages, int window, const uint8_t *select, double *out, double *lse) {
     if (Hq % Hkv) return -1;
     const int G = Hq / Hkv;
     for (int b = 0; b < B; ++b) {
@@ -134,19 +139,22 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_
         if (select && !select[bh]) continue;
         const int b = (int)(bh / Hq), h = (int)(bh % Hq), g = h / G;
         const int64_t L = seq_lens[b];
-        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(L + 1));
-        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(L + 1));
-        double *s = malloc(sizeof(double) * (size_t)(L + 1));
+        /* keys [lo, L): the query sits at position L - 1 */
+        const int64_t lo = (window > 0 && L > window) ? L - window : 0;
+        const int64_t nk = L - lo;
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)(nk + 1));
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)(nk + 1));
+        double *s = malloc(sizeof(double) * (size_t)(nk + 1));
         if (!krow || !vrow || !s) {
 #pragma omp atomic write
             bad = 1;
         } else {
-            for (int64_t j = 0; j < L; ++j) {
+            for (int64_t j = lo; j < L; ++j) {
                 int64_t pg = block_table[(int64_t)b * max_pages + j / P];
-                krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
-                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
+                krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
+                vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
             }
-            attend(q + bh * D, D, scale, sink_of(sinks, h), L, krow, vrow, s, out + bh * D,
+            attend(q + bh * D, D, scale, sink_of(sinks, h), nk, krow, vrow, s, out + bh * D,
                    lse + bh);
         }
         free(krow);
@@ -167,7 +175,7 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                    const int32_t *cu_seqlens, int n, const uint16_t *k_pages,
                    const uint16_t *v_pages, const int32_t *prefix_block_table,
                    const int32_t *prefix_lens, int64_t num_pages, int max_pages,
-                   const float *sinks, double scale, int Hq, int Hkv, int D, int P,
+                   const float *sinks, double scale, int Hq, int Hkv, int D, int P, int window,
                    const uint8_t *select, double *out, double *lse) {
     if (Hq % Hkv) return -1;
     const int G = Hq / Hkv;
@@ -192,7 +200,10 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         const int h = (int)(th % Hq), g = h / G, i = seq_of[t];
         const int64_t Pi = prefix_lens ? prefix_lens[i] : 0;
         const int64_t tl = t - cu_seqlens[i]; /* position among the new tokens */
-        const int64_t nk = Pi + tl + 1;
+        const int64_t pos = Pi + tl;           /* absolute position of the query */
+        /* keys at absolute positions [lo, pos]: prefix 0..Pi-1, then new tokens */
+        const int64_t lo = (window > 0 && pos + 1 > window) ? pos + 1 - window : 0;
+        const int64_t nk = pos + 1 - lo;
         const uint16_t **krow = malloc(sizeof(*krow) * (size_t)nk);
         const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)nk);
         double *s = malloc(sizeof(double) * (size_t)nk);
@@ -200,15 +211,16 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 #pragma omp atomic write
             bad = 1;
         } else {
-            for (int64_t j = 0; j < Pi; ++j) {
-                int64_t pg = prefix_block_table[(int64_t)i * max_pages + j / P];
-                krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
-                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
-            }
-            for (int64_t j = 0; j <= tl; ++j) {
-                int64_t row = cu_seqlens[i] + j;
-                krow[Pi + j] = k + (row * Hkv + g) * D;
-                vrow[Pi + j] = v + (row * Hkv + g) * D;
+            for (int64_t j = lo; j <= pos; ++j) {
+                if (j < Pi) {
+                    int64_t pg = prefix_block_table[(int64_t)i * max_pages + j / P];
+                    krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));
+                    vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));
+                } else {
+                    int64_t row = cu_seqlens[i] + (j - Pi);
+                    krow[j - lo] = k + (row * Hkv + g) * D;
+                    vrow[j - lo] = v + (row * Hkv + g) * D;
+                }
             }
             attend(q + th * D, D, scale, sink_of(sinks, h), nk, krow, vrow, s, out + th * D,
                    lse + th);

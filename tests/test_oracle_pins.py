@@ -9,7 +9,10 @@ Each pin ties the oracle to something it does not share code with:
   * invariances: permuting physical pages, splitting the keys and merging, the
     online (streaming) form seeded with the sink, decode == last causal row,
     chunked prefill == trailing rows of a full causal prefill;
-  * the append scatter read back through the block table.
+  * the append scatter read back through the block table;
+  * sliding window: SDPA on the last W keys sliced out explicitly (decode) or with
+    a band mask built from the window's definition (prefill, chunked), a window of
+    one key against the closed form, a window at least the length against no window.
 
 test_planted_mistakes_are_caught compiles copies of the oracle source with one
 plausible mistake each (dropped sink term, wrong GQA head, off-by-one slot, sign
@@ -105,6 +108,73 @@ def pin_prefill_sdpa(o, with_prefix: bool):
         ro, rl = sdpa_with_sink(q, k, v, w.scale, w.sinks, mask)
         np.testing.assert_allclose(out[cu[i]:cu[i + 1]], ro.permute(1, 0, 2).numpy(), rtol=RTOL, atol=ATOL)
         np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], rl.T.numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_decode_window_sdpa(o):
+    """Decode with window W == SDPA over the last W keys (sliced, not masked), incl.
+    W < L, W == L, W > L, W == 1, W and L off the page grid."""
+    lens = [1, 17, 64, 129, 40, 200]
+    w = inputs.make_decode(lens, len(lens), 8, 2, 64, seed=11, sinks=True)
+    for W in (1, 5, 40, 128, 300):
+        out, lse = o.decode(w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens,
+                            w.sinks, w.scale, window=W)
+        for b, L in enumerate(lens):
+            k, v = contiguous_kv(w.cache, b)
+            lo = max(0, L - W)
+            ro, rl = sdpa_with_sink(w.q[b].double()[:, None, :], k[:, lo:], v[:, lo:], w.scale, w.sinks)
+            np.testing.assert_allclose(out[b], ro[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+            np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_prefill_window_sdpa(o):
+    """Causal and chunked prefill with window W == SDPA with the band mask
+    pos - W < j <= pos (pos = prefix length + t), built here from that definition."""
+    new = [5, 33, 1, 20]
+    for with_prefix in (False, True):
+        pre = [0, 17, 40, 16] if with_prefix else None
+        w = inputs.make_prefill(new, 8, 2, 64, seed=12, sinks=True, prefix_lens=pre)
+        kw = {}
+        if with_prefix:
+            kw = dict(k_pages=w.prefix.k_pages, v_pages=w.prefix.v_pages,
+                      prefix_block_table=w.prefix.block_table, prefix_lens=w.prefix.lens)
+        for W in (1, 7, 24):
+            out, lse = o.prefill(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale, window=W, **kw)
+            cu = w.cu_seqlens.tolist()
+            for i, L in enumerate(new):
+                q = w.q[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+                k = w.k[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+                v = w.v[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+                P = 0
+                if with_prefix:
+                    pk, pv = contiguous_kv(w.prefix, i)
+                    P = pk.shape[1]
+                    k, v = torch.cat([pk, k], 1), torch.cat([pv, v], 1)
+                pos = P + torch.arange(L)[:, None]
+                j = torch.arange(P + L)[None, :]
+                mask = torch.where((j <= pos) & (j > pos - W), 0.0, -math.inf).double()
+                ro, rl = sdpa_with_sink(q, k, v, w.scale, w.sinks, mask)
+                np.testing.assert_allclose(out[cu[i]:cu[i + 1]], ro.permute(1, 0, 2).numpy(),
+                                           rtol=RTOL, atol=ATOL)
+                np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], rl.T.numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_window_special_cases(o):
+    """W = 1: only the query's own position, out = v * sigmoid(s - sink); W >= L (and
+    W <= 0): identical to no window."""
+    lens = [1, 16, 37]
+    w = inputs.make_decode(lens, 3, 4, 4, 64, seed=13, sinks=True)
+    args = (w.q, w.cache.k_pages, w.cache.v_pages, w.cache.block_table, w.seq_lens, w.sinks, w.scale)
+    out1, _ = o.decode(*args, window=1)
+    for b, L in enumerate(lens):
+        k, v = contiguous_kv(w.cache, b)
+        for h in range(4):
+            s = w.scale * float(np.dot(w.q[b, h].double().numpy(), k[h, L - 1].numpy()))
+            sig = 1.0 / (1.0 + math.exp(-(s - float(w.sinks[h]))))
+            np.testing.assert_allclose(out1[b, h], v[h, L - 1].numpy() * sig, rtol=1e-12, atol=1e-14)
+    full, full_lse = o.decode(*args)
+    for W in (37, 1000, 0, -5):
+        outw, lsew = o.decode(*args, window=W)
+        assert np.array_equal(outw, full) and np.array_equal(lsew, full_lse)
 
 
 def pin_single_key(o):
@@ -285,6 +355,9 @@ PINS = {
     "split_merge": pin_split_merge,
     "online": pin_online,
     "append_roundtrip": pin_append_roundtrip,
+    "decode_window_sdpa": pin_decode_window_sdpa,
+    "prefill_window_sdpa": pin_prefill_window_sdpa,
+    "window_special_cases": pin_window_special_cases,
 }
 
 
@@ -303,16 +376,28 @@ MUTATIONS = [
     ("GQA head taken modulo (decode)", "h = (int)(bh % Hq), g = h / G;", "h = (int)(bh % Hq), g = h % Hkv;"),
     ("GQA head taken modulo (prefill)", "g = h / G, i = seq_of[t];", "g = h % Hkv, i = seq_of[t];"),
     ("slot off by one (decode keys)",
-     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh",
-     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh"),
+     "krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh",
+     "krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            attend(q + bh"),
     ("exponent sign flipped", "double w = exp(s[j] - m);", "double w = exp(m - s[j]);"),
     ("lse without the max", "*lse = m + log(den);\n}", "*lse = log(den);\n}"),
     ("keys used as values", "out[d] += w * bf16_to_double(vrow[j][d]);", "out[d] += w * bf16_to_double(krow[j][d]);"),
-    ("causal window shifted by one", "krow[Pi + j] = k + (row * Hkv + g) * D;",
-     "krow[Pi + j] = k + ((row > 0 ? row - 1 : row) * Hkv + g) * D;"),
+    ("causal window shifted by one", "krow[j - lo] = k + (row * Hkv + g) * D;",
+     "krow[j - lo] = k + ((row > 0 ? row - 1 : row) * Hkv + g) * D;"),
     ("prefix page slot off by one",
-     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            for (int64_t j = 0; j <= tl",
-     "krow[j] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                vrow[j] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n            }\n            for (int64_t j = 0; j <= tl"),
+     "krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)(j % P));\n                    vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n                } else {",
+     "krow[j - lo] = page_row(k_pages, pg, Hkv, P, D, g, (int)((j + 1) % P));\n                    vrow[j - lo] = page_row(v_pages, pg, Hkv, P, D, g, (int)(j % P));\n                } else {"),
+    ("decode window one key too short",
+     "const int64_t lo = (window > 0 && L > window) ? L - window : 0;",
+     "const int64_t lo = (window > 0 && L > window) ? L - window + 1 : 0;"),
+    ("decode window ignored",
+     "const int64_t lo = (window > 0 && L > window) ? L - window : 0;",
+     "const int64_t lo = 0;"),
+    ("prefill window one key too long",
+     "const int64_t lo = (window > 0 && pos + 1 > window) ? pos + 1 - window : 0;",
+     "const int64_t lo = (window > 0 && pos > window) ? pos - window : 0;"),
+    ("prefill window measured from the new tokens only",
+     "const int64_t lo = (window > 0 && pos + 1 > window) ? pos + 1 - window : 0;",
+     "const int64_t lo = (window > 0 && tl + 1 > window) ? Pi + tl + 1 - window : 0;"),
     ("merge ignores the partial's max", "den += l[s] * w;", "den += l[s];"),
     ("online form skips the rescale", "den *= r;", "den *= 1.0;"),
     ("append writes the next slot",
