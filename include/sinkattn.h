@@ -78,6 +78,11 @@ typedef struct sinkattn_paged_desc {
     int32_t page_size;         /* P: 16 */
     int32_t num_pages;         /* pages in k_pages / v_pages (may be 0 for a prefill without prefix) */
     int32_t max_pages_per_seq; /* columns of the block table */
+    int32_t window;            /* sliding window W (decode and prefill): a query at
+                                * position pos sees only the keys at positions
+                                * pos - W < j <= pos (gptoss.md section 4: a 128-token
+                                * window on alternating layers, passed per call);
+                                * 0 or negative: no window */
 } sinkattn_paged_desc;
 
 /* Human-readable name of an error code (static string). */

@@ -168,6 +168,7 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.G = desc->num_qo_heads / desc->num_kv_heads;
     a.num_pages = desc->num_pages;
     a.max_pages = desc->max_pages_per_seq;
+    a.window = desc->window > 0 ? desc->window : 0;
     a.total_warps = P->layout.total_warps;
     a.status = reinterpret_cast<uint32_t *>(ws);
     a.ws_prefix = reinterpret_cast<int32_t *>(ws + P->layout.prefix);
@@ -328,6 +329,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     a.D = D;
     a.num_pages = has_prefix ? desc->num_pages : 0;
     a.max_pages = has_prefix ? desc->max_pages_per_seq : 0;
+    a.window = desc->window > 0 ? desc->window : 0;
     a.status = static_cast<uint32_t *>(workspace);
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
     if (e == cudaErrorNotSupported) return SINKATTN_ERR_UNSUPPORTED;

@@ -51,7 +51,7 @@ template <int D>
 int decode_smem_bytes(int B) {
     using C = DecodeCfg<D>;
     return 1024 /* alignment slack */ + C::kWarps * C::kWarpBytes +
-           C::kWarps * C::kStages * (8 + 4) + (2 * B + 1) * 4;
+           C::kWarps * C::kStages * (8 + 4 + 4) + (3 * B + 1) * 4;
 }
 
 __device__ __forceinline__ float quad_max(float x) {
@@ -63,9 +63,10 @@ __device__ __forceinline__ float quad_sum(float x) {
     return x + __shfl_xor_sync(0xffffffffu, x, 2);
 }
 
-// Lengths (validated, clamped) and the exclusive prefix sum of pages per
-// sequence into shared memory.  128 threads.
-__device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len) {
+// Lengths (validated, clamped), the first page each sequence's query sees (0, or the
+// page of its first key inside a sliding window) and the exclusive prefix sum of the
+// pages it sees, into shared memory.  128 threads.
+__device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len, int *s_first) {
     __shared__ int s_warp_tot[4];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int per_t = (a.B + 127) / 128;
@@ -79,7 +80,9 @@ __device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len) {
             L = L < 0 ? 0 : cap;
         }
         s_len[b] = L;
-        local += (L + kPageSize - 1) / kPageSize;
+        const int first = (a.window > 0 && L > a.window) ? (L - a.window) / kPageSize : 0;
+        s_first[b] = first;
+        local += (L + kPageSize - 1) / kPageSize - first;
     }
     int incl = local;
 #pragma unroll
@@ -93,7 +96,7 @@ __device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len) {
     for (int w = 0; w < wid; ++w) run += s_warp_tot[w];
     for (int b = b0; b < b1; ++b) {
         s_prefix[b] = run;
-        run += (s_len[b] + kPageSize - 1) / kPageSize;
+        run += (s_len[b] + kPageSize - 1) / kPageSize - s_first[b];
     }
     if (tid == 0) s_prefix[a.B] = s_warp_tot[0] + s_warp_tot[1] + s_warp_tot[2] + s_warp_tot[3];
     __syncthreads();
@@ -104,7 +107,9 @@ struct Cursor {
     int b, g, p, pb;  // pb = pages of sequence b
 };
 
-template <int D>
+// kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
+// window arithmetic.
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -115,8 +120,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
                                                 ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kWarps * C::kWarpBytes);
     int *s_nvalid = reinterpret_cast<int *>(bars + C::kWarps * S);
-    int *s_prefix = s_nvalid + C::kWarps * S;
+    int *s_lo = s_nvalid + C::kWarps * S;  // [warp][stage] first key of the page in the window
+    int *s_prefix = s_lo + C::kWarps * S;
     int *s_len = s_prefix + a.B + 1;
+    int *s_first = s_len + a.B;
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     }
     if (lane < S) mbar_init(&bars[wid * S + lane], 1);
     fence_mbar_init();
-    scan_pages(a, s_prefix, s_len);  // contains __syncthreads
+    scan_pages(a, s_prefix, s_len, s_first);  // contains __syncthreads
 
     const int64_t T = (int64_t)a.Hkv * s_prefix[a.B];
     int64_t per = (T + a.total_warps - 1) / a.total_warps;
@@ -145,6 +152,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     uint8_t *wbuf = smem + wid * C::kWarpBytes;
     uint64_t *wbar = bars + wid * S;
     int *wnv = s_nvalid + wid * S;
+    int *wlo = s_lo + wid * S;
 
     // locate the first unit: the last sequence whose first unit is <= u_begin
     Cursor cur;
@@ -184,7 +192,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             win_b = c.b;
             win_p0 = p0;
             const int pp = p0 + lane;
-            win_val = pp < c.pb ? a.block_table[(int64_t)c.b * a.max_pages + pp] : -1;
+            const int first = kWindow ? s_first[c.b] : 0;
+            win_val = pp < c.pb ? a.block_table[(int64_t)c.b * a.max_pages + first + pp] : -1;
         }
         return __shfl_sync(0xffffffffu, win_val, c.p - p0);
     };
@@ -194,8 +203,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         const int pg = page_of(c);
         const bool ok = pg >= 0 && pg < a.num_pages;
         if (lane == 0) {
-            const int nv = ok ? min(kPageSize, s_len[c.b] - kPageSize * c.p) : 0;
+            const int page = (kWindow ? s_first[c.b] : 0) + c.p;  // page index within the sequence
+            const int nv = ok ? min(kPageSize, s_len[c.b] - kPageSize * page) : 0;
             wnv[stage] = nv;
+            // keys before the sliding window in this page are hidden
+            if (kWindow) wlo[stage] = max(0, s_len[c.b] - a.window - kPageSize * page);
             uint64_t *bar = &wbar[stage];
             uint8_t *kb = wbuf + stage * C::kStageBytes;
             uint8_t *vb = kb + C::kPageBytes;
@@ -243,6 +255,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         uint8_t *kb = wbuf + stage * C::kStageBytes;
         uint8_t *vb = kb + C::kPageBytes;
         const int nv = wnv[stage];
+        const int klo = kWindow ? wlo[stage] : 0;
         if (nv < kPageSize) {
             // rows past the sequence end (or a skipped page) may hold anything,
             // even NaN; P is 0 there but 0 * NaN is not 0, so clear those V rows
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int tok = n * 8 + tc + (i & 1);
-                s[n][i] = tok < nv ? s[n][i] * a.scale_log2 : -INFINITY;
+                s[n][i] = (tok < nv && tok >= klo) ? s[n][i] * a.scale_log2 : -INFINITY;
             }
         const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
         const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
@@ -474,20 +487,26 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, decode_splitkv_kernel<D>);
-    if (e != cudaSuccess) return e;
-    const int ceiling = optin - (int)fa.sharedSizeBytes;  // dynamic + static <= opt-in maximum
-    if (bytes > ceiling) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(decode_splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ceiling);
-    if (e != cudaSuccess) return e;
-    int sms = 0, occ = 0;
+    // both variants (with and without a window) get the same grid: the split plan and the
+    // workspace layout depend on it
+    int sms = 0, occ = 1 << 30;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_splitkv_kernel<D>,
-                                                      C::kThreads, bytes);
-    if (e != cudaSuccess) return e;
+    const void *kernels[2] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, false>),
+                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true>)};
+    for (const void *k : kernels) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+        const int ceiling = optin - (int)fa.sharedSizeBytes;  // dynamic + static <= opt-in maximum
+        if (bytes > ceiling) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ceiling);
+        if (e != cudaSuccess) return e;
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, C::kThreads, bytes);
+        if (e != cudaSuccess) return e;
+        occ = min(occ, o);
+    }
     if (occ < 1) return cudaErrorInvalidConfiguration;
     *ctas = sms * occ;
     *warps = C::kWarps;
@@ -533,10 +552,15 @@ cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_
 cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap &kmap,
                                   const CUtensorMap &vmap, int ctas, int smem_bytes,
                                   cudaStream_t stream) {
-    if (D == 64)
-        decode_splitkv_kernel<64><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+    const bool w = a.window > 0;
+    if (D == 64 && w)
+        decode_splitkv_kernel<64, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+    else if (D == 64)
+        decode_splitkv_kernel<64, false><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+    else if (w)
+        decode_splitkv_kernel<128, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
     else
-        decode_splitkv_kernel<128><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+        decode_splitkv_kernel<128, false><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
     return cudaGetLastError();
 }
 

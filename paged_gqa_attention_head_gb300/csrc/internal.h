@@ -24,6 +24,7 @@ struct DecodeArgs {
     void *out;                   // bf16 [B, Hq, D]
     float *lse;                  // [B, Hq] or nullptr
     int B, Hq, Hkv, G, num_pages, max_pages;
+    int window;             // sliding window (keys at the last `window` positions); 0: none
     int total_warps;        // warps of the split-KV grid
     uint32_t *status;       // workspace header
     int32_t *ws_prefix;     // [B + 1] pages-per-sequence prefix sum (written by CTA 0)
@@ -62,6 +63,7 @@ struct PrefillArgs {
     void *out;   // bf16 [T, Hq, D]
     float *lse;  // [T, Hq] or nullptr
     int T, n, Hq, Hkv, G, D, num_pages, max_pages;
+    int window;  // sliding window (keys at the query's last `window` positions); 0: none
     uint32_t *status;
 };
 // Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.

@@ -313,10 +313,15 @@ __device__ __forceinline__ int item_rank(int k) {
     return k * G + ((k & 1) ? G - 1 - b : b);
 }
 
+// Key tiles of an item: prefix tiles 0..n_pre-1 (keys 128t .. 128t+127 of the prefix),
+// then the new-token tiles n_pre + k (keys P + 128k ..), up to the diagonal n_pre + qb.
+// A sliding window hides every tile before t0 from all 128 rows: the item visits tiles
+// t0 .. n_pre + qb, n_kv of them.
 struct ItemGeom {
-    int row0, L, P, n_pre, n_kv, g;
+    int row0, L, P, n_pre, t0, n_kv, g;
 };
 
+template <bool kWindow>
 __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it) {
     ItemGeom q;
     q.row0 = a.cu_seqlens[it.req];
@@ -328,12 +333,20 @@ __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it
         q.P = q.P < 0 ? 0 : (q.P > cap ? cap : q.P);
     }
     q.n_pre = (q.P + kBN - 1) / kBN;
-    q.n_kv = q.n_pre + it.qb + 1;
+    q.t0 = 0;
+    if (kWindow) {
+        // first key the block's first row sees: its position P + 128 qb, minus W - 1
+        const int lb = q.P + it.qb * kBM - a.window + 1;
+        if (lb > 0) q.t0 = lb < q.P ? lb / kBN : q.n_pre + (lb - q.P) / kBN;
+    }
+    q.n_kv = q.n_pre + it.qb + 1 - q.t0;
     q.g = it.h0 / a.G;
     return q;
 }
 
-template <int D>
+// kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
+// window arithmetic.
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kpmap,
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of(a, it);
+            const ItemGeom gm = geom_of<kWindow>(a, it);
             if (lane == 0 && a.prefix_lens) {
                 const int Praw = a.prefix_lens[it.req];
                 if (Praw < 0 || Praw > a.max_pages * kPageSize)
@@ -440,11 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int s = kv % NS, u = kv / NS;
-                // prefix tile: lane p < 8 looks up page 8j + p (issued before the wait below so
+                const int tt = kWindow ? gm.t0 + j : j;  // key tile
+                // prefix tile: lane p < 8 looks up page 8tt + p (issued before the wait below so
                 // the load overlaps it); nrow = its valid rows, pg = -1 for a missing page
                 int nrow = 0, pg = -1;
-                if (j < gm.n_pre && lane < 8) {
-                    const int page = j * 8 + lane;
+                if (tt < gm.n_pre && lane < 8) {
+                    const int page = tt * 8 + lane;
                     nrow = min(kPageSize, max(0, gm.P - page * kPageSize));
                     if (nrow > 0) {
                         pg = a.prefix_block_table[(int64_t)it.req * a.max_pages + page];
@@ -461,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t *kt = sK + s * C::kKVBytes;
                 uint8_t *vt = sV + s * C::kKVBytes;
-                if (j < gm.n_pre) {
+                if (tt < gm.n_pre) {
                     // eight pages of 16 tokens: each whole valid page by a TMA issued from its
                     // own lane, the others (ragged tail, missing page) by the warp
                     const bool full = nrow == kPageSize && pg >= 0;
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(&bars.v_full[s]);
                     }
                 } else if (lane == 0) {
-                    const int row = gm.row0 + (j - gm.n_pre) * kBN;
+                    const int row = gm.row0 + (tt - gm.n_pre) * kBN;
                     mbar_arrive_expect_tx(&bars.k_full[s], C::kKVBytes);
 #pragma unroll
                     for (int hf = 0; hf < C::kHalves; ++hf)
@@ -546,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status));
         };
         int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
-        int n_kv = rank < n_items ? geom_of(a, item_of(a, wl, rank)).n_kv : 0;
+        int n_kv = rank < n_items ? geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv : 0;
         uint32_t i = 0;
         int b = 0, pb = 0;            // i % NBS, i % NBP
         uint32_t use = 0, use_p = 0;  // i / NBS, i / NBP
@@ -612,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++j == n_kv) {
                     j = 0;
                     rank = item_rank(++k);
-                    if (rank < n_items) n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
+                    if (rank < n_items) n_kv = geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv;
                 }
             }
             continue;
@@ -632,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kv = 0, k = 0;
         bool ok = true;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
-            const int n_kv = geom_of(a, item_of(a, wl, rank)).n_kv;
+            const int n_kv = geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv;
             for (int j = 0; j < n_kv; ++j, ++kv) {
                 const int st = kv % NS;
                 if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
@@ -706,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = x < ntiles;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of(a, it);
+            const ItemGeom gm = geom_of<kWindow>(a, it);
             const int h = it.h0 + x;
             const int t = it.qb * kBM + r;  // position among the request's new tokens
             const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
@@ -723,13 +737,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++tcount;
                 tc::fence_after_sync();
-                int ncols;  // keys of this tile the row may see
-                if (j < gm.n_pre)
-                    ncols = min(kBN, gm.P - j * kBN);
-                else if (j - gm.n_pre == it.qb)
+                const int tt = kWindow ? gm.t0 + j : j;  // key tile
+                // keys lo .. ncols-1 of this tile are the row's to see
+                int ncols;
+                if (tt < gm.n_pre)
+                    ncols = min(kBN, gm.P - tt * kBN);
+                else if (tt - gm.n_pre == it.qb)
                     ncols = r + 1;  // diagonal tile: keys 0..r
                 else
                     ncols = kBN;
+                int lo = 0;
+                if (kWindow) {  // keys at positions <= (P + t) - W are outside the window
+                    const int key0 = tt < gm.n_pre ? tt * kBN : gm.P + (tt - gm.n_pre) * kBN;
+                    lo = gm.P + t - a.window + 1 - key0;
+                }
                 // the whole S row of this tile
                 uint32_t sv[kBN];
 #pragma unroll
@@ -741,10 +762,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_free[b]);
                 }
-                if (ncols < kBN) {  // diagonal, ragged or prefix-tail tile: hide invisible keys
+                if (ncols < kBN || lo > 0) {  // diagonal, ragged, prefix-tail or window edge
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (c >= ncols) sv[c] = 0xFF800000u;  // -inf
+                        if (c >= ncols || c < lo) sv[c] = 0xFF800000u;  // -inf
                 }
                 // row max: eight chains of three-input maxima over 16 keys each
                 float mx8[8];
@@ -908,19 +929,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kWindow>
 cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,
                      const CUtensorMap &vmap, const CUtensorMap &kpmap, const CUtensorMap &vpmap,
                      cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWindow>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     int device = 0, sms = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) return e;
     // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more)
-    prefill_kernel<D><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
+    prefill_kernel<D, kWindow><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
     return cudaGetLastError();
 }
 
@@ -929,8 +950,13 @@ cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtens
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const CUtensorMap &kpmap,
                            const CUtensorMap &vpmap, cudaStream_t stream) {
-    if (a.D == 64) return launch_d<64>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
-    if (a.D == 128) return launch_d<128>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+    const bool w = a.window > 0;
+    if (a.D == 64)
+        return w ? launch_d<64, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                 : launch_d<64, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+    if (a.D == 128)
+        return w ? launch_d<128, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                 : launch_d<128, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
     return cudaErrorNotSupported;
 }
 

@@ -158,9 +158,13 @@ class DecodeInputs:
     def seq_lens(self) -> torch.Tensor:
         return self.cache.lens
 
-    def kv_bytes(self) -> int:
-        """Bytes of K and V the attention must read: every cached token, both tensors."""
-        return int(self.cache.lens.sum()) * 2 * self.num_kv_heads * self.head_dim * 2
+    def kv_bytes(self, window: int = 0) -> int:
+        """Bytes of K and V the attention must read: every cached token (with a sliding
+        window, the last `window` of each sequence), both tensors."""
+        lens = self.cache.lens.long()
+        if window > 0:
+            lens = lens.clamp(max=window)
+        return int(lens.sum()) * 2 * self.num_kv_heads * self.head_dim * 2
 
 
 def make_decode(lens_spec, batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
@@ -189,14 +193,22 @@ class PrefillInputs:
     head_dim: int
     prefix_lens: list[int] = field(default_factory=list)
 
-    def causal_pairs(self) -> int:
-        """Number of (query, key) pairs the attention visits: prefix keys plus the causal triangle."""
+    def causal_pairs(self, window: int = 0) -> int:
+        """Number of (query, key) pairs the attention visits: prefix keys plus the causal
+        triangle; with a sliding window, min(window, position + 1) keys per query."""
         pre = self.prefix_lens or [0] * len(self.new_lens)
-        return sum(L * P + L * (L + 1) // 2 for L, P in zip(self.new_lens, pre))
+        if window <= 0:
+            return sum(L * P + L * (L + 1) // 2 for L, P in zip(self.new_lens, pre))
+        total = 0
+        for L, P in zip(self.new_lens, pre):
+            # query t sees min(window, P + t + 1) keys: the ramp part, then window each
+            ramp = max(0, min(L, window - P))  # queries with P + t + 1 <= window
+            total += sum(P + t + 1 for t in range(ramp)) + (L - ramp) * window
+        return total
 
-    def flops(self) -> int:
+    def flops(self, window: int = 0) -> int:
         """2 flops per multiply-add, for Q.K^T and P.V over the visited pairs."""
-        return 4 * self.head_dim * self.num_qo_heads * self.causal_pairs()
+        return 4 * self.head_dim * self.num_qo_heads * self.causal_pairs(window)
 
 
 def make_prefill(new_lens: list[int], num_qo_heads: int, num_kv_heads: int, head_dim: int,

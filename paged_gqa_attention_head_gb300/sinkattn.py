@@ -30,7 +30,7 @@ _P, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_si
 class PagedDesc(ctypes.Structure):
     _fields_ = [("num_seqs", _I32), ("num_qo_heads", _I32), ("num_kv_heads", _I32),
                 ("head_dim", _I32), ("page_size", _I32), ("num_pages", _I32),
-                ("max_pages_per_seq", _I32)]
+                ("max_pages_per_seq", _I32), ("window", _I32)]
 
 
 _DP = ctypes.POINTER(PagedDesc)
@@ -122,9 +122,11 @@ def workspace(nbytes: int, device: torch.device, tag: str = "default") -> torch.
 
 
 def paged_desc(num_seqs, num_qo_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
-               page_size=PAGE_SIZE) -> PagedDesc:
+               page_size=PAGE_SIZE, window=0) -> PagedDesc:
+    """window > 0: sliding window (each query sees the keys at its last `window`
+    positions); 0: full attention."""
     return PagedDesc(num_seqs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
-                     max_pages_per_seq)
+                     max_pages_per_seq, int(window))
 
 
 _ws_sizes: dict = {}
@@ -158,7 +160,7 @@ def get_status(ws: torch.Tensor) -> int:
 
 
 def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
-                 want_lse):
+                 want_lse, window=0):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
@@ -183,7 +185,7 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
     elif lse is not None:
         _need(lse, "lse", torch.float32, dev, 2)
-    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1])
+    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window)
     nbytes = decode_workspace_size(desc)
     if ws is None:
         ws = workspace(nbytes, dev)
@@ -194,10 +196,11 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None, lse=None,
-           workspace_buf=None, return_lse=True):
-    """Split-KV paged decode with sinks (sinkattn_decode).  Returns (out, lse)."""
+           workspace_buf=None, return_lse=True, window=0):
+    """Split-KV paged decode with sinks (sinkattn_decode).  window > 0: sliding window.
+    Returns (out, lse)."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
-                                             scale, out, lse, workspace_buf, return_lse)
+                                             scale, out, lse, workspace_buf, return_lse, window)
     _check(load().sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                   _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                   ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(q.device)),
@@ -206,10 +209,10 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, o
 
 
 def decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
-                   lse=None, workspace_buf=None, return_lse=True):
+                   lse=None, workspace_buf=None, return_lse=True, window=0):
     """First decode kernel only (sinkattn_decode_splitkv); follow with decode_merge."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
-                                             scale, out, lse, workspace_buf, return_lse)
+                                             scale, out, lse, workspace_buf, return_lse, window)
     _check(load().sinkattn_decode_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                           _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                           ctypes.byref(desc), _ptr(ws), ws.numel(),
@@ -227,8 +230,9 @@ def decode_merge(seq_lens, sinks, out, lse, desc, ws):
 
 def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
             prefix_block_table=None, prefix_lens=None, out=None, lse=None, workspace_buf=None,
-            return_lse=True):
-    """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  Returns (out, lse)."""
+            return_lse=True, window=0):
+    """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  window > 0:
+    sliding window.  Returns (out, lse)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k, "k", torch.bfloat16, dev, 3)
@@ -252,7 +256,7 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
-    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp)
+    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window)
     nbytes = prefill_workspace_size(desc)
     ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -285,7 +289,7 @@ def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages, worksp
 
 
 def decode_noalloc(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
-                   lse=None, status=None):
+                   lse=None, status=None, window=0):
     """sinkattn_decode_noalloc: the same decode with the library's fixed scratch array
     instead of a workspace, for callers that cannot allocate device memory.  Calls on
     one device must not overlap on the GPU.  status: optional int32/uint32 device
@@ -299,7 +303,7 @@ def decode_noalloc(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1])
+    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(load().sinkattn_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                           _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
