@@ -286,26 +286,32 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     rows = {}
     reps = 20
 
-    def decode_row(name):
+    def decode_row(name, window=0):
         w = inputs.make_workload(name, seed=0)
         c = w.cache
         args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
                 c.lens.to(dev), None if w.sinks is None else w.sinks.to(dev), w.scale)
         out = torch.empty_like(args[0])
         lse = torch.empty(args[0].shape[:2], dtype=torch.float32, device=dev)
-        f = lambda: sa.decode(*args, out=out, lse=lse)  # noqa: E731
+        f = lambda: sa.decode(*args, out=out, lse=lse, window=window)  # noqa: E731
         for _ in range(3):
             f()
         ms = time_loop(torch, f, reps, stream) / reps
-        gbs = w.kv_bytes() / (ms * 1e-3) / 1e9
+        nbytes = w.kv_bytes(window)
+        gbs = nbytes / (ms * 1e-3) / 1e9
         r = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
-             "kv_bytes": w.kv_bytes(), "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1)}
+             "kv_bytes": nbytes, "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1)}
+        if window:
+            r["window"] = window
         del args, out, lse, w
         torch.cuda.empty_cache()
         return r
 
     for name in ("qwen3_decode", "longctx_decode"):
         rows[name] = decode_row(name)
+    # a gpt-oss sliding-window layer (128 positions): the last 128 keys of each sequence,
+    # ~9 MB of KV, so the launch and the first copies dominate
+    rows["gptoss_decode_window128"] = decode_row(HEADLINE, window=128)
 
     # append of the prefill workload's K/V into HND pages
     a = inputs.make_append([4096, 2048, 1024, 512], [0, 0, 0, 0], 8, 64, seed=0)
@@ -320,28 +326,33 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     rows["gptoss_append"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
                              "bytes": moved}
 
-    for name in ("gptoss_prefill", "longctx_chunked"):
+    for name, window in (("gptoss_prefill", 0), ("longctx_chunked", 0), ("gptoss_prefill", 128)):
         p = inputs.make_workload(name, seed=0)
+        key = name if not window else f"{name}_window{window}"
         kw = {}
         if p.prefix is not None:
             kw = dict(k_pages=p.prefix.k_pages.to(dev), v_pages=p.prefix.v_pages.to(dev),
                       prefix_block_table=p.prefix.block_table.to(dev),
                       prefix_lens=p.prefix.lens.to(dev))
         pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+        kw["window"] = window
         try:
             sa.prefill(*pargs, **kw)
         except sa.SinkAttnError as e:
-            rows[name] = {"unavailable": str(e)}
+            rows[key] = {"unavailable": str(e)}
             continue
         f = lambda: sa.prefill(*pargs, **kw)  # noqa: E731
         for _ in range(3):
             f()
         ms = time_loop(torch, f, reps, stream) / reps
-        tf = p.flops() / (ms * 1e-3) / 1e12
-        rows[name] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
-                      "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": p.flops(),
-                      "peak_source": f"{peak_src} bf16_tflops (burst)",
-                      "traffic": traffic_for("prefill_kernel", name)}
+        flops = p.flops(window)
+        tf = flops / (ms * 1e-3) / 1e12
+        rows[key] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
+                     "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": flops,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "traffic": None if window else traffic_for("prefill_kernel", name)}
+        if window:
+            rows[key]["window"] = window
     return rows
 
 
