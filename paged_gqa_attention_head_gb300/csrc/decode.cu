@@ -32,7 +32,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMinUnitsPerWarp = 16;  // pages per warp at least (keeps partials few)
+constexpr int kMinUnitsPerWarp = 4;  // pages per warp at least (keeps partials few)
 
 template <int D>
 struct DecodeCfg {
