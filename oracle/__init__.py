@@ -51,6 +51,14 @@ def _load():
         lib.oracle_merge.restype = None
         lib.oracle_online.argtypes = [P, P, P, I, D, D, I64, I, I64, P, P]
         lib.oracle_online.restype = None
+        lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, D, I, I, I, I, I, I64, I, I, P, P, P]
+        lib.oracle_decode_fp8.restype = I
+        lib.oracle_append_kv_fp8.argtypes = [P, P, P, P, P, I, P, P, I, I64, I, I, I, P, P]
+        lib.oracle_append_kv_fp8.restype = I
+        lib.oracle_e4m3_codes.argtypes = [P, I64, P]
+        lib.oracle_e4m3_codes.restype = None
+        lib.oracle_e4m3_values.argtypes = [P, I64, P]
+        lib.oracle_e4m3_values.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = I
         _lib = lib
@@ -79,6 +87,16 @@ def _f32(t) -> Optional[np.ndarray]:
         return None
     a = t if isinstance(t, np.ndarray) else t.detach().cpu().float().numpy()
     return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _u8(t) -> np.ndarray:
+    """uint8 / float8_e4m3fn torch tensor or uint8 array -> contiguous uint8 numpy array."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint8
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype in (torch.uint8, torch.float8_e4m3fn), t.dtype
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.uint8).numpy())
 
 
 def _ptr(a) -> Optional[int]:
@@ -155,6 +173,62 @@ def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages):
     return kp, vp
 
 
+def e4m3_values(codes) -> np.ndarray:
+    """Value of each E4M3 code (float64; NaN for the NaN codes)."""
+    c = _u8(codes)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_values(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_codes(y) -> np.ndarray:
+    """Nearest E4M3 code of each float32 (ties to even, saturating to +-448, NaN kept)."""
+    a = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _load().oracle_e4m3_codes(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks, scale: float,
+               select: Optional[np.ndarray] = None, window: int = 0):
+    """Decode over an FP8 E4M3 cache: pages uint8 [num_pages,Hkv,P,D] of codes, element
+    value scale[g] * e4m3(code) with fp32 k_scale / v_scale [Hkv] (None: 1).  Otherwise as
+    decode(); returns (out [B,Hq,D], lse [B,Hq]) in float64."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _u8(k_pages), _u8(v_pages)
+    B, Hq, D = qb.shape
+    num_pages, Hkv, P, D2 = kb.shape
+    assert D == D2
+    bt, sl, sk = _i32(block_table), _i32(seq_lens), _f32(sinks)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    out = np.full((B, Hq, D), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
+    rc = lib.oracle_decode_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+                               _ptr(sk), float(scale), B, Hq, Hkv, D, P, num_pages, bt.shape[1],
+                               int(window), _ptr(sel), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_fp8 rejected its inputs ({rc})")
+    return out, lse
+
+
+def append_kv_fp8(k, v, k_scale, v_scale, cu_seqlens, block_table, start_pos, k_pages, v_pages):
+    """Quantise new bf16 rows to E4M3 codes (x / scale[g], nearest, saturating) and scatter
+    them into copies of the uint8 pages; returns (k_pages, v_pages) as uint8 arrays."""
+    lib = _load()
+    kb, vb = _bits(k), _bits(v)
+    kp, vp = _u8(k_pages).copy(), _u8(v_pages).copy()
+    num_pages, Hkv, P, D = kp.shape
+    cu, bt, sp = _i32(cu_seqlens), _i32(block_table), _i32(start_pos)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    rc = lib.oracle_append_kv_fp8(_ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs), _ptr(cu), cu.shape[0] - 1,
+                                  _ptr(bt), _ptr(sp), bt.shape[1], num_pages, Hkv, D, P, _ptr(kp),
+                                  _ptr(vp))
+    if rc != 0:
+        raise ValueError("oracle_append_kv_fp8 rejected its inputs")
+    return kp, vp
+
+
 def partial(q, k, v, scale: float, j0: int, j1: int):
     """Sink-free state (m, l, acc[D]) of contiguous keys [j0, j1); q [D], k/v [n, D] bf16."""
     lib = _load()
@@ -205,7 +279,8 @@ class using_library:
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_decode", "oracle_prefill", "oracle_append_kv", "oracle_partial",
-                     "oracle_merge", "oracle_online", "oracle_max_threads"):
+                     "oracle_merge", "oracle_online", "oracle_max_threads", "oracle_decode_fp8",
+                     "oracle_append_kv_fp8", "oracle_e4m3_codes", "oracle_e4m3_values"):
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = lib

@@ -376,3 +376,180 @@ void oracle_online(const uint16_t *q, const uint16_t *k, const uint16_t *v, int 
     oracle_merge(S, m, den, acc, D, -INFINITY, out, lse);
     free(acc);
 }
+
+/* ------------------------------------------------------------------------------
+ * FP8 KV cache.  The pages name an FP8 serving precision ("GPT-OSS on Day 0",
+ * section "GPT-OSS on Hopper") and an 8-bit KV-cache type (TensorSharp gptoss.md
+ * section 10, "Memory and KV cache strategy") but give no scale convention.  The
+ * reading taken here: each K/V element is one OCP FP8 E4M3 code (1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN;
+ * largest finite 448), and its value is scale[g] * e4m3(code) with one fp32 scale
+ * per KV head g, separately for K and for V.
+ *
+ * Quantisation (the fp8 append): x is the bf16 value as float; y = x / scale[g] in
+ * IEEE single precision (round to nearest); the code is y rounded to the nearest
+ * E4M3 value, ties to the even mantissa, with finite overflow and infinities
+ * saturated to +-448 and NaN kept NaN (0x7F with the sign bit of y).
+ */
+
+/* The value of an E4M3 code, from the format's definition. */
+double oracle_e4m3_value(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+    else
+        mag = ldexp(8.0 + m, e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* Nearest E4M3 code of a float (ties to even, saturating, NaN preserved). */
+uint8_t oracle_e4m3_code(float y) {
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    if (isnan(y)) return (uint8_t)(sign | 0x7F);
+    double a = fabs((double)y);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E); /* saturation: 448 is code 0x7E */
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; rint rounds half to even */
+        double q = rint(ldexp(a, 9)); /* 0..8; 8 is the smallest normal, code 0x08 */
+        return (uint8_t)(sign | (uint8_t)q);
+    }
+    int e2;
+    frexp(a, &e2);    /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;   /* a in [2^e, 2^(e+1)), e in [-6, 8] */
+    double q = rint(ldexp(a, 3 - e)); /* 8..16: significand with 3 fraction bits */
+    if (q == 16.0) {
+        q = 8.0;
+        e += 1;
+    }
+    int field = e + 7; /* 1..15 */
+    if (field > 15 || (field == 15 && q - 8.0 > 6.0)) return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | (uint8_t)(field << 3) | (uint8_t)(q - 8.0));
+}
+
+/* attend() over E4M3 rows: the key and value elements are scale * e4m3(code). */
+static void attend_e4m3(const uint16_t *q, int D, double scale, double sink, int64_t n,
+                        const uint8_t *const *krow, const uint8_t *const *vrow, double kscale,
+                        double vscale, double *s, double *out, double *lse) {
+    double top = sink; /* m of the definition */
+    for (int64_t j = 0; j < n; ++j) {
+        double qk = 0.0;
+        for (int d = 0; d < D; ++d)
+            qk += bf16_to_double(q[d]) * (kscale * oracle_e4m3_value(krow[j][d]));
+        s[j] = scale * qk;
+        if (s[j] > top) top = s[j];
+    }
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (top == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double z = exp(sink - top); /* the denominator, starting with the sink's term */
+    for (int64_t j = 0; j < n; ++j) {
+        double e = exp(s[j] - top);
+        z += e;
+        for (int d = 0; d < D; ++d) out[d] += e * (vscale * oracle_e4m3_value(vrow[j][d]));
+    }
+    for (int d = 0; d < D; ++d) out[d] /= z;
+    *lse = top + log(z);
+}
+
+/*
+ * Decode over an FP8 E4M3 cache: oracle_decode with byte pages
+ * k_pages, v_pages uint8 [num_pages, Hkv, P, D] and fp32 scales k_scale, v_scale [Hkv]
+ * (NULL: 1).  Same visible keys, sinks, window and return codes.
+ */
+int oracle_decode_fp8(const uint16_t *q, const uint8_t *k_pages, const uint8_t *v_pages,
+                      const float *k_scale, const float *v_scale, const int32_t *block_table,
+                      const int32_t *seq_lens, const float *sinks, double scale, int B, int Hq,
+                      int Hkv, int D, int P, int64_t num_pages, int max_pages, int window,
+                      const uint8_t *select, double *out, double *lse) {
+    if (Hq % Hkv) return -1;
+    const int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L < 0 || (int64_t)L > (int64_t)max_pages * P) return -1;
+        for (int j = 0; j < (L + P - 1) / P; ++j) {
+            int32_t pg = block_table[(int64_t)b * max_pages + j];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+        if (select && !select[bh]) continue;
+        const int b = (int)(bh / Hq), h = (int)(bh - (int64_t)b * Hq), g = h / G;
+        const int64_t L = seq_lens[b];
+        const int64_t first = (window > 0 && L > window) ? L - window : 0; /* first visible key */
+        const int64_t nk = L - first;
+        const uint8_t **krow = malloc(sizeof(*krow) * (size_t)(nk + 1));
+        const uint8_t **vrow = malloc(sizeof(*vrow) * (size_t)(nk + 1));
+        double *s = malloc(sizeof(double) * (size_t)(nk + 1));
+        if (!krow || !vrow || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int64_t j = first; j < L; ++j) {
+                int64_t pg = block_table[(int64_t)b * max_pages + j / P];
+                int64_t off = ((pg * Hkv + g) * (int64_t)P + j % P) * D;
+                krow[j - first] = k_pages + off;
+                vrow[j - first] = v_pages + off;
+            }
+            attend_e4m3(q + bh * D, D, scale, sink_of(sinks, h), nk, krow, vrow,
+                        k_scale ? (double)k_scale[g] : 1.0, v_scale ? (double)v_scale[g] : 1.0, s,
+                        out + bh * D, lse + bh);
+        }
+        free(krow);
+        free(vrow);
+        free(s);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * Append into an FP8 E4M3 cache: token placement as oracle_append_kv; each element
+ * x (bf16) is stored as oracle_e4m3_code(x / scale[g]), the division in single
+ * precision.  k_scale, v_scale [Hkv] (NULL: 1).
+ */
+int oracle_append_kv_fp8(const uint16_t *k, const uint16_t *v, const float *k_scale,
+                         const float *v_scale, const int32_t *cu_seqlens, int n,
+                         const int32_t *block_table, const int32_t *start_pos, int max_pages,
+                         int64_t num_pages, int Hkv, int D, int P, uint8_t *k_pages,
+                         uint8_t *v_pages) {
+    for (int i = 0; i < n; ++i) {
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
+            int64_t pos = start_pos[i] + (t - cu_seqlens[i]);
+            if (pos < 0 || pos / P >= max_pages) return -1;
+            int32_t pg = block_table[(int64_t)i * max_pages + pos / P];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
+            int64_t pos = start_pos[i] + (t - cu_seqlens[i]);
+            int64_t pg = block_table[(int64_t)i * max_pages + pos / P];
+            for (int g = 0; g < Hkv; ++g) {
+                const float ks = k_scale ? k_scale[g] : 1.0f, vs = v_scale ? v_scale[g] : 1.0f;
+                int64_t off = ((pg * Hkv + g) * (int64_t)P + pos % P) * D;
+                for (int d = 0; d < D; ++d) {
+                    float kx = (float)bf16_to_double(k[(t * Hkv + g) * D + d]);
+                    float vx = (float)bf16_to_double(v[(t * Hkv + g) * D + d]);
+                    k_pages[off + d] = oracle_e4m3_code(kx / ks);
+                    v_pages[off + d] = oracle_e4m3_code(vx / vs);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Element-wise oracle_e4m3_code / oracle_e4m3_value over arrays. */
+void oracle_e4m3_codes(const float *y, int64_t n, uint8_t *codes) {
+    for (int64_t i = 0; i < n; ++i) codes[i] = oracle_e4m3_code(y[i]);
+}
+
+void oracle_e4m3_values(const uint8_t *codes, int64_t n, double *values) {
+    for (int64_t i = 0; i < n; ++i) values[i] = oracle_e4m3_value(codes[i]);
+}

@@ -16,7 +16,11 @@ Recipe (shared by every workload):
     permutation, so a sequence's pages are scattered through the pool;
   * the unused slots of each sequence's last page, the distractor pages and
     the unused block-table columns are poisoned (NaN values, page index -1) so
-    that any read beyond a sequence shows up in the results.
+    that any read beyond a sequence shows up in the results;
+  * FP8 E4M3 caches: per-KV-head scales s_g = (4.5 / 448) * (1 + g / (2 Hkv)),
+    codes = torch's float8_e4m3fn cast of the standard normal float32 values
+    divided by s_g and clipped to [-448, 448]; poisoned slots hold the NaN code
+    0x7F.
 
 Random streams are keyed by (seed, stream id, chunk index) through numpy's
 SeedSequence, so a tensor's contents do not depend on the thread count or on
@@ -36,6 +40,7 @@ import torch
 PAGE_SIZE = 16
 _CHUNK = 1 << 22  # elements per independently seeded chunk
 BF16_NAN_BITS = 0x7FC0
+E4M3_NAN_CODE = 0x7F
 
 # stream ids: one per kind of tensor so that draws are independent
 _S_LENS, _S_Q, _S_K, _S_V, _S_SINK, _S_PERM, _S_KNEW, _S_VNEW, _S_PREFIX = range(9)
@@ -84,9 +89,43 @@ def normal_bf16(shape, seed: int, stream: int) -> torch.Tensor:
     return out.reshape(shape)
 
 
+def fp8_head_scales(num_kv_heads: int) -> torch.Tensor:
+    """Per-KV-head scales of the synthetic FP8 caches (float32 [Hkv])."""
+    g = torch.arange(num_kv_heads, dtype=torch.float64)
+    return ((4.5 / 448.0) * (1.0 + g / (2 * num_kv_heads))).to(torch.float32)
+
+
+def normal_e4m3(shape, head_scales: torch.Tensor, seed: int, stream: int) -> torch.Tensor:
+    """E4M3 codes (uint8) of standard normal float32 values divided by the scale of
+    their KV head, for pages [num_pages, Hkv, 16, D]; chunked like normal_bf16."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    Hkv, row = shape[1], shape[2] * shape[3]
+    inv_rows = (1.0 / head_scales.double()).numpy().astype(np.float32)
+    out = torch.empty(n, dtype=torch.uint8)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def work(i: int) -> None:
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        buf = _rng(seed, stream, i).standard_normal(hi - lo, dtype=np.float32)
+        head = (np.arange(lo, hi, dtype=np.int64) // row) % Hkv
+        buf = np.clip(buf * inv_rows[head], -448.0, 448.0).astype(np.float32)
+        out[lo:hi] = torch.from_numpy(buf).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    if nchunks <= 1:
+        if n:
+            work(0)
+    else:
+        with ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out.reshape(shape)
+
+
 def poison_rows_(t: torch.Tensor) -> None:
-    """Fill a bf16 tensor (view) with NaN."""
-    t.view(torch.int16).fill_(BF16_NAN_BITS)
+    """Fill a bf16 tensor (view) with NaN; a uint8 (E4M3 code) tensor with the NaN code."""
+    if t.dtype == torch.uint8:
+        t.fill_(E4M3_NAN_CODE)
+    else:
+        t.view(torch.int16).fill_(BF16_NAN_BITS)
 
 
 def draw_lengths(spec, count: int, seed: int) -> list[int]:
@@ -106,18 +145,25 @@ def draw_lengths(spec, count: int, seed: int) -> list[int]:
 
 @dataclass
 class PagedCache:
-    """KV pages [num_pages, Hkv, 16, D] bf16 plus the block table of each sequence."""
+    """KV pages [num_pages, Hkv, 16, D] (bf16, or uint8 E4M3 codes with per-head
+    scales) plus the block table of each sequence."""
     k_pages: torch.Tensor
     v_pages: torch.Tensor
     block_table: torch.Tensor  # [num_seqs, max_pages_per_seq] int32, unused = -1
     lens: torch.Tensor  # [num_seqs] int32 tokens held in the pages
     num_pages: int = 0
+    k_scale: Optional[torch.Tensor] = None  # [Hkv] float32 (FP8 caches only)
+    v_scale: Optional[torch.Tensor] = None
+
+    @property
+    def fp8(self) -> bool:
+        return self.k_pages.dtype == torch.uint8
 
 
 def make_paged_cache(lens: list[int], num_kv_heads: int, head_dim: int, seed: int,
                      distractor_frac: float = 0.05, poison: bool = True,
                      max_pages_per_seq: Optional[int] = None, k_stream: int = _S_K,
-                     v_stream: int = _S_V) -> PagedCache:
+                     v_stream: int = _S_V, kv_dtype: str = "bf16") -> PagedCache:
     npages_seq = [(L + PAGE_SIZE - 1) // PAGE_SIZE for L in lens]
     used = sum(npages_seq)
     num_pages = used + int(math.ceil(distractor_frac * used))
@@ -125,8 +171,16 @@ def make_paged_cache(lens: list[int], num_kv_heads: int, head_dim: int, seed: in
     maxp = max_pages_per_seq if max_pages_per_seq is not None else max(1, max(npages_seq, default=1))
     perm = _rng(seed, _S_PERM).permutation(num_pages).astype(np.int64)
     shape = (num_pages, num_kv_heads, PAGE_SIZE, head_dim)
-    k_pages = normal_bf16(shape, seed, k_stream)
-    v_pages = normal_bf16(shape, seed, v_stream)
+    ks = vs = None
+    if kv_dtype == "fp8":
+        ks = fp8_head_scales(num_kv_heads)
+        vs = (ks * 1.25).to(torch.float32)
+        k_pages = normal_e4m3(shape, ks, seed, k_stream)
+        v_pages = normal_e4m3(shape, vs, seed, v_stream)
+    else:
+        assert kv_dtype == "bf16", kv_dtype
+        k_pages = normal_bf16(shape, seed, k_stream)
+        v_pages = normal_bf16(shape, seed, v_stream)
     bt = torch.full((len(lens), maxp), -1, dtype=torch.int32)
     cursor = 0
     for b, (L, np_b) in enumerate(zip(lens, npages_seq)):
@@ -139,9 +193,12 @@ def make_paged_cache(lens: list[int], num_kv_heads: int, head_dim: int, seed: in
             poison_rows_(v_pages[last, :, L % PAGE_SIZE:, :])
     if poison and num_pages > used:
         idx = torch.from_numpy(perm[used:])
-        k_pages.view(torch.int16)[idx] = BF16_NAN_BITS
-        v_pages.view(torch.int16)[idx] = BF16_NAN_BITS
-    return PagedCache(k_pages, v_pages, bt, torch.tensor(lens, dtype=torch.int32), num_pages)
+        for pages in (k_pages, v_pages):
+            if kv_dtype == "fp8":
+                pages[idx] = E4M3_NAN_CODE
+            else:
+                pages.view(torch.int16)[idx] = BF16_NAN_BITS
+    return PagedCache(k_pages, v_pages, bt, torch.tensor(lens, dtype=torch.int32), num_pages, ks, vs)
 
 
 @dataclass
@@ -164,14 +221,18 @@ class DecodeInputs:
         lens = self.cache.lens.long()
         if window > 0:
             lens = lens.clamp(max=window)
-        return int(lens.sum()) * 2 * self.num_kv_heads * self.head_dim * 2
+        elem = 1 if self.cache.fp8 else 2
+        return int(lens.sum()) * 2 * self.num_kv_heads * self.head_dim * elem
 
 
 def make_decode(lens_spec, batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                 seed: int = 0, sinks: bool = True, scale: Optional[float] = None,
-                poison: bool = True, distractor_frac: float = 0.05) -> DecodeInputs:
+                poison: bool = True, distractor_frac: float = 0.05,
+                kv_dtype: str = "bf16") -> DecodeInputs:
+    """kv_dtype "bf16" or "fp8" (E4M3 codes with per-KV-head scales)."""
     lens = draw_lengths(lens_spec, batch, seed)
-    cache = make_paged_cache(lens, num_kv_heads, head_dim, seed, distractor_frac, poison)
+    cache = make_paged_cache(lens, num_kv_heads, head_dim, seed, distractor_frac, poison,
+                             kv_dtype=kv_dtype)
     q = normal_bf16((batch, num_qo_heads, head_dim), seed, _S_Q)
     s = torch.from_numpy(normal_f32(num_qo_heads, seed, _S_SINK)) if sinks else None
     sc = scale if scale is not None else 1.0 / math.sqrt(head_dim)
@@ -246,14 +307,14 @@ class AppendInputs:
 
 
 def make_append(new_lens: list[int], start_pos: list[int], num_kv_heads: int, head_dim: int,
-                seed: int = 0) -> AppendInputs:
+                seed: int = 0, kv_dtype: str = "bf16") -> AppendInputs:
     T = sum(new_lens)
     cu = torch.zeros(len(new_lens) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(new_lens, dtype=torch.int64), 0).to(torch.int32)
     k = normal_bf16((T, num_kv_heads, head_dim), seed, _S_KNEW)
     v = normal_bf16((T, num_kv_heads, head_dim), seed, _S_VNEW)
     totals = [s + L for s, L in zip(start_pos, new_lens)]
-    cache = make_paged_cache(totals, num_kv_heads, head_dim, seed, poison=True)
+    cache = make_paged_cache(totals, num_kv_heads, head_dim, seed, poison=True, kv_dtype=kv_dtype)
     return AppendInputs(k, v, cu, torch.tensor(start_pos, dtype=torch.int32), cache)
 
 
@@ -272,6 +333,16 @@ WORKLOADS = {
                            num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True),
     "longctx_chunked": dict(kind="chunked", lens=[512] * 8, prefix_lens=[16384] * 8,
                             num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True),
+    # the decode shapes over an FP8 E4M3 cache
+    "gptoss_decode_fp8": dict(kind="decode", batch=64, lens=("uniform", 512, 8192),
+                              num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,
+                              kv_dtype="fp8"),
+    "qwen3_decode_fp8": dict(kind="decode", batch=128, lens=("uniform", 1024, 32768),
+                             num_qo_heads=64, num_kv_heads=4, head_dim=128, sinks=False,
+                             kv_dtype="fp8"),
+    "longctx_decode_fp8": dict(kind="decode", batch=256, lens=("loguniform", 128, 131072),
+                               num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,
+                               kv_dtype="fp8"),
 }
 
 
@@ -280,7 +351,8 @@ def make_workload(name: str, seed: int = 0):
     kind = w.pop("kind")
     if kind == "decode":
         return make_decode(w["lens"], w["batch"], w["num_qo_heads"], w["num_kv_heads"],
-                           w["head_dim"], seed=seed, sinks=w["sinks"])
+                           w["head_dim"], seed=seed, sinks=w["sinks"],
+                           kv_dtype=w.get("kv_dtype", "bf16"))
     if kind == "prefill":
         return make_prefill(w["lens"], w["num_qo_heads"], w["num_kv_heads"], w["head_dim"],
                             seed=seed, sinks=w["sinks"])

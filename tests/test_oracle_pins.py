@@ -12,7 +12,13 @@ Each pin ties the oracle to something it does not share code with:
   * the append scatter read back through the block table;
   * sliding window: SDPA on the last W keys sliced out explicitly (decode) or with
     a band mask built from the window's definition (prefill, chunked), a window of
-    one key against the closed form, a window at least the length against no window.
+    one key against the closed form, a window at least the length against no window;
+  * FP8 E4M3 cache: the code table against torch's float8_e4m3fn and the format's
+    closed forms; the rounding against torch's cast (in range), exact midpoints
+    (ties to the even code) and saturation; decode with power-of-two scales equal,
+    bit for bit, to the bf16 decode of the same values; decode with arbitrary
+    per-head scales against SDPA on torch-dequantised keys and values; the
+    quantising append against torch's cast, slot by slot.
 
 test_planted_mistakes_are_caught compiles copies of the oracle source with one
 plausible mistake each (dropped sink term, wrong GQA head, off-by-one slot, sign
@@ -340,6 +346,112 @@ def pin_append_roundtrip(o):
     assert np.array_equal(kp.transpose(0, 2, 1, 3)[keep], k_old.transpose(0, 2, 1, 3)[keep])
 
 
+def _dequant_pages(pages_u8, scales):
+    """torch (library) dequantisation of E4M3 pages [N, Hkv, 16, D] -> float64."""
+    vals = pages_u8.view(torch.float8_e4m3fn).to(torch.float64)
+    return vals * scales.to(torch.float64).view(1, -1, 1, 1)
+
+
+def pin_e4m3_table(o):
+    codes = np.arange(256, dtype=np.uint8)
+    v = o.e4m3_values(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(v, ref)  # NaN positions must agree too
+    closed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+              0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0, 0xB8: -1.0,
+              0xFE: -448.0}
+    for c, x in closed.items():
+        assert v[c] == x, (hex(c), v[c], x)
+    assert math.copysign(1.0, v[0x80]) < 0 and v[0x80] == 0.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert np.all(np.diff(v[:0x7F]) > 0)  # positive codes increase strictly
+
+
+def pin_e4m3_rounding(o):
+    pos = np.arange(0x7F, dtype=np.uint8)  # every finite non-negative code
+    vals = torch.from_numpy(pos).view(torch.float8_e4m3fn).float().numpy()
+    np.testing.assert_array_equal(o.e4m3_codes(vals), pos)
+    np.testing.assert_array_equal(o.e4m3_codes(-vals[1:]), pos[1:] | 0x80)
+    # exact midpoints go to the even code; one float32 step either side goes to the nearer one
+    mid = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(np.float32)
+    lo_c, hi_c = pos[:-1], pos[1:]
+    even = np.where(lo_c % 2 == 0, lo_c, hi_c)
+    np.testing.assert_array_equal(o.e4m3_codes(mid), even)
+    np.testing.assert_array_equal(o.e4m3_codes(np.nextafter(mid, np.float32(0))), lo_c)
+    np.testing.assert_array_equal(o.e4m3_codes(np.nextafter(mid, np.float32(1e9))), hi_c)
+    sat = np.array([448, 449, 463.9, 464, 480, 1e4, 3e38, np.inf], dtype=np.float32)
+    assert np.all(o.e4m3_codes(sat) == 0x7E) and np.all(o.e4m3_codes(-sat) == 0xFE)
+    assert np.all(o.e4m3_codes(np.array([np.nan], dtype=np.float32)) & 0x7F == 0x7F)
+    assert o.e4m3_codes(np.array([-0.0], dtype=np.float32))[0] == 0x80
+    y = np.random.default_rng(5).standard_normal(200_000).astype(np.float32) * np.float32(60)
+    y = y[np.abs(y) < 448]
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(o.e4m3_codes(y), ref)
+
+
+def _fp8_decode_case(seed=21):
+    lens = [1, 17, 64, 129, 40, 200]
+    return inputs.make_decode(lens, len(lens), 8, 2, 64, seed=seed, sinks=True, kv_dtype="fp8")
+
+
+def pin_decode_fp8_pow2_is_bf16_decode(o):
+    """With power-of-two scales every dequantised value is a bf16 number: the FP8 decode
+    must equal the (pinned) bf16 decode of those values exactly."""
+    w = _fp8_decode_case()
+    c = w.cache
+    ks = torch.tensor([2.0 ** -5, 2.0 ** -6], dtype=torch.float32)
+    vs = torch.tensor([2.0 ** -4, 2.0 ** -7], dtype=torch.float32)
+    kb = _dequant_pages(c.k_pages, ks).to(torch.bfloat16)
+    vb = _dequant_pages(c.v_pages, vs).to(torch.bfloat16)
+    for W in (0, 1, 40, 300):
+        a_out, a_lse = o.decode_fp8(w.q, c.k_pages, c.v_pages, ks, vs, c.block_table, c.lens, w.sinks,
+                                    w.scale, window=W)
+        b_out, b_lse = o.decode(w.q, kb, vb, c.block_table, c.lens, w.sinks, w.scale, window=W)
+        np.testing.assert_array_equal(a_out, b_out)
+        np.testing.assert_array_equal(a_lse, b_lse)
+
+
+def pin_decode_fp8_sdpa(o):
+    """Arbitrary per-head scales: SDPA (float64) on keys/values dequantised by torch."""
+    w = _fp8_decode_case(seed=22)
+    c = w.cache
+    deq = inputs.PagedCache(_dequant_pages(c.k_pages, c.k_scale), _dequant_pages(c.v_pages, c.v_scale),
+                            c.block_table, c.lens, c.num_pages)
+    for W in (0, 40):
+        out, lse = o.decode_fp8(w.q, c.k_pages, c.v_pages, c.k_scale, c.v_scale, c.block_table, c.lens,
+                                w.sinks, w.scale, window=W)
+        for b, L in enumerate(c.lens.tolist()):
+            k, v = contiguous_kv(deq, b)
+            lo = max(0, L - W) if W else 0
+            ro, rl = sdpa_with_sink(w.q[b].double()[:, None, :], k[:, lo:], v[:, lo:], w.scale, w.sinks)
+            np.testing.assert_allclose(out[b], ro[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+            np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_append_fp8(o):
+    a = inputs.make_append([5, 16, 33, 0, 1], [0, 7, 16, 3, 31], 2, 64, seed=14, kv_dtype="fp8")
+    c = a.cache
+    kp, vp = o.append_kv_fp8(a.k, a.v, c.k_scale, c.v_scale, a.cu_seqlens, c.block_table, a.start_pos,
+                             c.k_pages, c.v_pages)
+
+    def torch_codes(x, s):  # [Hkv, D] bf16 -> codes, torch's cast after the float32 division
+        y = x.float() / s.view(-1, 1)
+        return y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    touched = np.zeros(kp.shape[:1] + kp.shape[2:3], dtype=bool)
+    cu = a.cu_seqlens.tolist()
+    for i in range(5):
+        for t in range(cu[i], cu[i + 1]):
+            pos = int(a.start_pos[i]) + t - cu[i]
+            pg = int(c.block_table[i, pos // 16])
+            np.testing.assert_array_equal(kp[pg, :, pos % 16], torch_codes(a.k[t], c.k_scale))
+            np.testing.assert_array_equal(vp[pg, :, pos % 16], torch_codes(a.v[t], c.v_scale))
+            touched[pg, pos % 16] = True
+    keep = ~touched
+    old = c.k_pages.numpy()
+    assert np.array_equal(kp.transpose(0, 2, 1, 3)[keep], old.transpose(0, 2, 1, 3)[keep])
+
+
 PINS = {
     "decode_sdpa_nosink": lambda o: pin_decode_sdpa(o, False),
     "decode_sdpa_sink": lambda o: pin_decode_sdpa(o, True),
@@ -358,6 +470,11 @@ PINS = {
     "decode_window_sdpa": pin_decode_window_sdpa,
     "prefill_window_sdpa": pin_prefill_window_sdpa,
     "window_special_cases": pin_window_special_cases,
+    "e4m3_table": pin_e4m3_table,
+    "e4m3_rounding": pin_e4m3_rounding,
+    "decode_fp8_pow2_is_bf16_decode": pin_decode_fp8_pow2_is_bf16_decode,
+    "decode_fp8_sdpa": pin_decode_fp8_sdpa,
+    "append_fp8": pin_append_fp8,
 }
 
 
@@ -400,6 +517,23 @@ MUTATIONS = [
      "const int64_t lo = (window > 0 && tl + 1 > window) ? Pi + tl + 1 - window : 0;"),
     ("merge ignores the partial's max", "den += l[s] * w;", "den += l[s];"),
     ("online form skips the rescale", "den *= r;", "den *= 1.0;"),
+    ("e4m3 subnormals decoded as normals", "mag = ldexp((double)m, -9);", "mag = ldexp(8.0 + m, -10);"),
+    ("e4m3 exponent bias off by one", "mag = ldexp(8.0 + m, e - 10);", "mag = ldexp(8.0 + m, e - 9);"),
+    ("e4m3 rounding ties away from zero", "double q = rint(ldexp(a, 3 - e));",
+     "double q = round(ldexp(a, 3 - e));"),
+    ("e4m3 subnormal rounding on the wrong grid", "double q = rint(ldexp(a, 9));",
+     "double q = rint(ldexp(a, 8));"),
+    ("e4m3 overflow saturates to NaN", "return (uint8_t)(sign | 0x7E); /* saturation",
+     "return (uint8_t)(sign | 0x7F); /* saturation"),
+    ("fp8 decode ignores the V scale", "out[d] += e * (vscale * oracle_e4m3_value(vrow[j][d]));",
+     "out[d] += e * oracle_e4m3_value(vrow[j][d]);"),
+    ("fp8 decode takes head 0's K scale", "k_scale ? (double)k_scale[g] : 1.0",
+     "k_scale ? (double)k_scale[0] : 1.0"),
+    ("fp8 decode drops the sink", "double z = exp(sink - top);", "double z = 0.0;"),
+    ("fp8 decode ignores the window",
+     "const int64_t first = (window > 0 && L > window) ? L - window : 0;", "const int64_t first = 0;"),
+    ("fp8 append quantises V with the K scale", "v_pages[off + d] = oracle_e4m3_code(vx / vs);",
+     "v_pages[off + d] = oracle_e4m3_code(vx / ks);"),
     ("append writes the next slot",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)((pos + 1) % P));"),
