@@ -21,8 +21,9 @@
  *     token j of sequence b is slot j % page_size of page block_table[b][j / page_size]
  *     block_table: int32 [num_seqs, max_pages_per_seq], row-major
  *
- * Supported: bf16 data, fp32 sinks, head_dim 64 or 128, page_size 16,
- * num_qo_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ * Supported: bf16 data (and FP8 E4M3 KV caches for decode and append, see below),
+ * fp32 sinks, head_dim 64 or 128, page_size 16, num_qo_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}.
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers into memory the caller owns; the
@@ -153,6 +154,55 @@ int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pa
 int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out, float *lse,
                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                           sinkattn_stream_t stream);
+
+/* -------------------------------------------------------- FP8 E4M3 KV cache --
+ * A KV cache of one byte per element.  The pages name an FP8 serving precision
+ * ("GPT-OSS on Day 0", section "GPT-OSS on Hopper") and an 8-bit KV-cache type
+ * (TensorSharp gptoss.md section 10, "Memory and KV cache strategy") without a scale
+ * convention; this library's convention:
+ *   - each element is an OCP FP8 E4M3 code (sign, 4 exponent bits with bias 7,
+ *     3 mantissa bits; no infinities; 0x7F / 0xFF are NaN; largest finite 448);
+ *   - its value is scale[g] * e4m3(code), with one fp32 scale per KV head g, one
+ *     array for K (k_scale) and one for V (v_scale), each fp32 [Hkv] on the device;
+ *     NULL means every scale is 1.  Scales must be positive and finite.
+ * Pages keep the HND layout: uint8 [num_pages, Hkv, 16, D].
+ *
+ * sinkattn_decode_fp8: the decode above over such a cache (same q, block_table,
+ * seq_lens, sinks, scale, out, lse, descriptor, window and status behaviour).  The
+ * product q.k is formed with q converted to fp16: |q| entries must be below 65504
+ * (values below 2^-14 lose precision as fp16 subnormals).  The probabilities enter
+ * the P.V product rounded to fp16 (relative error <= 2^-11 each), so an output's
+ * absolute error is bounded by about 2^-11 * max |v| over its keys plus the bf16
+ * rounding of the output; lse is not affected.  NaN codes in visible keys give
+ * unspecified outputs.  The workspace is the
+ * decode workspace (sinkattn_decode_workspace_size covers both caches), and
+ * sinkattn_decode_merge completes sinkattn_decode_fp8_splitkv exactly as it
+ * completes sinkattn_decode_splitkv.
+ */
+int sinkattn_decode_fp8(const void *q, const void *k_pages, const void *v_pages,
+                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+                        const int32_t *seq_lens, const float *sinks, float scale, void *out,
+                        float *lse, const sinkattn_paged_desc *desc, void *workspace,
+                        size_t ws_bytes, sinkattn_stream_t stream);
+
+/* First kernel of sinkattn_decode_fp8 (the split-KV pass; see sinkattn_decode_splitkv). */
+int sinkattn_decode_fp8_splitkv(const void *q, const void *k_pages, const void *v_pages,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                const float *sinks, float scale, void *out, float *lse,
+                                const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                                sinkattn_stream_t stream);
+
+/* sinkattn_append_kv into an FP8 cache: bf16 rows k, v [T, Hkv, D] are quantised,
+ * element x of KV head g to the E4M3 code nearest to x / scale[g] (the division in
+ * IEEE single precision; ties to the even code; finite values beyond 448 and
+ * infinities saturate to +-448; NaN stays NaN), and written to the same slots
+ * sinkattn_append_kv would write.  k_pages, v_pages: uint8 [num_pages, Hkv, 16, D]. */
+int sinkattn_append_kv_fp8(const void *k, const void *v, const float *k_scale,
+                           const float *v_scale, const int32_t *cu_seqlens, int32_t total_tokens,
+                           const int32_t *block_table, const int32_t *start_pos, void *k_pages,
+                           void *v_pages, const sinkattn_paged_desc *desc, void *workspace,
+                           size_t ws_bytes, sinkattn_stream_t stream);
 
 /* ------------------------------------------------------- decode, no allocation --
  * No counterpart on the source pages: an addition for callers that cannot allocate

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsinkattn.so")
-SOURCES = ["api.cpp", "decode.cu", "append.cu", "prefill.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cpp", "decode.cu", "decode_fp8.cu", "append.cu", "prefill.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -48,17 +48,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// bf16 tensor of `rank` dims (innermost first), 128-byte swizzled boxes.
+// Tensor of `rank` dims (innermost first); bf16 with 128-byte swizzled boxes unless
+// told otherwise.
 int encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-               const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+               const cuuint64_t *strides_bytes, const cuuint32_t *box,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = tensor_map_encoder();
     if (!enc) return SINKATTN_ERR_CUDA;
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
-                     dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = enc(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SINKATTN_OK : SINKATTN_ERR_INVALID_ARG;
+}
+
+// FP8 pages [num_pages, Hkv, 16, D] of uint8 codes: one box is a whole (page, head),
+// 16 rows of D bytes, swizzled by 64 bytes (D = 64) or 128 bytes (D = 128).
+int encode_pages_map_fp8(CUtensorMap *m, const void *pages, int num_pages, int Hkv, int D) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
+    const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)kPageSize * D,
+                                   (cuuint64_t)Hkv * kPageSize * D};
+    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kPageSize, 1, 1};
+    return encode_map(m, pages, 4, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Pages [num_pages, Hkv, 16, D]: dims {D, 16, Hkv, num_pages}; a box is one
@@ -104,9 +118,13 @@ int check_decode_desc(const sinkattn_paged_desc *d) {
     return SINKATTN_OK;
 }
 
+// One workspace layout serves both split-KV kernels (bf16 and FP8 cache): the
+// partial-state slots are sized for the larger of their grids, so the merge reads
+// the same offsets after either.
 struct DecodeLayout {
     size_t prefix, plan, ml, acc, total;
-    int ctas, warps_per_cta, smem, total_warps;
+    int ctas, warps_per_cta, smem, total_warps;     // bf16 cache kernel
+    int ctas8, warps_per_cta8, smem8, total_warps8;  // FP8 cache kernel
 };
 
 int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
@@ -117,9 +135,15 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
                                      &L->smem),
                  "decode launch shape");
     if (rc) return rc;
-    L->total_warps = L->ctas * L->warps_per_cta;
     const int G = d->num_qo_heads / d->num_kv_heads;
-    const size_t slots = (size_t)L->total_warps + (size_t)d->num_seqs * d->num_kv_heads;
+    rc = cuda_rc(decode_fp8_launch_shape(d->head_dim, G, d->num_seqs, device, &L->ctas8,
+                                         &L->warps_per_cta8, &L->smem8),
+                 "fp8 decode launch shape");
+    if (rc) return rc;
+    L->total_warps = L->ctas * L->warps_per_cta;
+    L->total_warps8 = L->ctas8 * L->warps_per_cta8;
+    const int most = L->total_warps > L->total_warps8 ? L->total_warps : L->total_warps8;
+    const size_t slots = (size_t)most + (size_t)d->num_seqs * d->num_kv_heads;
     size_t off = kStatusBytes;
     L->prefix = off;
     off += align_up(((size_t)d->num_seqs + 1) * 4);
@@ -175,7 +199,47 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.ws_plan = reinterpret_cast<int64_t *>(ws + P->layout.plan);
     a.part_ml = reinterpret_cast<float *>(ws + P->layout.ml);
     a.part_acc = reinterpret_cast<float *>(ws + P->layout.acc);
+    a.k_scale = nullptr;
+    a.v_scale = nullptr;
     return SINKATTN_OK;
+}
+
+int append_common(const void *k, const void *v, const int32_t *cu_seqlens, int32_t total_tokens,
+                  const int32_t *block_table, const int32_t *start_pos, void *k_pages,
+                  void *v_pages, const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                  bool fp8, const float *k_scale, const float *v_scale, sinkattn_stream_t stream) {
+    int rc = check_heads(desc);
+    if (rc) return rc;
+    if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (!k || !v || !cu_seqlens || !block_table || !start_pos || !k_pages || !v_pages)
+        return SINKATTN_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        !aligned(cu_seqlens, 4) || !aligned(block_table, 4) || !aligned(start_pos, 4) ||
+        (k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (workspace && (ws_bytes < kStatusBytes || !aligned(workspace, kAlign)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_pages < 1 || desc->max_pages_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
+    AppendArgs a;
+    a.k = k;
+    a.v = v;
+    a.cu_seqlens = cu_seqlens;
+    a.block_table = block_table;
+    a.start_pos = start_pos;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.T = total_tokens;
+    a.n = desc->num_seqs;
+    a.Hkv = desc->num_kv_heads;
+    a.D = desc->head_dim;
+    a.num_pages = desc->num_pages;
+    a.max_pages = desc->max_pages_per_seq;
+    a.status = static_cast<uint32_t *>(workspace);
+    a.fp8 = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return cuda_rc(launch_append_kv(a, (cudaStream_t)stream), "append launch");
 }
 
 }  // namespace
@@ -266,6 +330,45 @@ int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
     return sinkattn_decode_merge(seq_lens, sinks, out, lse, desc, workspace, ws_bytes, stream);
 }
 
+int sinkattn_decode_fp8_splitkv(const void *q, const void *k_pages, const void *v_pages,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                const float *sinks, float scale, void *out, float *lse,
+                                const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                                sinkattn_stream_t stream) {
+    DecodePrep P;
+    int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
+                            ws_bytes, &P);
+    if (rc) return rc;
+    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+        (k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+        return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0) return SINKATTN_OK;
+    CUtensorMap kmap, vmap;
+    rc = encode_pages_map_fp8(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    rc = encode_pages_map_fp8(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    P.args.k_scale = k_scale;
+    P.args.v_scale = v_scale;
+    P.args.total_warps = P.layout.total_warps8;
+    return cuda_rc(launch_decode_fp8(desc->head_dim, P.args, kmap, vmap, P.layout.ctas8,
+                                     P.layout.smem8, (cudaStream_t)stream),
+                   "fp8 split-KV decode launch");
+}
+
+int sinkattn_decode_fp8(const void *q, const void *k_pages, const void *v_pages,
+                        const float *k_scale, const float *v_scale, const int32_t *block_table,
+                        const int32_t *seq_lens, const float *sinks, float scale, void *out,
+                        float *lse, const sinkattn_paged_desc *desc, void *workspace,
+                        size_t ws_bytes, sinkattn_stream_t stream) {
+    int rc = sinkattn_decode_fp8_splitkv(q, k_pages, v_pages, k_scale, v_scale, block_table,
+                                         seq_lens, sinks, scale, out, lse, desc, workspace,
+                                         ws_bytes, stream);
+    if (rc) return rc;
+    return sinkattn_decode_merge(seq_lens, sinks, out, lse, desc, workspace, ws_bytes, stream);
+}
+
 int sinkattn_prefill_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes) {
     if (!bytes) return SINKATTN_ERR_INVALID_ARG;
     int rc = check_heads(desc);
@@ -341,34 +444,17 @@ int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,
                        const int32_t *start_pos, void *k_pages, void *v_pages,
                        const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                        sinkattn_stream_t stream) {
-    int rc = check_heads(desc);
-    if (rc) return rc;
-    if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
-    if (!k || !v || !cu_seqlens || !block_table || !start_pos || !k_pages || !v_pages)
-        return SINKATTN_ERR_INVALID_ARG;
-    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
-        !aligned(cu_seqlens, 4) || !aligned(block_table, 4) || !aligned(start_pos, 4))
-        return SINKATTN_ERR_INVALID_ARG;
-    if (workspace && (ws_bytes < kStatusBytes || !aligned(workspace, kAlign)))
-        return SINKATTN_ERR_INVALID_ARG;
-    if (desc->num_pages < 1 || desc->max_pages_per_seq < 1) return SINKATTN_ERR_INVALID_ARG;
-    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
-    AppendArgs a;
-    a.k = k;
-    a.v = v;
-    a.cu_seqlens = cu_seqlens;
-    a.block_table = block_table;
-    a.start_pos = start_pos;
-    a.k_pages = k_pages;
-    a.v_pages = v_pages;
-    a.T = total_tokens;
-    a.n = desc->num_seqs;
-    a.Hkv = desc->num_kv_heads;
-    a.D = desc->head_dim;
-    a.num_pages = desc->num_pages;
-    a.max_pages = desc->max_pages_per_seq;
-    a.status = static_cast<uint32_t *>(workspace);
-    return cuda_rc(launch_append_kv(a, (cudaStream_t)stream), "append launch");
+    return append_common(k, v, cu_seqlens, total_tokens, block_table, start_pos, k_pages, v_pages,
+                         desc, workspace, ws_bytes, false, nullptr, nullptr, stream);
+}
+
+int sinkattn_append_kv_fp8(const void *k, const void *v, const float *k_scale,
+                           const float *v_scale, const int32_t *cu_seqlens, int32_t total_tokens,
+                           const int32_t *block_table, const int32_t *start_pos, void *k_pages,
+                           void *v_pages, const sinkattn_paged_desc *desc, void *workspace,
+                           size_t ws_bytes, sinkattn_stream_t stream) {
+    return append_common(k, v, cu_seqlens, total_tokens, block_table, start_pos, k_pages, v_pages,
+                         desc, workspace, ws_bytes, true, k_scale, v_scale, stream);
 }
 
 int sinkattn_get_status(void *workspace, uint32_t *status_out, sinkattn_stream_t stream) {

@@ -3,6 +3,13 @@
 // attention).  A pure copy, bound by HBM bandwidth: one thread moves one
 // 16-byte vector; consecutive threads move consecutive vectors of a row, so both
 // the reads of k/v and the writes of a (page, head, slot) row are coalesced.
+//
+// Into an FP8 E4M3 cache each element x becomes the E4M3 code nearest to
+// x / scale[g] (IEEE single-precision division; nearest, ties to even; finite
+// overflow saturates to +-448, NaN stays NaN): one thread reads 8 bf16 (16 bytes)
+// and writes 8 codes (8 bytes).
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -10,6 +17,18 @@ namespace sinkattn {
 
 namespace {
 
+// Four bf16 (two packed pairs) -> four E4M3 codes of x / s, lowest element in the low byte.
+__device__ __forceinline__ uint32_t quantize4(uint2 bf, float s) {
+    const float x0 = __uint_as_float(bf.x << 16), x1 = __uint_as_float(bf.x & 0xFFFF0000u);
+    const float x2 = __uint_as_float(bf.y << 16), x3 = __uint_as_float(bf.y & 0xFFFF0000u);
+    const uint32_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x0, s), __fdiv_rn(x1, s)),
+                                                  __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c23 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x2, s), __fdiv_rn(x3, s)),
+                                                  __NV_SATFINITE, __NV_E4M3);
+    return (c01 & 0xFFFFu) | (c23 << 16);
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(256) append_kv_kernel(const AppendArgs a) {
     const int vec_per_row = a.D / 8;  // 16-byte vectors per (token, head) row
     const int64_t total = (int64_t)a.T * a.Hkv * vec_per_row;
@@ -47,8 +66,16 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const AppendArgs a) {
         const int64_t dst = ((((int64_t)pg * a.Hkv + g) * kPageSize) + pos % kPageSize) * a.D + c * 8;
         const uint4 kv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.k) + src);
         const uint4 vv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.v) + src);
-        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.k_pages) + dst) = kv;
-        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.v_pages) + dst) = vv;
+        if (kFp8) {
+            const float ks = a.k_scale ? a.k_scale[g] : 1.f, vs = a.v_scale ? a.v_scale[g] : 1.f;
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.k_pages) + dst) =
+                make_uint2(quantize4(make_uint2(kv.x, kv.y), ks), quantize4(make_uint2(kv.z, kv.w), ks));
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.v_pages) + dst) =
+                make_uint2(quantize4(make_uint2(vv.x, vv.y), vs), quantize4(make_uint2(vv.z, vv.w), vs));
+        } else {
+            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.k_pages) + dst) = kv;
+            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.v_pages) + dst) = vv;
+        }
     }
 }
 
@@ -64,7 +91,10 @@ cudaError_t launch_append_kv(const AppendArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t want = (total + 255) / 256;
     const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-    append_kv_kernel<<<grid, 256, 0, stream>>>(a);
+    if (a.fp8)
+        append_kv_kernel<true><<<grid, 256, 0, stream>>>(a);
+    else
+        append_kv_kernel<false><<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

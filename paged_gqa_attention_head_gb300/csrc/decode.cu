@@ -23,16 +23,13 @@
 #include <mutex>
 #include <vector>
 
+#include "decode_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace sinkattn {
 
 namespace {
-
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMinUnitsPerWarp = 4;  // pages per warp at least (keeps partials few)
 
 template <int D>
 struct DecodeCfg {
@@ -53,59 +50,6 @@ int decode_smem_bytes(int B) {
     return 1024 /* alignment slack */ + C::kWarps * C::kWarpBytes +
            C::kWarps * C::kStages * (8 + 4 + 4) + (3 * B + 1) * 4;
 }
-
-__device__ __forceinline__ float quad_max(float x) {
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-    return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-}
-__device__ __forceinline__ float quad_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    return x + __shfl_xor_sync(0xffffffffu, x, 2);
-}
-
-// Lengths (validated, clamped), the first page each sequence's query sees (0, or the
-// page of its first key inside a sliding window) and the exclusive prefix sum of the
-// pages it sees, into shared memory.  128 threads.
-__device__ void scan_pages(const DecodeArgs &a, int *s_prefix, int *s_len, int *s_first) {
-    __shared__ int s_warp_tot[4];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int per_t = (a.B + 127) / 128;
-    const int b0 = min(a.B, tid * per_t), b1 = min(a.B, b0 + per_t);
-    const int cap = a.max_pages * kPageSize;
-    int local = 0;
-    for (int b = b0; b < b1; ++b) {
-        int L = a.seq_lens[b];
-        if (L < 0 || L > cap) {
-            set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
-            L = L < 0 ? 0 : cap;
-        }
-        s_len[b] = L;
-        const int first = (a.window > 0 && L > a.window) ? (L - a.window) / kPageSize : 0;
-        s_first[b] = first;
-        local += (L + kPageSize - 1) / kPageSize - first;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp_tot[wid] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int w = 0; w < wid; ++w) run += s_warp_tot[w];
-    for (int b = b0; b < b1; ++b) {
-        s_prefix[b] = run;
-        run += (s_len[b] + kPageSize - 1) / kPageSize - s_first[b];
-    }
-    if (tid == 0) s_prefix[a.B] = s_warp_tot[0] + s_warp_tot[1] + s_warp_tot[2] + s_warp_tot[3];
-    __syncthreads();
-}
-
-// Position in the unit list: sequence b, KV head g, page p of the sequence.
-struct Cursor {
-    int b, g, p, pb;  // pb = pages of sequence b
-};
 
 // kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
 // window arithmetic.

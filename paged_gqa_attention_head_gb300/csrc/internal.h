@@ -31,6 +31,8 @@ struct DecodeArgs {
     int64_t *ws_plan;       // [2]: total page units, page units per warp
     float *part_ml;         // [slots, G, 2] partial (max, sum), log2 domain
     float *part_acc;        // [slots, G, D] partial unnormalised outputs
+    const float *k_scale;   // FP8 cache: [Hkv] per-KV-head scales, or nullptr (1)
+    const float *v_scale;
 };
 
 // Grid and shared memory of the split-KV decode kernel for head_dim D and
@@ -42,14 +44,22 @@ cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap 
                                   cudaStream_t stream);
 cudaError_t launch_decode_merge(int D, const DecodeArgs &a, cudaStream_t stream);
 
+// The same for the decode over an FP8 E4M3 cache (uint8 tensor maps, one box per page).
+cudaError_t decode_fp8_launch_shape(int D, int G, int B, int device, int *ctas, int *warps_per_cta,
+                                    int *smem_bytes);
+cudaError_t launch_decode_fp8(int D, const DecodeArgs &a, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, int ctas, int smem_bytes, cudaStream_t stream);
+
 struct AppendArgs {
     const void *k, *v;  // bf16 [T, Hkv, D]
     const int32_t *cu_seqlens;
     const int32_t *block_table;
     const int32_t *start_pos;
-    void *k_pages, *v_pages;
+    void *k_pages, *v_pages;  // bf16, or uint8 E4M3 codes when fp8
     int T, n, Hkv, D, num_pages, max_pages;
     uint32_t *status;
+    bool fp8;                          // quantise to E4M3 codes
+    const float *k_scale, *v_scale;    // fp8: [Hkv] per-KV-head scales, or nullptr (1)
 };
 cudaError_t launch_append_kv(const AppendArgs &a, cudaStream_t stream);
 

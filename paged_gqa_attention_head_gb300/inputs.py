@@ -100,16 +100,17 @@ def normal_e4m3(shape, head_scales: torch.Tensor, seed: int, stream: int) -> tor
     their KV head, for pages [num_pages, Hkv, 16, D]; chunked like normal_bf16."""
     n = int(np.prod(shape)) if len(shape) else 1
     Hkv, row = shape[1], shape[2] * shape[3]
+    assert _CHUNK % row == 0
     inv_rows = (1.0 / head_scales.double()).numpy().astype(np.float32)
     out = torch.empty(n, dtype=torch.uint8)
     nchunks = (n + _CHUNK - 1) // _CHUNK
 
     def work(i: int) -> None:
-        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
-        buf = _rng(seed, stream, i).standard_normal(hi - lo, dtype=np.float32)
-        head = (np.arange(lo, hi, dtype=np.int64) // row) % Hkv
-        buf = np.clip(buf * inv_rows[head], -448.0, 448.0).astype(np.float32)
-        out[lo:hi] = torch.from_numpy(buf).to(torch.float8_e4m3fn).view(torch.uint8)
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)  # chunks hold whole rows
+        buf = _rng(seed, stream, i).standard_normal(hi - lo, dtype=np.float32).reshape(-1, row)
+        head = (np.arange(lo // row, hi // row, dtype=np.int64) % Hkv)
+        buf = np.clip(buf * inv_rows[head][:, None], -448.0, 448.0).astype(np.float32)
+        out[lo:hi] = torch.from_numpy(buf.reshape(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
 
     if nchunks <= 1:
         if n:
@@ -163,7 +164,8 @@ class PagedCache:
 def make_paged_cache(lens: list[int], num_kv_heads: int, head_dim: int, seed: int,
                      distractor_frac: float = 0.05, poison: bool = True,
                      max_pages_per_seq: Optional[int] = None, k_stream: int = _S_K,
-                     v_stream: int = _S_V, kv_dtype: str = "bf16") -> PagedCache:
+                     v_stream: int = _S_V, kv_dtype: str = "bf16",
+                     fp8_unit_scales: bool = False) -> PagedCache:
     npages_seq = [(L + PAGE_SIZE - 1) // PAGE_SIZE for L in lens]
     used = sum(npages_seq)
     num_pages = used + int(math.ceil(distractor_frac * used))
@@ -173,8 +175,11 @@ def make_paged_cache(lens: list[int], num_kv_heads: int, head_dim: int, seed: in
     shape = (num_pages, num_kv_heads, PAGE_SIZE, head_dim)
     ks = vs = None
     if kv_dtype == "fp8":
-        ks = fp8_head_scales(num_kv_heads)
-        vs = (ks * 1.25).to(torch.float32)
+        if fp8_unit_scales:  # codes are the N(0,1) values themselves
+            ks = vs = torch.ones(num_kv_heads, dtype=torch.float32)
+        else:
+            ks = fp8_head_scales(num_kv_heads)
+            vs = (ks * 1.25).to(torch.float32)
         k_pages = normal_e4m3(shape, ks, seed, k_stream)
         v_pages = normal_e4m3(shape, vs, seed, v_stream)
     else:
@@ -228,11 +233,12 @@ class DecodeInputs:
 def make_decode(lens_spec, batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                 seed: int = 0, sinks: bool = True, scale: Optional[float] = None,
                 poison: bool = True, distractor_frac: float = 0.05,
-                kv_dtype: str = "bf16") -> DecodeInputs:
-    """kv_dtype "bf16" or "fp8" (E4M3 codes with per-KV-head scales)."""
+                kv_dtype: str = "bf16", fp8_unit_scales: bool = False) -> DecodeInputs:
+    """kv_dtype "bf16" or "fp8" (E4M3 codes with per-KV-head scales; fp8_unit_scales:
+    all scales 1, the codes then encode the N(0,1) values directly)."""
     lens = draw_lengths(lens_spec, batch, seed)
     cache = make_paged_cache(lens, num_kv_heads, head_dim, seed, distractor_frac, poison,
-                             kv_dtype=kv_dtype)
+                             kv_dtype=kv_dtype, fp8_unit_scales=fp8_unit_scales)
     q = normal_bf16((batch, num_qo_heads, head_dim), seed, _S_Q)
     s = torch.from_numpy(normal_f32(num_qo_heads, seed, _S_SINK)) if sinks else None
     sc = scale if scale is not None else 1.0 / math.sqrt(head_dim)

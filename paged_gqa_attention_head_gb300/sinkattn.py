@@ -48,6 +48,12 @@ SIGNATURES = {
     "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
                                         _P, _SZ, _P]),
     "sinkattn_append_kv": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ,
+                                           _P]),
+    "sinkattn_decode_fp8_splitkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
+                                                   _P, _SZ, _P]),
+    "sinkattn_append_kv_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _DP, _P, _SZ,
+                                              _P]),
     "sinkattn_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
 }
 
@@ -159,12 +165,17 @@ def get_status(ws: torch.Tensor) -> int:
     return v.value
 
 
+def _codes(t: torch.Tensor) -> torch.Tensor:
+    """An FP8 E4M3 cache tensor as its uint8 codes (float8_e4m3fn tensors are viewed)."""
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
 def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
-                 want_lse, window=0):
+                 want_lse, window=0, kv_dtype=torch.bfloat16):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
-    _need(k_pages, "k_pages", torch.bfloat16, dev, 4)
-    _need(v_pages, "v_pages", torch.bfloat16, dev, 4)
+    _need(k_pages, "k_pages", kv_dtype, dev, 4)
+    _need(v_pages, "v_pages", kv_dtype, dev, 4)
     _need(block_table, "block_table", torch.int32, dev, 2)
     _need(seq_lens, "seq_lens", torch.int32, dev, 1)
     B, Hq, D = q.shape
@@ -285,6 +296,72 @@ def append_kv(k, v, cu_seqlens, block_table, start_pos, k_pages, v_pages, worksp
                                      _ptr(start_pos), _ptr(k_pages), _ptr(v_pages),
                                      ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(dev)),
            "sinkattn_append_kv")
+    return k_pages, v_pages
+
+
+def _scales(k_scale, v_scale, Hkv, dev):
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            _need(t, name, torch.float32, dev, 1)
+            if t.shape[0] != Hkv:
+                raise ValueError(f"{name} must have one entry per KV head")
+
+
+def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None, scale=None,
+               out=None, lse=None, workspace_buf=None, return_lse=True, window=0):
+    """Split-KV paged decode over an FP8 E4M3 cache (sinkattn_decode_fp8).  k_pages / v_pages:
+    uint8 (or float8_e4m3fn) [num_pages, Hkv, 16, D] codes; k_scale / v_scale: float32 [Hkv]
+    per-KV-head scales or None (1).  Returns (out, lse)."""
+    k_pages, v_pages = _codes(k_pages), _codes(v_pages)
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             kv_dtype=torch.uint8)
+    _scales(k_scale, v_scale, k_pages.shape[1], q.device)
+    _check(load().sinkattn_decode_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(sinks),
+                                      scale, _ptr(out), _ptr(lse), ctypes.byref(desc), _ptr(ws),
+                                      ws.numel(), _stream(q.device)), "sinkattn_decode_fp8")
+    return out, lse
+
+
+def decode_fp8_splitkv(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None,
+                       scale=None, out=None, lse=None, workspace_buf=None, return_lse=True, window=0):
+    """First kernel of decode_fp8 only (sinkattn_decode_fp8_splitkv); follow with decode_merge."""
+    k_pages, v_pages = _codes(k_pages), _codes(v_pages)
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             kv_dtype=torch.uint8)
+    _scales(k_scale, v_scale, k_pages.shape[1], q.device)
+    _check(load().sinkattn_decode_fp8_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
+                                              _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+                                              _ptr(sinks), scale, _ptr(out), _ptr(lse),
+                                              ctypes.byref(desc), _ptr(ws), ws.numel(),
+                                              _stream(q.device)), "sinkattn_decode_fp8_splitkv")
+    return out, lse, ws, desc
+
+
+def append_kv_fp8(k, v, k_scale, v_scale, cu_seqlens, block_table, start_pos, k_pages, v_pages,
+                  workspace_buf=None):
+    """Quantise new bf16 K/V rows to E4M3 codes (x / scale[g], nearest, saturating) and scatter
+    them into an FP8 cache in place (sinkattn_append_kv_fp8)."""
+    dev = k.device
+    k_pages, v_pages = _codes(k_pages), _codes(v_pages)
+    _need(k, "k", torch.bfloat16, dev, 3)
+    _need(v, "v", torch.bfloat16, dev, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(start_pos, "start_pos", torch.int32, dev, 1)
+    _need(k_pages, "k_pages", torch.uint8, dev, 4)
+    _need(v_pages, "v_pages", torch.uint8, dev, 4)
+    T, Hkv, D = k.shape
+    _scales(k_scale, v_scale, Hkv, dev)
+    n = cu_seqlens.shape[0] - 1
+    desc = paged_desc(n, Hkv, Hkv, D, k_pages.shape[0], block_table.shape[1])
+    ws = workspace_buf if workspace_buf is not None else workspace(256, dev, "append")
+    _check(load().sinkattn_append_kv_fp8(_ptr(k), _ptr(v), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(cu_seqlens), T, _ptr(block_table), _ptr(start_pos),
+                                         _ptr(k_pages), _ptr(v_pages), ctypes.byref(desc), _ptr(ws),
+                                         ws.numel(), _stream(dev)), "sinkattn_append_kv_fp8")
     return k_pages, v_pages
 
 
