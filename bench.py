@@ -316,18 +316,24 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     rows = {}
     reps = 20
 
-    def decode_row(name, window=0):
+    def decode_row(name, window=0, graph=False):
         w = inputs.make_workload(name, seed=0)
         c = w.cache
-        args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
-                c.lens.to(dev), None if w.sinks is None else w.sinks.to(dev), w.scale)
-        out = torch.empty_like(args[0])
-        lse = torch.empty(args[0].shape[:2], dtype=torch.float32, device=dev)
-        f = lambda: sa.decode(*args, out=out, lse=lse, window=window)  # noqa: E731
+        q, sinks = w.q.to(dev), None if w.sinks is None else w.sinks.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        if c.fp8:  # E4M3 pages with per-KV-head scales
+            args = (q, c.k_pages.to(dev), c.v_pages.to(dev), c.k_scale.to(dev), c.v_scale.to(dev),
+                    c.block_table.to(dev), c.lens.to(dev), sinks, w.scale)
+            f = lambda: sa.decode_fp8(*args, out=out, lse=lse, window=window)  # noqa: E731
+        else:
+            args = (q, c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
+                    sinks, w.scale)
+            f = lambda: sa.decode(*args, out=out, lse=lse, window=window)  # noqa: E731
         for _ in range(3):
             f()
-        if window:
-            # ~10 us of GPU work: time a CUDA graph of the calls, not the host's launches
+        if window or graph:
+            # short GPU work: time a CUDA graph of the calls, not the host's launches
             g = capture_steps(torch, f, reps)
             time_graph(torch, g, stream)
             ms = time_graph(torch, g, stream) / reps
@@ -339,8 +345,11 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
              "kv_bytes": nbytes, "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1)}
         if window:
             r["window"] = window
+        if window or graph:
             r["launch"] = f"CUDA graph of {reps} calls"
-        del args, out, lse, w
+        if c.fp8:
+            r["kv_dtype"] = "fp8 e4m3 (per-KV-head scales)"
+        del args, out, lse, w, q, sinks
         torch.cuda.empty_cache()
         return r
 
@@ -349,6 +358,10 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     # a gpt-oss sliding-window layer (128 positions): the last 128 keys of each sequence,
     # ~9 MB of KV, so the launch and the first copies dominate
     rows["gptoss_decode_window128"] = decode_row(HEADLINE, window=128)
+    # the decode shapes over an FP8 E4M3 cache (half the KV bytes per token)
+    rows["gptoss_decode_fp8"] = decode_row("gptoss_decode_fp8", graph=True)
+    for name in ("qwen3_decode_fp8", "longctx_decode_fp8"):
+        rows[name] = decode_row(name)
 
     # append of the prefill workload's K/V into HND pages
     a = inputs.make_append([4096, 2048, 1024, 512], [0, 0, 0, 0], 8, 64, seed=0)
@@ -362,6 +375,20 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     moved = 2 * 2 * a.k.numel() * 2  # read k, v and write them
     rows["gptoss_append"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
                              "bytes": moved}
+    # the same append into an FP8 cache (quantising: read bf16, write one byte per element)
+    a8 = inputs.make_append([4096, 2048, 1024, 512], [0, 0, 0, 0], 8, 64, seed=0, kv_dtype="fp8")
+    c8 = a8.cache
+    a8args = (a8.k.to(dev), a8.v.to(dev), c8.k_scale.to(dev), c8.v_scale.to(dev),
+              a8.cu_seqlens.to(dev), c8.block_table.to(dev), a8.start_pos.to(dev),
+              c8.k_pages.to(dev), c8.v_pages.to(dev))
+    f = lambda: sa.append_kv_fp8(*a8args)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = time_loop(torch, f, reps, stream) / reps
+    moved = 2 * a8.k.numel() * (2 + 1)  # read k, v (bf16) and write their codes
+    rows["gptoss_append_fp8"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
+                                 "bytes": moved}
+    del aargs, a8args
 
     for name, window in (("gptoss_prefill", 0), ("longctx_chunked", 0), ("gptoss_prefill", 128)):
         p = inputs.make_workload(name, seed=0)

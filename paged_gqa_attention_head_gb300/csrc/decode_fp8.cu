@@ -82,9 +82,19 @@ __device__ __forceinline__ int tok_row(int k) {
     return k;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// The two E4M3 codes in bits 0-15 (or 16-31) of w to an f16 pair, the lower byte in the
+// lower half: one cvt on a 16-bit half of the register, no repacking.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r) : "r"(w));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
+        : "=r"(r) : "r"(w));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
@@ -268,10 +278,14 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
     }
     // V: tokens 2t, 2t+1, 2t+8, 2t+9 of the MMA's k axis; bytes [gr * D/8, +D/8)
     uint32_t voff[4];
+    int vrow[4];
     {
         const int ks[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) voff[i] = swz<D>(tok_row<D>(ks[i]), gr * (D / 8));
+        for (int i = 0; i < 4; ++i) {
+            vrow[i] = tok_row<D>(ks[i]);
+            voff[i] = swz<D>(vrow[i], gr * (D / 8));
+        }
     }
 
     uint32_t qf[C::kKSteps][NH][2];
@@ -289,21 +303,56 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
                 mbar_wait(&wbar[v % S], (uint32_t)((v / S) & 1), 100000000ull);
             return;
         }
-        uint8_t *kb = wbuf + stage * C::kStageBytes;  // K of page j at kb + j * kPageBytes
-        uint8_t *vb = kb + U * C::kPageBytes;         // V of page j at vb + j * kPageBytes
+        // Take the unit's fragments into registers and hand the stage straight back to the
+        // copy engine: the next copy then overlaps this unit's arithmetic, so nearly every
+        // stage of the ring is in flight rather than one held per warp while it computes.
+        const uint8_t *kb = wbuf + stage * C::kStageBytes;  // K of page j at kb + j * kPageBytes
+        const uint8_t *vb = kb + U * C::kPageBytes;         // V of page j at vb + j * kPageBytes
         int nv[U], klo[U];
+        uint32_t kw[U][2][C::kKWords];  // K rows gr, gr + 8: the lane's run of D/4 bytes
+        uint32_t vw[U][4][C::kVWords];  // V rows of tokens 2t, 2t+1, 2t+8, 2t+9: D/8 bytes
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             nv[j] = wnv[stage * U + j];
             klo[j] = kWindow ? wlo[stage * U + j] : 0;
-            if (nv[j] < kPageSize) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int i = 0; i < C::kKWords / 4; ++i) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(kb + j * C::kPageBytes + koff[r][i]);
+                    kw[j][r][4 * i] = w.x;
+                    kw[j][r][4 * i + 1] = w.y;
+                    kw[j][r][4 * i + 2] = w.z;
+                    kw[j][r][4 * i + 3] = w.w;
+                }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint8_t *src = vb + j * C::kPageBytes + voff[i];
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (D == 64) {
+                    const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                    w[0] = x.x;
+                    w[1] = x.y;
+                } else {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(src);
+                    w[0] = x.x;
+                    w[1] = x.y;
+                    w[2] = x.z;
+                    w[3] = x.w;
+                }
                 // rows past the sequence end may hold NaN codes; P is 0 there but 0 * NaN
-                // is not 0, so clear those V rows (swizzling stays inside a row)
-                for (int i = nv[j] * (D / 16) + lane; i < kPageSize * (D / 16); i += 32)
-                    *reinterpret_cast<uint4 *>(vb + j * C::kPageBytes + i * 16) = make_uint4(0, 0, 0, 0);
+                // is not 0, so those V rows become zeros
+                const bool live = vrow[i] < nv[j];
+#pragma unroll
+                for (int e = 0; e < C::kVWords; ++e) vw[j][i][e] = live ? w[e] : 0u;
             }
         }
+        fence_proxy_async_smem();
         __syncwarp();
+        if (u + S < n_units) {
+            produce(stage, pc);
+            advance(pc);
+        }
 
         if (seg_start) {
             const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
@@ -343,23 +392,12 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
         float s[U][NH][4];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-            uint32_t kw[2][C::kKWords];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int i = 0; i < C::kKWords / 4; ++i) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(kb + j * C::kPageBytes + koff[r][i]);
-                    kw[r][4 * i] = w.x;
-                    kw[r][4 * i + 1] = w.y;
-                    kw[r][4 * i + 2] = w.z;
-                    kw[r][4 * i + 3] = w.w;
-                }
 #pragma unroll
             for (int nt = 0; nt < NH; ++nt) s[j][nt][0] = s[j][nt][1] = s[j][nt][2] = s[j][nt][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < C::kKSteps; ++kk) {
-                const uint32_t a0 = e4m3x2_to_f16x2(kw[0][kk]), a2 = e4m3x2_to_f16x2(kw[0][kk] >> 16);
-                const uint32_t a1 = e4m3x2_to_f16x2(kw[1][kk]), a3 = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+                const uint32_t a0 = e4m3x2_lo_to_f16x2(kw[j][0][kk]), a2 = e4m3x2_hi_to_f16x2(kw[j][0][kk]);
+                const uint32_t a1 = e4m3x2_lo_to_f16x2(kw[j][1][kk]), a3 = e4m3x2_hi_to_f16x2(kw[j][1][kk]);
 #pragma unroll
                 for (int nt = 0; nt < NH; ++nt)
                     mma_f16_16816(s[j][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
@@ -413,37 +451,21 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
         // O^T += V^T P^T, one 16-token k-step per page
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-            uint32_t vw[4][C::kVWords];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint8_t *src = vb + j * C::kPageBytes + voff[i];
-                if (D == 64) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(src);
-                    vw[i][0] = w.x;
-                    vw[i][1] = w.y;
-                } else {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(src);
-                    vw[i][0] = w.x;
-                    vw[i][1] = w.y;
-                    vw[i][2] = w.z;
-                    vw[i][3] = w.w;
-                }
-            }
             // word layout per token row: [half 0 (rows gr): D/64 words][half 1 (rows gr+8)]
 #pragma unroll
             for (int mp = 0; mp < C::kMTiles / 2; ++mp) {  // m-tiles 2mp, 2mp + 1
                 const int wi = (mp >> 1), sel = (mp & 1) ? 0x7362 : 0x5140;
-                const uint32_t x00 = __byte_perm(vw[0][wi], vw[1][wi], sel);  // half 0, tokens 2t, 2t+1
-                const uint32_t x01 = __byte_perm(vw[0][wi + D / 64], vw[1][wi + D / 64], sel);  // half 1
-                const uint32_t x10 = __byte_perm(vw[2][wi], vw[3][wi], sel);  // half 0, tokens + 8
-                const uint32_t x11 = __byte_perm(vw[2][wi + D / 64], vw[3][wi + D / 64], sel);
+                const uint32_t x00 = __byte_perm(vw[j][0][wi], vw[j][1][wi], sel);  // half 0, tokens 2t, 2t+1
+                const uint32_t x01 = __byte_perm(vw[j][0][wi + D / 64], vw[j][1][wi + D / 64], sel);  // half 1
+                const uint32_t x10 = __byte_perm(vw[j][2][wi], vw[j][3][wi], sel);  // half 0, tokens + 8
+                const uint32_t x11 = __byte_perm(vw[j][2][wi + D / 64], vw[j][3][wi + D / 64], sel);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int mt = 2 * mp + e;
-                    const uint32_t a0 = e4m3x2_to_f16x2(x00 >> (16 * e));
-                    const uint32_t a1 = e4m3x2_to_f16x2(x01 >> (16 * e));
-                    const uint32_t a2 = e4m3x2_to_f16x2(x10 >> (16 * e));
-                    const uint32_t a3 = e4m3x2_to_f16x2(x11 >> (16 * e));
+                    const uint32_t a0 = e ? e4m3x2_hi_to_f16x2(x00) : e4m3x2_lo_to_f16x2(x00);
+                    const uint32_t a1 = e ? e4m3x2_hi_to_f16x2(x01) : e4m3x2_lo_to_f16x2(x01);
+                    const uint32_t a2 = e ? e4m3x2_hi_to_f16x2(x10) : e4m3x2_lo_to_f16x2(x10);
+                    const uint32_t a3 = e ? e4m3x2_hi_to_f16x2(x11) : e4m3x2_lo_to_f16x2(x11);
 #pragma unroll
                     for (int nt = 0; nt < NH; ++nt)
                         mma_f16_16816(acc[mt][nt], a0, a1, a2, a3, pb[j][nt][0], pb[j][nt][1]);
@@ -509,13 +531,6 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
             seg_start = true;
         }
         advance(cur);
-
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (u + S < n_units) {
-            produce(stage, pc);
-            advance(pc);
-        }
     }
 }
 
