@@ -417,7 +417,68 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
                      "traffic": None if window else traffic_for("prefill_kernel", name)}
         if window:
             rows[key]["window"] = window
+    rows["longctx_mixed"] = mixed_row(torch, sa, inputs, dev, stream, pk, reps)
     return rows
+
+
+def mixed_row(torch, sa, inputs, dev, stream, pk, reps):
+    """The long-context mixed batch: the 256-sequence decode and the 8 chunked-prefill
+    requests of one step issued on two streams at once, against the same two calls one
+    after the other and the lower bound max(KV bytes / HBM peak, FLOP / bf16 peak)."""
+    wd = inputs.make_workload("longctx_decode", seed=0)
+    c = wd.cache
+    q = wd.q.to(dev)
+    dargs = (q, c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
+             wd.sinks.to(dev), wd.scale)
+    dout, dlse = torch.empty_like(q), torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    dws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        q.shape[0], q.shape[1], c.k_pages.shape[1], q.shape[2], c.k_pages.shape[0],
+        c.block_table.shape[1])), dtype=torch.uint8, device=dev)
+    wp = inputs.make_workload("longctx_chunked", seed=0)
+    pre = wp.prefix
+    pargs = (wp.q.to(dev), wp.k.to(dev), wp.v.to(dev), wp.cu_seqlens.to(dev), wp.sinks.to(dev),
+             wp.scale)
+    pkw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
+               prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
+    pout = torch.empty_like(pargs[0])
+    plse = torch.empty(pargs[0].shape[:2], dtype=torch.float32, device=dev)
+    pws = torch.zeros(max(256, sa.prefill_workspace_size(sa.paged_desc(
+        wp.cu_seqlens.shape[0] - 1, wp.q.shape[1], wp.k.shape[1], wp.q.shape[2],
+        pre.k_pages.shape[0], pre.block_table.shape[1]))), dtype=torch.uint8, device=dev)
+    fd = lambda: sa.decode(*dargs, out=dout, lse=dlse, workspace_buf=dws)  # noqa: E731
+    fp = lambda: sa.prefill(*pargs, **pkw, out=pout, lse=plse, workspace_buf=pws)  # noqa: E731
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        s1.wait_event(ev)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s1):
+            fd()
+        with torch.cuda.stream(s2):
+            fp()
+        e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+        e1.record(s1)
+        e2.record(s2)
+        stream.wait_event(e1)
+        stream.wait_event(e2)
+
+    for f in (fd, fp, both):
+        for _ in range(3):
+            f()
+    ms_d = time_loop(torch, fd, reps, stream) / reps
+    ms_p = time_loop(torch, fp, reps, stream) / reps
+    ms_both = time_loop(torch, both, reps, stream) / reps
+    nbytes, flops = wd.kv_bytes(), wp.flops()
+    bound = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12)) * 1e3
+    r = {"ms": round(ms_both, 5), "decode_ms": round(ms_d, 5), "chunked_ms": round(ms_p, 5),
+         "sequential_ms": round(ms_d + ms_p, 5), "lower_bound_ms": round(bound, 5),
+         "frac_of_bound": round(bound / ms_both, 4), "kv_bytes": nbytes, "flops": flops,
+         "launch": "decode (split-KV + merge) and chunked prefill on two streams"}
+    del dargs, pargs, pkw, dws, pws
+    torch.cuda.empty_cache()
+    return r
 
 
 def cpu_baseline(w, budget_s: float = 12.0):
