@@ -1,0 +1,55 @@
+"""Calls on different streams run concurrently and independently: a decode and a chunked
+prefill issued at the same time on two streams (each with its own workspace, as a
+serving loop mixing decode and prefill requests would do) give bit for bit the results
+of the same calls issued one after the other."""
+import pytest
+import torch
+
+from paged_gqa_attention_head_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_and_chunked_prefill_on_two_streams_match_sequential(sa, cuda_dev):
+    dev = cuda_dev
+    w = inputs.make_decode(("uniform", 200, 20000), 96, 64, 8, 64, seed=211, sinks=True)
+    c = w.cache
+    dargs = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
+             c.lens.to(dev), w.sinks.to(dev), w.scale)
+    p = inputs.make_prefill([700, 129, 512], 64, 8, 64, seed=212, sinks=True,
+                            prefix_lens=[3000, 0, 1200])
+    pre = p.prefix
+    pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+    pkw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
+               prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
+
+    ref_d = sa.decode(*dargs)
+    ref_p = sa.prefill(*pargs, **pkw)
+    torch.cuda.synchronize()
+    ref_d = tuple(t.clone() for t in ref_d)
+    ref_p = tuple(t.clone() for t in ref_p)
+
+    dws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        w.q.shape[0], 64, 8, 64, c.k_pages.shape[0], c.block_table.shape[1])), dtype=torch.uint8,
+        device=dev)
+    pws = torch.zeros(max(256, sa.prefill_workspace_size(sa.paged_desc(
+        3, 64, 8, 64, pre.k_pages.shape[0], pre.block_table.shape[1]))), dtype=torch.uint8,
+        device=dev)
+    d_out, d_lse = torch.empty_like(ref_d[0]), torch.empty_like(ref_d[1])
+    p_out, p_lse = torch.empty_like(ref_p[0]), torch.empty_like(ref_p[1])
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for _ in range(4):
+        d_out.fill_(0)
+        p_out.fill_(0)
+        ev = torch.cuda.Event()
+        ev.record()
+        s1.wait_event(ev)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s1):
+            sa.decode(*dargs, out=d_out, lse=d_lse, workspace_buf=dws)
+        with torch.cuda.stream(s2):
+            sa.prefill(*pargs, **pkw, out=p_out, lse=p_lse, workspace_buf=pws)
+        torch.cuda.synchronize()
+        assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
+        assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
+    assert sa.get_status(dws) == 0 and sa.get_status(pws) == 0
