@@ -84,6 +84,17 @@ typedef struct sinkattn_paged_desc {
                                 * pos - W < j <= pos (gptoss.md section 4: a 128-token
                                 * window on alternating layers, passed per call);
                                 * 0 or negative: no window */
+    int32_t max_sms;           /* SMs the persistent grids may use (split-KV decode and
+                                * prefill): 0 = all of them; n > 0 = at most n, leaving the
+                                * rest to kernels the caller runs at the same time on other
+                                * streams (for example a decode batch beside a chunked
+                                * prefill).  Negative: SINKATTN_ERR_INVALID_ARG.  No page
+                                * has this: it is a scheduling control of this library.  It
+                                * changes which warp does which part of a decode, so decode
+                                * sums may round differently than with all SMs; prefill
+                                * results do not depend on it.  The decode workspace size
+                                * query takes it into account (a smaller grid needs fewer
+                                * partial-state slots). */
 } sinkattn_paged_desc;
 
 /* Human-readable name of an error code (static string). */

@@ -97,7 +97,7 @@ int encode_rows_map(CUtensorMap *m, const void *base, int T, int H, int D, int r
 int check_heads(const sinkattn_paged_desc *d) {
     if (!d) return SINKATTN_ERR_INVALID_ARG;
     if (d->num_seqs < 0 || d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
-        d->num_pages < 0 || d->max_pages_per_seq < 0)
+        d->num_pages < 0 || d->max_pages_per_seq < 0 || d->max_sms < 0)
         return SINKATTN_ERR_INVALID_ARG;
     if (d->num_qo_heads % d->num_kv_heads) return SINKATTN_ERR_INVALID_ARG;
     const int G = d->num_qo_heads / d->num_kv_heads;
@@ -140,6 +140,17 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
                                          &L->warps_per_cta8, &L->smem8),
                  "fp8 decode launch shape");
     if (rc) return rc;
+    if (d->max_sms > 0) {
+        // both grids are (SMs x CTAs per SM); keep the CTAs per SM, on max_sms SMs
+        int sms = 0;
+        rc = cuda_rc(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
+                     "cudaDeviceGetAttribute");
+        if (rc) return rc;
+        if (d->max_sms < sms) {
+            L->ctas = L->ctas / sms * d->max_sms;
+            L->ctas8 = L->ctas8 / sms * d->max_sms;
+        }
+    }
     L->total_warps = L->ctas * L->warps_per_cta;
     L->total_warps8 = L->ctas8 * L->warps_per_cta8;
     const int most = L->total_warps > L->total_warps8 ? L->total_warps : L->total_warps8;
@@ -433,6 +444,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     a.num_pages = has_prefix ? desc->num_pages : 0;
     a.max_pages = has_prefix ? desc->max_pages_per_seq : 0;
     a.window = desc->window > 0 ? desc->window : 0;
+    a.max_sms = desc->max_sms;
     a.status = static_cast<uint32_t *>(workspace);
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
     if (e == cudaErrorNotSupported) return SINKATTN_ERR_UNSUPPORTED;

@@ -74,6 +74,7 @@ struct PrefillArgs {
     float *lse;  // [T, Hq] or nullptr
     int T, n, Hq, Hkv, G, D, num_pages, max_pages;
     int window;  // sliding window (keys at the query's last `window` positions); 0: none
+    int max_sms;  // SMs the persistent grid may use; 0: all
     uint32_t *status;
 };
 // Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.

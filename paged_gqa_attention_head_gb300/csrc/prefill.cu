@@ -940,7 +940,9 @@ cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtens
     int device = 0, sms = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) return e;
-    // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more)
+    // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more),
+    // on at most max_sms SMs when the caller keeps the others for concurrent work
+    if (a.max_sms > 0 && a.max_sms < sms) sms = a.max_sms;
     prefill_kernel<D, kWindow><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
     return cudaGetLastError();
 }

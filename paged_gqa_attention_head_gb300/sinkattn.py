@@ -30,7 +30,7 @@ _P, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_si
 class PagedDesc(ctypes.Structure):
     _fields_ = [("num_seqs", _I32), ("num_qo_heads", _I32), ("num_kv_heads", _I32),
                 ("head_dim", _I32), ("page_size", _I32), ("num_pages", _I32),
-                ("max_pages_per_seq", _I32), ("window", _I32)]
+                ("max_pages_per_seq", _I32), ("window", _I32), ("max_sms", _I32)]
 
 
 _DP = ctypes.POINTER(PagedDesc)
@@ -128,11 +128,13 @@ def workspace(nbytes: int, device: torch.device, tag: str = "default") -> torch.
 
 
 def paged_desc(num_seqs, num_qo_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
-               page_size=PAGE_SIZE, window=0) -> PagedDesc:
+               page_size=PAGE_SIZE, window=0, max_sms=0) -> PagedDesc:
     """window > 0: sliding window (each query sees the keys at its last `window`
-    positions); 0: full attention."""
+    positions); 0: full attention.  max_sms > 0: the persistent decode and prefill grids
+    use at most that many SMs (the rest stay free for concurrent work on other streams);
+    0: all SMs."""
     return PagedDesc(num_seqs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
-                     max_pages_per_seq, int(window))
+                     max_pages_per_seq, int(window), int(max_sms))
 
 
 _ws_sizes: dict = {}
@@ -171,7 +173,7 @@ def _codes(t: torch.Tensor) -> torch.Tensor:
 
 
 def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
-                 want_lse, window=0, kv_dtype=torch.bfloat16):
+                 want_lse, window=0, kv_dtype=torch.bfloat16, max_sms=0):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k_pages, "k_pages", kv_dtype, dev, 4)
@@ -196,7 +198,8 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
         lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
     elif lse is not None:
         _need(lse, "lse", torch.float32, dev, 2)
-    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window)
+    desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window,
+                      max_sms=max_sms)
     nbytes = decode_workspace_size(desc)
     if ws is None:
         ws = workspace(nbytes, dev)
@@ -207,11 +210,12 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None, lse=None,
-           workspace_buf=None, return_lse=True, window=0):
-    """Split-KV paged decode with sinks (sinkattn_decode).  window > 0: sliding window.
-    Returns (out, lse)."""
+           workspace_buf=None, return_lse=True, window=0, max_sms=0):
+    """Split-KV paged decode with sinks (sinkattn_decode).  window > 0: sliding window;
+    max_sms > 0: the split-KV grid on at most that many SMs.  Returns (out, lse)."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
-                                             scale, out, lse, workspace_buf, return_lse, window)
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             max_sms=max_sms)
     _check(load().sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                   _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                   ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(q.device)),
@@ -220,10 +224,11 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, o
 
 
 def decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
-                   lse=None, workspace_buf=None, return_lse=True, window=0):
+                   lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
     """First decode kernel only (sinkattn_decode_splitkv); follow with decode_merge."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
-                                             scale, out, lse, workspace_buf, return_lse, window)
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             max_sms=max_sms)
     _check(load().sinkattn_decode_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                           _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                           ctypes.byref(desc), _ptr(ws), ws.numel(),
@@ -241,9 +246,10 @@ def decode_merge(seq_lens, sinks, out, lse, desc, ws):
 
 def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
             prefix_block_table=None, prefix_lens=None, out=None, lse=None, workspace_buf=None,
-            return_lse=True, window=0):
+            return_lse=True, window=0, max_sms=0):
     """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  window > 0:
-    sliding window.  Returns (out, lse)."""
+    sliding window; max_sms > 0: the persistent grid on at most that many SMs.  Returns
+    (out, lse)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k, "k", torch.bfloat16, dev, 3)
@@ -267,7 +273,7 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
-    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window)
+    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window, max_sms=max_sms)
     nbytes = prefill_workspace_size(desc)
     ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -308,14 +314,14 @@ def _scales(k_scale, v_scale, Hkv, dev):
 
 
 def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None, scale=None,
-               out=None, lse=None, workspace_buf=None, return_lse=True, window=0):
+               out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
     """Split-KV paged decode over an FP8 E4M3 cache (sinkattn_decode_fp8).  k_pages / v_pages:
     uint8 (or float8_e4m3fn) [num_pages, Hkv, 16, D] codes; k_scale / v_scale: float32 [Hkv]
     per-KV-head scales or None (1).  Returns (out, lse)."""
     k_pages, v_pages = _codes(k_pages), _codes(v_pages)
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             kv_dtype=torch.uint8)
+                                             kv_dtype=torch.uint8, max_sms=max_sms)
     _scales(k_scale, v_scale, k_pages.shape[1], q.device)
     _check(load().sinkattn_decode_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                       _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(sinks),
@@ -325,12 +331,13 @@ def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sin
 
 
 def decode_fp8_splitkv(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None,
-                       scale=None, out=None, lse=None, workspace_buf=None, return_lse=True, window=0):
+                       scale=None, out=None, lse=None, workspace_buf=None, return_lse=True, window=0,
+                       max_sms=0):
     """First kernel of decode_fp8 only (sinkattn_decode_fp8_splitkv); follow with decode_merge."""
     k_pages, v_pages = _codes(k_pages), _codes(v_pages)
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             kv_dtype=torch.uint8)
+                                             kv_dtype=torch.uint8, max_sms=max_sms)
     _scales(k_scale, v_scale, k_pages.shape[1], q.device)
     _check(load().sinkattn_decode_fp8_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                               _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),

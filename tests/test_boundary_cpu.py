@@ -56,6 +56,7 @@ def _desc(sa, **kw):
     (dict(head_dim=96), 2), (dict(num_qo_heads=12, num_kv_heads=4), 2),   # G = 3
     (dict(num_qo_heads=9), 1), (dict(num_pages=0), 1), (dict(max_pages_per_seq=0), 1),
     (dict(num_kv_heads=0), 1), (dict(num_qo_heads=64, num_kv_heads=2), 2),  # G = 32
+    (dict(max_sms=-1), 1),
 ])
 def test_decode_workspace_size_rejects(sa, bad, code):
     n = ctypes.c_size_t()
@@ -103,3 +104,13 @@ def test_prefix_arguments_all_or_nothing(sa):
     rc = lib.sinkattn_prefill(p, p, p, p, 8, p, None, None, None, None, 0.125, p, None,
                               ctypes.byref(d), p, 256, None)
     assert rc == 1
+
+
+def test_desc_layout_matches_the_header(sa):
+    """The binding's struct has the header's fields, in order, all int32."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct sinkattn_paged_desc \{(.*?)\} sinkattn_paged_desc;", text,
+                     flags=re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+)\s*;", body)
+    assert [f for f, _ in sa.PagedDesc._fields_] == fields
+    assert ctypes.sizeof(sa.PagedDesc) == 4 * len(fields)

@@ -1,11 +1,13 @@
 """Calls on different streams run concurrently and independently: a decode and a chunked
 prefill issued at the same time on two streams (each with its own workspace, as a
 serving loop mixing decode and prefill requests would do) give bit for bit the results
-of the same calls issued one after the other."""
+of the same calls issued one after the other.  With desc.max_sms the persistent grids
+leave SMs free for such concurrent work; capped calls keep their results."""
 import pytest
 import torch
 
 from paged_gqa_attention_head_gb300 import inputs
+from tolerances import check_lse, check_out
 
 pytestmark = pytest.mark.gpu
 
@@ -53,3 +55,44 @@ def test_decode_and_chunked_prefill_on_two_streams_match_sequential(sa, cuda_dev
         assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
         assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
     assert sa.get_status(dws) == 0 and sa.get_status(pws) == 0
+
+
+@pytest.mark.parametrize("max_sms", [1, 37])
+def test_prefill_on_fewer_sms_is_bit_identical(sa, cuda_dev, max_sms):
+    """desc.max_sms caps the persistent prefill grid; every item is computed the same way
+    whichever CTA takes it, so the results do not change."""
+    dev = cuda_dev
+    p = inputs.make_prefill([700, 129, 512], 64, 8, 64, seed=213, sinks=True,
+                            prefix_lens=[3000, 0, 1200])
+    pre = p.prefix
+    args = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+    kw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
+              prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
+    ref = [t.clone() for t in sa.prefill(*args, **kw)]
+    got = sa.prefill(*args, **kw, max_sms=max_sms)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+
+
+@pytest.mark.parametrize("max_sms", [1, 20])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_decode_on_fewer_sms_matches_the_oracle(sa, oracle_mod, cuda_dev, max_sms, kv):
+    """desc.max_sms caps the persistent split-KV grid (fewer warps, longer shares, other
+    split points): the results stay within the parity bar of the oracle."""
+    dev = cuda_dev
+    w = inputs.make_decode(("uniform", 1, 5000), 24, 32, 4, 64, seed=214, sinks=True, kv_dtype=kv)
+    c = w.cache
+    common = (c.block_table.to(dev), c.lens.to(dev), w.sinks.to(dev), w.scale)
+    if kv == "fp8":
+        out, lse = sa.decode_fp8(w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev),
+                                 c.k_scale.to(dev), c.v_scale.to(dev), *common, max_sms=max_sms)
+        ro, rl = oracle_mod.decode_fp8(w.q, c.k_pages, c.v_pages, c.k_scale, c.v_scale,
+                                       c.block_table, c.lens, w.sinks, w.scale)
+    else:
+        out, lse = sa.decode(w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), *common,
+                             max_sms=max_sms)
+        ro, rl = oracle_mod.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks,
+                                   w.scale)
+    torch.cuda.synchronize()
+    check_out(out, ro)
+    check_lse(lse, rl)
