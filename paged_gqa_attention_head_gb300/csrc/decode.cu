@@ -13,7 +13,8 @@
 // contiguous ranges, one per warp, so every warp moves the same number of bytes
 // whatever the length mix.  Each warp streams its pages through a private ring
 // of shared-memory stages filled by TMA (4-D tensor maps over the page pool,
-// 128-byte swizzle), and computes all G query heads of the KV head with
+// 128-byte swizzle; the grid is as many 4-warp CTAs as fit on every SM), and
+// computes all G query heads of the KV head with
 // m16n8k16 tensor-core MMAs (heads on the M axis, 16 tokens of a page on N).
 // A (sequence, KV head) that one warp covers entirely is finished in place with
 // the sink folded in; otherwise the warp leaves a sink-free partial state and
@@ -35,7 +36,12 @@ template <int D>
 struct DecodeCfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = kWarps * 32;
-    static constexpr int kStages = D == 64 ? 6 : 3;
+    // Ring depth per warp.  An SM keeps ~192 KB of pages in flight either way; shallow
+    // rings let more warps share it (D=64: 3 x 4 KB per warp, four 4-warp CTAs per SM;
+    // D=128: 2 x 8 KB, three CTAs, bounded by registers), and the per-warp work on a page
+    // (ldmatrix, MMAs, softmax), not HBM, is what more warps hide: measured 6 -> 3 stages
+    // at D=64 raised a 256-sequence long-context batch from 6.04 to 6.57 TB/s.
+    static constexpr int kStages = D == 64 ? 3 : 2;
     static constexpr int kHalves = D / 64;               // 128-byte column blocks per row
     static constexpr int kPageBytes = kPageSize * D * 2;  // one (page, head) of K or of V
     static constexpr int kStageBytes = 2 * kPageBytes;
