@@ -41,6 +41,9 @@
  *     that lives in the workspace; read it with sinkattn_get_status.  Outputs of
  *     the affected rows are then unspecified (but no memory outside the given
  *     buffers is touched).
+ *   - Empty work: a decode with num_seqs == 0, or a prefill or append with
+ *     num_seqs == 0 or total_tokens == 0, returns SINKATTN_OK at once after the
+ *     descriptor's shapes are checked; its data pointers may then be NULL.
  */
 #ifndef SINKATTN_H
 #define SINKATTN_H

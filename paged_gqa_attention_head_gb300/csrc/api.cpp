@@ -222,6 +222,7 @@ int append_common(const void *k, const void *v, const int32_t *cu_seqlens, int32
     int rc = check_heads(desc);
     if (rc) return rc;
     if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;  // no tokens: a no-op
     if (!k || !v || !cu_seqlens || !block_table || !start_pos || !k_pages || !v_pages)
         return SINKATTN_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
@@ -301,6 +302,8 @@ int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pa
                             const float *sinks, float scale, void *out, float *lse,
                             const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                             sinkattn_stream_t stream) {
+    // an empty batch is a no-op (its data pointers may be NULL)
+    if (desc && desc->num_seqs == 0) return check_decode_desc(desc);
     DecodePrep P;
     int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
                             ws_bytes, &P);
@@ -321,6 +324,7 @@ int sinkattn_decode_splitkv(const void *q, const void *k_pages, const void *v_pa
 int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out, float *lse,
                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                           sinkattn_stream_t stream) {
+    if (desc && desc->num_seqs == 0) return check_decode_desc(desc);  // an empty batch
     DecodePrep P;
     // the merge reads the plan written by the split-KV kernel; q and the block
     // table are not used, so stand-in non-null pointers pass the checks
@@ -347,6 +351,8 @@ int sinkattn_decode_fp8_splitkv(const void *q, const void *k_pages, const void *
                                 const float *sinks, float scale, void *out, float *lse,
                                 const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                                 sinkattn_stream_t stream) {
+    // an empty batch is a no-op (its data pointers may be NULL)
+    if (desc && desc->num_seqs == 0) return check_decode_desc(desc);
     DecodePrep P;
     int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
                             ws_bytes, &P);
@@ -397,6 +403,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     int rc = check_heads(desc);
     if (rc) return rc;
     if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
+    if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;  // no tokens: a no-op
     if (!(scale > 0.f) || !(scale < INFINITY)) return SINKATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !cu_seqlens || !out || !workspace) return SINKATTN_ERR_INVALID_ARG;
     if (ws_bytes < kStatusBytes) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;

@@ -76,11 +76,28 @@ def test_null_pointers_rejected_before_cuda(sa):
     d = _desc(sa)
     assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None,
                                ctypes.byref(d), None, 0, None) == 1
-    assert lib.sinkattn_prefill(None, None, None, None, 0, None, None, None, None, None, 0.125,
+    assert lib.sinkattn_prefill(None, None, None, None, 8, None, None, None, None, None, 0.125,
                                 None, None, ctypes.byref(d), None, 0, None) == 1
-    assert lib.sinkattn_append_kv(None, None, None, 0, None, None, None, None, ctypes.byref(d),
+    assert lib.sinkattn_append_kv(None, None, None, 8, None, None, None, None, ctypes.byref(d),
                                   None, 0, None) == 1
     assert lib.sinkattn_get_status(None, None, None) == 1
+
+
+def test_empty_work_is_a_no_op_before_cuda(sa):
+    """No sequences (decode) or no tokens (prefill, append): OK at once, NULL data allowed;
+    the descriptor is still checked."""
+    lib = sa.load()
+    d = _desc(sa, num_seqs=0)
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None,
+                               ctypes.byref(d), None, 0, None) == 0
+    d = _desc(sa)
+    assert lib.sinkattn_prefill(None, None, None, None, 0, None, None, None, None, None, 0.125,
+                                None, None, ctypes.byref(d), None, 0, None) == 0
+    assert lib.sinkattn_append_kv(None, None, None, 0, None, None, None, None, ctypes.byref(d),
+                                  None, 0, None) == 0
+    bad = _desc(sa, num_seqs=0, head_dim=96)
+    assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None,
+                               ctypes.byref(bad), None, 0, None) == 2
 
 
 def test_misaligned_pointers_rejected(sa):
