@@ -21,7 +21,7 @@ NVCC = os.environ.get("NVCC", "nvcc")
 
 
 # The prefill kernel re-balances registers between warpgroups with setmaxnreg; the
-# split adds up to exactly the registers it is launched with (384 threads x 168), so
+# split adds up to exactly the registers it is launched with (512 threads x 128), so
 # the build refuses any other register count (a larger split than the launch
 # budget would make setmaxnreg wait forever).
 PREFILL_LAUNCH_REGS = 128
