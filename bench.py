@@ -251,56 +251,110 @@ def run_ours(args, rank, world, local_rank):
     assert sa.get_status(sa.workspace(0, dev)) == 0, "device status reported a problem"
 
     # ---- e2e: the same decode through the C ABI with host buffers copied every step
-    # The step's inputs sit in one pinned staging buffer (q, block table, lengths, sinks at
+    # A step's inputs sit in one pinned staging buffer (q, block table, lengths, sinks at
     # 256-byte aligned offsets) and go over in one copy; out and lse are views of one device
-    # buffer and come back in one copy.
+    # buffer and come back in one copy.  Two slots of each: step k uses slot k % 2.
     names = ("q", "bt", "sl", "sk")
     offs, n_in = {}, 0
     for k in names:
         offs[k] = n_in
         n_in += -(-d[k].numel() * d[k].element_size() // 256) * 256
-    host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
-    dev_in_buf = torch.empty(n_in, dtype=torch.uint8, device=dev)
 
     def view(buf, k, like):
         nb = like.numel() * like.element_size()
         return buf[offs[k]:offs[k] + nb].view(like.dtype).view(like.shape)
 
-    for k in names:
-        view(host_in, k, d[k]).copy_(d[k].cpu())
-    dev_in = {k: view(dev_in_buf, k, d[k]) for k in names}
     n_out = out.numel() * 2
-    dev_res = torch.empty(n_out + lse.numel() * 4, dtype=torch.uint8, device=dev)
-    out_v = dev_res[:n_out].view(torch.bfloat16).view(out.shape)
-    lse_v = dev_res[n_out:].view(torch.float32).view(lse.shape)
-    host_res = torch.empty(dev_res.numel(), dtype=torch.uint8).pin_memory()
+    n_res = n_out + lse.numel() * 4
+    host_in = [torch.empty(n_in, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    dev_in_buf = [torch.empty(n_in, dtype=torch.uint8, device=dev) for _ in range(2)]
+    for hb in host_in:
+        for k in names:
+            view(hb, k, d[k]).copy_(d[k].cpu())
+    dev_in = [{k: view(b, k, d[k]) for k in names} for b in dev_in_buf]
+    dev_res = [torch.empty(n_res, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_v = [r[:n_out].view(torch.bfloat16).view(out.shape) for r in dev_res]
+    lse_v = [r[n_out:].view(torch.float32).view(lse.shape) for r in dev_res]
+    host_res = [torch.empty(n_res, dtype=torch.uint8).pin_memory() for _ in range(2)]
 
-    def e2e_step():
-        dev_in_buf.copy_(host_in, non_blocking=True)
-        sa.decode(dev_in["q"], d["kp"], d["vp"], dev_in["bt"], dev_in["sl"], dev_in["sk"], w.scale,
-                  out=out_v, lse=lse_v)
-        host_res.copy_(dev_res, non_blocking=True)
+    def decode_slot(s):
+        sa.decode(dev_in[s]["q"], d["kp"], d["vp"], dev_in[s]["bt"], dev_in[s]["sl"], dev_in[s]["sk"],
+                  w.scale, out=out_v[s], lse=lse_v[s])
+
+    def e2e_serial(n):
+        # copy in, decode, copy out, one after the other on the current stream
+        for _ in range(n):
+            dev_in_buf[0].copy_(host_in[0], non_blocking=True)
+            decode_slot(0)
+            host_res[0].copy_(dev_res[0], non_blocking=True)
+
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # the slot's inputs are on the device
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the slot's decode is done
+    ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's result is on the host
+
+    def e2e_pipelined(n):
+        # step k + 1's inputs go over on one copy stream while step k decodes on the current
+        # stream, and step k's result comes back on another; a slot is reused two steps later,
+        # once its decode (for the inputs) and its copy back (for the result) are done
+        main = torch.cuda.current_stream(dev)
+        h2d_stream.wait_stream(main)
+        d2h_stream.wait_stream(main)
+
+        def copy_in(k):
+            s = k % 2
+            if k >= 2:
+                h2d_stream.wait_event(ev_used[s])
+            with torch.cuda.stream(h2d_stream):
+                dev_in_buf[s].copy_(host_in[s], non_blocking=True)
+            ev_in[s].record(h2d_stream)
+
+        copy_in(0)
+        for k in range(n):
+            s = k % 2
+            if k + 1 < n:
+                copy_in(k + 1)
+            main.wait_event(ev_in[s])
+            if k >= 2:
+                main.wait_event(ev_back[s])
+            decode_slot(s)
+            ev_used[s].record(main)
+            d2h_stream.wait_event(ev_used[s])
+            with torch.cuda.stream(d2h_stream):
+                host_res[s].copy_(dev_res[s], non_blocking=True)
+            ev_back[s].record(d2h_stream)
+        main.wait_stream(h2d_stream)
+        main.wait_stream(d2h_stream)
 
     for _ in range(3):
-        e2e_step()
+        e2e_serial(1)
+    e2e_pipelined(4)
+    torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    # issued call by call from Python (host launch work included), then as a CUDA graph of K
-    # captured steps (how a serving loop issues them; each replayed step still copies its
-    # inputs in and its results out)
-    e2e_direct_ms = reduce_step_time(dist, time_loop(torch, e2e_step, args.steps, stream),
-                                     dev) / args.steps
-    egraph = capture_steps(torch, e2e_step, args.steps)
+    # issued call by call from Python (host launch work included), then as one CUDA graph of
+    # the K steps (how a serving loop issues them; each replayed step still copies its inputs
+    # in and its results out)
+    e2e_direct_ms = reduce_step_time(dist, time_loop(torch, lambda: e2e_pipelined(args.steps), 1,
+                                                     stream), dev) / args.steps
+    egraph = capture_steps(torch, lambda: e2e_pipelined(args.steps), 1)
+    sgraph = capture_steps(torch, lambda: e2e_serial(args.steps), 1)
     time_graph(torch, egraph, stream)
+    time_graph(torch, sgraph, stream)
     if dist:
         dist.barrier()
     e2e_ms = reduce_step_time(dist, time_graph(torch, egraph, stream), dev) / args.steps
-    h2d = host_in.numel()
-    d2h = host_res.numel()
+    if dist:
+        dist.barrier()
+    e2e_serial_ms = reduce_step_time(dist, time_graph(torch, sgraph, stream), dev) / args.steps
+    h2d = n_in
+    d2h = n_res
     torch.cuda.synchronize()
     ref_out, _ = sa.decode(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"], w.scale)
-    assert torch.equal(host_res[:n_out].view(torch.bfloat16).view(out.shape), ref_out.cpu()), \
-        "end-to-end decode differs from the device-resident one"
+    ref_host = ref_out.cpu()
+    for s in range(2):  # both slots hold a replayed step's result
+        assert torch.equal(host_res[s][:n_out].view(torch.bfloat16).view(out.shape), ref_host), \
+            "end-to-end decode differs from the device-resident one"
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -317,13 +371,17 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(whole_job_value(kv_bytes, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "every step copies q, block table, lengths and sinks in from one pinned "
-                        "host buffer (one copy), runs the decode and reads out + lse back (one "
-                        "copy); the K steps run as one captured CUDA graph; the KV cache is "
-                        "resident state",
+                "note": "every step copies q, block table, lengths and sinks in from a pinned "
+                        "host buffer (one copy), runs the decode and reads out + lse back into "
+                        "pinned host memory (one copy); step k+1's copy in and step k's copy out "
+                        "run on two copy streams while step k decodes (two buffer slots); the K "
+                        "steps run as one captured CUDA graph; the KV cache is resident state",
+                "serial": {"value": round(whole_job_value(kv_bytes, world, e2e_serial_ms), 2),
+                           "ms_per_step": round(e2e_serial_ms, 5),
+                           "note": "copy in, decode, copy out one after the other on one stream"},
                 "direct_calls": {"value": round(whole_job_value(kv_bytes, world, e2e_direct_ms), 2),
                                  "ms_per_step": round(e2e_direct_ms, 5),
-                                 "note": "the same steps issued call by call from Python"}},
+                                 "note": "the pipelined steps issued call by call from Python"}},
         "gpu_launches": 2 * args.steps,
         "launch": f"one CUDA graph of {args.steps} captured decode steps (split-KV + merge each), "
                   "replayed once",
