@@ -762,10 +762,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.s_free[b]);
                 }
-                if (ncols < kBN || lo > 0) {  // diagonal, ragged, prefix-tail or window edge
+                if (__any_sync(0xffffffffu, ncols < kBN || lo > 0)) {
+                    // diagonal, ragged, prefix-tail or window edge: only the 32-key chunks in
+                    // which some row of the warp hides a key are masked key by key
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c >= ncols || c < lo) sv[c] = 0xFF800000u;  // -inf
+                    for (int ch = 0; ch < kBN / 32; ++ch) {
+                        const int c0 = ch * 32;
+                        if (__any_sync(0xffffffffu, ncols < c0 + 32 || lo > c0)) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (c0 + e >= ncols || c0 + e < lo) sv[c0 + e] = 0xFF800000u;  // -inf
+                        }
+                    }
                 }
                 // row max: eight chains of three-input maxima over 16 keys each
                 float mx8[8];
