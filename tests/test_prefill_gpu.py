@@ -67,6 +67,46 @@ def test_chunked_prefill_over_paged_prefix(sa, oracle_mod, cuda_dev, D):
     assert sa.get_status(sa.workspace(0, cuda_dev, "prefill")) == 0
 
 
+def _grow_keys(p, per_tile):
+    """Scale every key by 1 + per_tile * position / 128, in the new tokens and in the prefix
+    pages, so that each 128-key tile's scores reach higher than the tile before: the running
+    max of every row grows through the row and the online softmax must rescale its output
+    (the keys are rounded to bf16 again, so the oracle and the kernel see the same values)."""
+    n = len(p.cu_seqlens) - 1
+    cu = p.cu_seqlens.tolist()
+    pre = p.prefix.lens.tolist() if p.prefix is not None else [0] * n
+    k = p.k.float()
+    for i in range(n):
+        pos = torch.arange(cu[i + 1] - cu[i], dtype=torch.float32) + pre[i]
+        k[cu[i]:cu[i + 1]] *= (1 + per_tile * pos / 128)[:, None, None]
+    p.k = k.bfloat16()
+    if p.prefix is not None:
+        kp = p.prefix.k_pages.float()
+        for i in range(n):
+            for pg in range((pre[i] + 15) // 16):
+                phys = int(p.prefix.block_table[i, pg])
+                pos = torch.arange(16, dtype=torch.float32) + 16 * pg
+                kp[phys] *= (1 + per_tile * pos / 128)[None, :, None]
+        p.prefix.k_pages = kp.bfloat16()
+    return p
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("per_tile", [3.0, 8.0])
+def test_prefill_running_max_grows_across_tiles(sa, oracle_mod, cuda_dev, D, per_tile):
+    """Scores that rise tile by tile (each tile's row max ~11 or ~30 log2 units above the
+    last): the output is rescaled many times within a row, causal and chunked."""
+    for prefix in (None, [300, 0, 700]):
+        p = inputs.make_prefill([600, 129, 260], 8, 2, D, seed=int(per_tile) + D, sinks=True,
+                                prefix_lens=prefix)
+        p = _grow_keys(p, per_tile)
+        out, lse = run_prefill(sa, p, cuda_dev)
+        ro, rl = oracle_prefill(oracle_mod, p)
+        check_out(out, ro)
+        check_lse(lse, rl)
+        assert sa.get_status(sa.workspace(0, cuda_dev, "prefill")) == 0
+
+
 def test_prefill_null_sinks_equal_neg_inf_bitwise(sa, cuda_dev):
     p = inputs.make_prefill([300, 129], 16, 4, 128, seed=4, sinks=False, prefix_lens=[40, 0])
     o1, l1 = run_prefill(sa, p, cuda_dev, sinks=None)
