@@ -448,6 +448,43 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
 
     for name in ("qwen3_decode", "longctx_decode"):
         rows[name] = decode_row(name)
+
+    # decode step with its K/V append: one call (the new rows written by the decode kernel)
+    # against two (the append kernel, then the decode); each a CUDA graph of `reps` steps
+    # over the same cache (every step rewrites the same slots with the same rows)
+    w = inputs.make_workload(HEADLINE, seed=0)
+    c = w.cache
+    q, sinks = w.q.to(dev), w.sinks.to(dev)
+    kp, vp, bt, sl = c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev)
+    B, Hkv, D = q.shape[0], kp.shape[1], q.shape[2]
+    k_new, v_new = (t.to(dev) for t in inputs.new_rows(B, Hkv, D, seed=0))
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    start = (sl - 1).clamp(min=0)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    fused = lambda: sa.decode_append(q, k_new, v_new, kp, vp, bt, sl, sinks, w.scale, out=out,  # noqa: E731
+                                     lse=lse)
+
+    def two_calls():
+        sa.append_kv(k_new, v_new, cu1, bt, start, kp, vp)
+        sa.decode(q, kp, vp, bt, sl, sinks, w.scale, out=out, lse=lse)
+
+    da = {}
+    for key, f in (("fused", fused), ("append_then_decode", two_calls)):
+        for _ in range(3):
+            f()
+        g = capture_steps(torch, f, reps)
+        time_graph(torch, g, stream)
+        da[key] = time_graph(torch, g, stream) / reps
+    nbytes = w.kv_bytes()
+    rows["gptoss_decode_append"] = {
+        "ms": round(da["fused"], 5), "GB/s": round(nbytes / (da["fused"] * 1e-3) / 1e9, 1),
+        "frac_hbm": round(nbytes / (da["fused"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+        "append_then_decode_ms": round(da["append_then_decode"], 5), "kv_bytes": nbytes,
+        "launch": f"CUDA graph of {reps} steps (fused: split-KV with append + merge; two calls: "
+                  "append, split-KV, merge)"}
+    del w, c, q, sinks, kp, vp, bt, sl, k_new, v_new, out, lse
+    torch.cuda.empty_cache()
     # a gpt-oss sliding-window layer (128 positions): the last 128 keys of each sequence,
     # ~9 MB of KV, so the launch and the first copies dominate
     rows["gptoss_decode_window128"] = decode_row(HEADLINE, window=128)

@@ -169,6 +169,32 @@ int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out
                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                           sinkattn_stream_t stream);
 
+/* Decode step with its K/V append: each sequence's new token (the step's query token) is
+ * written into the cache and then attended, in the order of TensorSharp
+ * docs/models/gptoss.md, section 3 "Forward graph" (append K and V to the cache, then
+ * attention over it), without a launch of its own: the warp that reads a sequence's last
+ * page puts the new row into its copy of the page and into the cache.
+ *
+ * k_new, v_new: bf16 [B, Hkv, D], 16-byte aligned: row (b, g) is the new token of
+ *              sequence b for KV head g
+ * seq_lens:    as for sinkattn_decode, COUNTING the new token: it sits at position
+ *              seq_lens[b] - 1, i.e. page block_table[b][(seq_lens[b] - 1) / 16], slot
+ *              (seq_lens[b] - 1) % 16.  A sequence with seq_lens[b] = 0 has no new token
+ *              (nothing is written; out = 0, lse = sink).
+ * k_pages, v_pages: the cache; the new rows are written into it (each (page, KV head,
+ *              slot) by exactly one thread; no other byte changes).  A block-table entry
+ *              outside [0, num_pages) sets SINKATTN_STATUS_BAD_PAGE and writes nothing.
+ * Other arguments, workspace and errors as for sinkattn_decode (and the sliding window
+ * and SM budget of the descriptor apply).  The result equals sinkattn_append_kv of the
+ * same rows at start positions seq_lens - 1 followed by sinkattn_decode, bit for bit.
+ * Sequences must not share the page their new token goes to.
+ */
+int sinkattn_decode_append(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                           void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                           const float *sinks, float scale, void *out, float *lse,
+                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                           sinkattn_stream_t stream);
+
 /* -------------------------------------------------------- FP8 E4M3 KV cache --
  * A KV cache of one byte per element.  The pages name an FP8 serving precision
  * ("GPT-OSS on Day 0", section "GPT-OSS on Hopper") and an 8-bit KV-cache type

@@ -212,6 +212,10 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.part_acc = reinterpret_cast<float *>(ws + P->layout.acc);
     a.k_scale = nullptr;
     a.v_scale = nullptr;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.k_pages_w = nullptr;
+    a.v_pages_w = nullptr;
     return SINKATTN_OK;
 }
 
@@ -343,6 +347,36 @@ int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
                                      lse, desc, workspace, ws_bytes, stream);
     if (rc) return rc;
     return sinkattn_decode_merge(seq_lens, sinks, out, lse, desc, workspace, ws_bytes, stream);
+}
+
+int sinkattn_decode_append(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                           void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                           const float *sinks, float scale, void *out, float *lse,
+                           const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                           sinkattn_stream_t stream) {
+    // an empty batch is a no-op (its data pointers may be NULL)
+    if (desc && desc->num_seqs == 0) return check_decode_desc(desc);
+    DecodePrep P;
+    int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
+                            ws_bytes, &P);
+    if (rc) return rc;
+    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !k_new || !v_new ||
+        !aligned(k_new, 16) || !aligned(v_new, 16))
+        return SINKATTN_ERR_INVALID_ARG;
+    CUtensorMap kmap, vmap;
+    rc = encode_pages_map(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    rc = encode_pages_map(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    P.args.k_new = k_new;
+    P.args.v_new = v_new;
+    P.args.k_pages_w = k_pages;
+    P.args.v_pages_w = v_pages;
+    rc = cuda_rc(launch_decode_splitkv(desc->head_dim, P.args, kmap, vmap, P.layout.ctas,
+                                       P.layout.smem, (cudaStream_t)stream),
+                 "split-KV decode with append launch");
+    if (rc) return rc;
+    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, (cudaStream_t)stream), "merge launch");
 }
 
 int sinkattn_decode_fp8_splitkv(const void *q, const void *k_pages, const void *v_pages,

@@ -19,6 +19,13 @@
 // A (sequence, KV head) that one warp covers entirely is finished in place with
 // the sink folded in; otherwise the warp leaves a sink-free partial state and
 // the merge kernel combines the pieces and adds the sink.
+//
+// Decode with append (the step's new K/V row of each sequence is first written to
+// the cache, then attended; TensorSharp docs/models/gptoss.md, section 3 "Forward
+// graph"): exactly one warp reads the last page of each (sequence, KV head).  Once
+// that page's copy has landed, the warp writes the new row, taken from the inputs,
+// over its slot in the shared-memory stage (the copy read the slot before the row
+// existed) and into the cache, so the append needs no launch of its own.
 #include <float.h>
 
 #include <mutex>
@@ -54,12 +61,12 @@ template <int D>
 int decode_smem_bytes(int B) {
     using C = DecodeCfg<D>;
     return 1024 /* alignment slack */ + C::kWarps * C::kWarpBytes +
-           C::kWarps * C::kStages * (8 + 4 + 4) + (3 * B + 1) * 4;
+           C::kWarps * C::kStages * (8 + 4 + 4 + 4) + (3 * B + 1) * 4;
 }
 
 // kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
-// window arithmetic.
-template <int D, bool kWindow>
+// window arithmetic.  kAppend: the new K/V rows a.k_new / a.v_new are appended (see above).
+template <int D, bool kWindow, bool kAppend = false>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -74,6 +81,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     int *s_prefix = s_lo + C::kWarps * S;
     int *s_len = s_prefix + a.B + 1;
     int *s_first = s_len + a.B;
+    int *s_pg = s_first + a.B;  // [warp][stage] physical page of the stage (appending kernel)
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
@@ -103,6 +111,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     uint64_t *wbar = bars + wid * S;
     int *wnv = s_nvalid + wid * S;
     int *wlo = s_lo + wid * S;
+    int *wpg = s_pg + wid * S;
 
     // locate the first unit: the last sequence whose first unit is <= u_begin
     Cursor cur;
@@ -158,6 +167,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             wnv[stage] = nv;
             // keys before the sliding window in this page are hidden
             if (kWindow) wlo[stage] = max(0, s_len[c.b] - a.window - kPageSize * page);
+            if (kAppend) wpg[stage] = pg;
             uint64_t *bar = &wbar[stage];
             uint8_t *kb = wbuf + stage * C::kStageBytes;
             uint8_t *vb = kb + C::kPageBytes;
@@ -216,6 +226,28 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
                     make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
+        }
+        if (kAppend) {
+            // the unit holding the sequence's last token (its new one, at L - 1): that row
+            // comes from the inputs, into the stage and into the cache (nv > 0: a valid page)
+            const int L = s_len[cur.b];
+            const int page = (kWindow ? s_first[cur.b] : 0) + cur.p;
+            if (nv > 0 && page == (L - 1) / kPageSize) {
+                constexpr int kChunks = D / 8;  // 16-byte chunks of one row
+                const int slot = (L - 1) % kPageSize;
+                if (lane < 2 * kChunks) {
+                    const bool isv = lane >= kChunks;
+                    const int ck = lane % kChunks;
+                    const int64_t row = ((int64_t)cur.b * a.Hkv + cur.g) * D + ck * 8;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const __nv_bfloat16 *>(isv ? a.v_new : a.k_new) + row);
+                    *reinterpret_cast<uint4 *>((isv ? vb : kb) + (ck >> 3) * 2048 + sw128(slot, ck & 7)) = w;
+                    const int64_t dst = (((int64_t)wpg[stage] * a.Hkv + cur.g) * kPageSize + slot) * D + ck * 8;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(isv ? a.v_pages_w : a.k_pages_w) +
+                                               dst) = w;
+                }
+                __syncwarp();
+            }
         }
 
         if (seg_start) {
@@ -437,13 +469,16 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    // both variants (with and without a window) get the same grid: the split plan and the
+    // every variant (with and without a window, with and without append) gets the same grid:
+    // the split plan and the
     // workspace layout depend on it
     int sms = 0, occ = 1 << 30;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    const void *kernels[2] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, false>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true>)};
+    const void *kernels[4] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, false>),
+                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true>),
+                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, false, true>),
+                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true, true>)};
     for (const void *k : kernels) {
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, k);
@@ -503,6 +538,17 @@ cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap 
                                   const CUtensorMap &vmap, int ctas, int smem_bytes,
                                   cudaStream_t stream) {
     const bool w = a.window > 0;
+    if (a.k_new) {  // decode with append: same grid and plan
+        if (D == 64 && w)
+            decode_splitkv_kernel<64, true, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+        else if (D == 64)
+            decode_splitkv_kernel<64, false, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+        else if (w)
+            decode_splitkv_kernel<128, true, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+        else
+            decode_splitkv_kernel<128, false, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
+        return cudaGetLastError();
+    }
     if (D == 64 && w)
         decode_splitkv_kernel<64, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
     else if (D == 64)

@@ -33,6 +33,10 @@ struct DecodeArgs {
     float *part_acc;        // [slots, G, D] partial unnormalised outputs
     const float *k_scale;   // FP8 cache: [Hkv] per-KV-head scales, or nullptr (1)
     const float *v_scale;
+    const void *k_new;      // decode with append: bf16 [B, Hkv, D] new rows, or nullptr
+    const void *v_new;
+    void *k_pages_w;        // the cache the new rows are written into (decode with append)
+    void *v_pages_w;
 };
 
 // Grid and shared memory of the split-KV decode kernel for head_dim D and

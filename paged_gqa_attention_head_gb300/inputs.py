@@ -245,6 +245,13 @@ def make_decode(lens_spec, batch: int, num_qo_heads: int, num_kv_heads: int, hea
     return DecodeInputs(q, cache, s, sc, num_qo_heads, num_kv_heads, head_dim)
 
 
+def new_rows(batch: int, num_kv_heads: int, head_dim: int, seed: int = 0):
+    """The new token's K and V rows of every sequence of a decode step, bf16 [B, Hkv, D]
+    ~ N(0, 1) (for the decode with append)."""
+    shape = (batch, num_kv_heads, head_dim)
+    return normal_bf16(shape, seed + 7919, _S_KNEW), normal_bf16(shape, seed + 7919, _S_VNEW)
+
+
 @dataclass
 class PrefillInputs:
     q: torch.Tensor  # [T, Hq, D] bf16 (new tokens, packed)

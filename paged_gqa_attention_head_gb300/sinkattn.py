@@ -43,6 +43,8 @@ SIGNATURES = {
     "sinkattn_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_splitkv": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_merge": (ctypes.c_int, [_P, _P, _P, _P, _DP, _P, _SZ, _P]),
+    "sinkattn_decode_append": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ,
+                                              _P]),
     "sinkattn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _P]),
     "sinkattn_prefill_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
     "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
@@ -311,6 +313,27 @@ def _scales(k_scale, v_scale, Hkv, dev):
             _need(t, name, torch.float32, dev, 1)
             if t.shape[0] != Hkv:
                 raise ValueError(f"{name} must have one entry per KV head")
+
+
+def decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None,
+                  out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
+    """Decode step with its K/V append (sinkattn_decode_append): the new rows k_new / v_new
+    [B, Hkv, D] go into the cache at position seq_lens - 1 (seq_lens counts them) and are
+    attended in the same pass.  k_pages / v_pages are written in place.  Returns (out, lse)."""
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             max_sms=max_sms)
+    B, Hkv, D = q.shape[0], k_pages.shape[1], q.shape[2]
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, torch.bfloat16, q.device, 3)
+        if tuple(t.shape) != (B, Hkv, D):
+            raise ValueError(f"{name} must be [B, Hkv, D] = {(B, Hkv, D)}")
+    _check(load().sinkattn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
+                                         _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                         _ptr(sinks), scale, _ptr(out), _ptr(lse), ctypes.byref(desc),
+                                         _ptr(ws), ws.numel(), _stream(q.device)),
+           "sinkattn_decode_append")
+    return out, lse
 
 
 def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None, scale=None,
