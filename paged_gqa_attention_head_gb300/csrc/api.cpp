@@ -356,13 +356,14 @@ int sinkattn_decode_append(const void *q, const void *k_new, const void *v_new, 
                            sinkattn_stream_t stream) {
     // an empty batch is a no-op (its data pointers may be NULL)
     if (desc && desc->num_seqs == 0) return check_decode_desc(desc);
+    // the new rows and the cache: checked before anything touches the device
+    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !k_new || !v_new ||
+        !aligned(k_new, 16) || !aligned(v_new, 16))
+        return SINKATTN_ERR_INVALID_ARG;
     DecodePrep P;
     int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
                             ws_bytes, &P);
     if (rc) return rc;
-    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !k_new || !v_new ||
-        !aligned(k_new, 16) || !aligned(v_new, 16))
-        return SINKATTN_ERR_INVALID_ARG;
     CUtensorMap kmap, vmap;
     rc = encode_pages_map(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
     if (rc) return rc;

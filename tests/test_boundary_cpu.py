@@ -81,6 +81,15 @@ def test_null_pointers_rejected_before_cuda(sa):
     assert lib.sinkattn_append_kv(None, None, None, 8, None, None, None, None, ctypes.byref(d),
                                   None, 0, None) == 1
     assert lib.sinkattn_get_status(None, None, None) == 1
+    assert lib.sinkattn_decode_append(None, None, None, None, None, None, None, None, 0.125, None,
+                                      None, ctypes.byref(d), None, 0, None) == 1
+    # every other pointer in place, the new rows missing or misaligned
+    buf = (ctypes.c_uint8 * 4096)()
+    p16 = (ctypes.addressof(buf) + 15) // 16 * 16
+    ws = (ctypes.addressof(buf) + 255) // 256 * 256
+    for k_new, v_new in ((None, p16), (p16, None), (p16 + 4, p16)):
+        assert lib.sinkattn_decode_append(p16, k_new, v_new, p16, p16, p16, p16, None, 0.125, p16,
+                                          None, ctypes.byref(d), ws, 256, None) == 1
 
 
 def test_empty_work_is_a_no_op_before_cuda(sa):
@@ -95,6 +104,9 @@ def test_empty_work_is_a_no_op_before_cuda(sa):
                                 None, None, ctypes.byref(d), None, 0, None) == 0
     assert lib.sinkattn_append_kv(None, None, None, 0, None, None, None, None, ctypes.byref(d),
                                   None, 0, None) == 0
+    d0 = _desc(sa, num_seqs=0)
+    assert lib.sinkattn_decode_append(None, None, None, None, None, None, None, None, 0.125, None,
+                                      None, ctypes.byref(d0), None, 0, None) == 0
     bad = _desc(sa, num_seqs=0, head_dim=96)
     assert lib.sinkattn_decode(None, None, None, None, None, None, 0.125, None, None,
                                ctypes.byref(bad), None, 0, None) == 2
