@@ -183,7 +183,8 @@ int sinkattn_decode_merge(const int32_t *seq_lens, const float *sinks, void *out
  *              (nothing is written; out = 0, lse = sink).
  * k_pages, v_pages: the cache; the new rows are written into it (each (page, KV head,
  *              slot) by exactly one thread; no other byte changes).  A block-table entry
- *              outside [0, num_pages) sets SINKATTN_STATUS_BAD_PAGE and writes nothing.
+ *              outside [0, num_pages) sets SINKATTN_STATUS_BAD_PAGE and writes nothing; so does
+ *              a length beyond max_pages_per_seq * 16 (SINKATTN_STATUS_BAD_LENGTH).
  * Other arguments, workspace and errors as for sinkattn_decode (and the sliding window
  * and SM budget of the descriptor apply).  The result equals sinkattn_append_kv of the
  * same rows at start positions seq_lens - 1 followed by sinkattn_decode, bit for bit.

@@ -229,10 +229,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         }
         if (kAppend) {
             // the unit holding the sequence's last token (its new one, at L - 1): that row
-            // comes from the inputs, into the stage and into the cache (nv > 0: a valid page)
+            // comes from the inputs, into the stage and into the cache (nv > 0: a valid page;
+            // a length beyond the block table, clamped above, has no slot: nothing is written)
             const int L = s_len[cur.b];
             const int page = (kWindow ? s_first[cur.b] : 0) + cur.p;
-            if (nv > 0 && page == (L - 1) / kPageSize) {
+            if (nv > 0 && page == (L - 1) / kPageSize && a.seq_lens[cur.b] == L) {
                 constexpr int kChunks = D / 8;  // 16-byte chunks of one row
                 const int slot = (L - 1) % kPageSize;
                 if (lane < 2 * kChunks) {

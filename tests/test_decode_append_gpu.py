@@ -103,3 +103,33 @@ def test_decode_append_gptoss_decode_config(sa, cuda_dev):
     assert torch.equal(_bits(out), _bits(ref_out))
     assert torch.equal(lse.cpu().view(torch.int32), ref_lse.cpu().view(torch.int32))
     assert torch.equal(_bits(kp), _bits(ref_kp)) and torch.equal(_bits(vp), _bits(ref_vp))
+
+
+def test_decode_append_length_beyond_block_table_writes_nothing(sa, cuda_dev):
+    """A length past the block table sets the status bit; that sequence's new row goes nowhere
+    (the other sequences' rows are written as usual)."""
+    lens = [20, 40, 33]
+    w = inputs.make_decode(lens, 3, 8, 2, 64, seed=9, sinks=True)
+    k_new, v_new = inputs.new_rows(3, 2, 64, seed=9)
+    d = _dev(w, cuda_dev)
+    cap = d["bt"].shape[1] * 16
+    bad = d["sl"].clone()
+    bad[1] = cap + 5
+    ok_kp, ok_vp = d["kp"].clone(), d["vp"].clone()
+    sa.decode_append(d["q"], k_new.to(cuda_dev), v_new.to(cuda_dev), ok_kp, ok_vp, d["bt"], d["sl"],
+                     d["sk"], w.scale)
+    kp, vp = d["kp"].clone(), d["vp"].clone()
+    ws = sa.workspace(0, cuda_dev)
+    sa.get_status(ws)
+    sa.decode_append(d["q"], k_new.to(cuda_dev), v_new.to(cuda_dev), kp, vp, d["bt"], bad, d["sk"],
+                     w.scale)
+    torch.cuda.synchronize()
+    assert sa.get_status(ws) & sa.STATUS_BAD_LENGTH
+    # the pages of sequence 1 keep their old contents, the others take the new rows
+    bt = w.cache.block_table
+    own1 = [int(p) for p in bt[1].tolist() if p >= 0]
+    others = [int(p) for r in (0, 2) for p in bt[r].tolist() if p >= 0]
+    assert torch.equal(_bits(kp[own1]), _bits(d["kp"][own1]))
+    assert torch.equal(_bits(vp[own1]), _bits(d["vp"][own1]))
+    assert torch.equal(_bits(kp[others]), _bits(ok_kp[others]))
+    assert torch.equal(_bits(vp[others]), _bits(ok_vp[others]))
