@@ -2,6 +2,7 @@
 cross-rank reduction the GPU replicas use (slowest rank's time, whole-job value), and
 the reference arm's non-zero ranks leave without work or output.  Decode and prefill
 do not shard (independent replicas), so this reduction is the only cross-rank step."""
+import json
 import os
 import socket
 import subprocess
@@ -71,3 +72,24 @@ def test_reference_arm_other_ranks_exit_without_work():
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the oracle on the host cores) on a single process: one JSON line
+    with the contract's keys, its cpu_baseline and e2e describing the same run."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
