@@ -309,7 +309,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
                      sinkattn_stream_t stream);
 
 /* ------------------------------------------------------------------ append --
- * Write new K/V rows into the paged cache ("append (K, V) to KV cache" before the
+ * Write new K/V rows into the paged cache (each layer stores its K and V there before its
  * attention, gptoss.md section 3).  Token t of request i (cu_seqlens[i] <= t <
  * cu_seqlens[i+1]) goes to position pos = start_pos[i] + t - cu_seqlens[i], i.e. slot
  * pos % 16 of page block_table[i][pos / 16], for every KV head.  A bit-exact copy.

@@ -234,8 +234,8 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 /*
- * Append new K/V rows into HND pages ("append (K, V) to KV cache" before the
- * attention, gptoss.md section 3).  Token t of sequence i goes to position
+ * Append new K/V rows into HND pages (each layer stores its K and V in the cache before
+ * its attention, gptoss.md section 3).  Token t of sequence i goes to position
  * pos = start_pos[i] + (t - cu_seqlens[i]): page block_table[i][pos / P], slot pos % P.
  * Copies bit patterns; pages are modified in place.  Returns -1 (nothing written)
  * if any destination is out of range.
