@@ -143,3 +143,14 @@ def test_desc_layout_matches_the_header(sa):
     fields = re.findall(r"int32_t\s+(\w+)\s*;", body)
     assert [f for f, _ in sa.PagedDesc._fields_] == fields
     assert ctypes.sizeof(sa.PagedDesc) == 4 * len(fields)
+
+
+def test_header_compiles_as_c99_and_cpp17(tmp_path):
+    """The boundary is a C ABI: its header stands alone in C99 and in C++17, warning-free."""
+    import shutil
+    for cc, std, lang in (("gcc", "c99", "c"), ("g++", "c++17", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        r = subprocess.run([cc, "-fsyntax-only", f"-std={std}", "-Wall", "-Wextra", "-Werror",
+                            "-x", lang, HEADER], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
