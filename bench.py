@@ -25,6 +25,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -646,9 +647,33 @@ def mixed_row(torch, sa, inputs, dev, stream, pk, reps):
     return r
 
 
+def _omp_threads(n: int):
+    """Set this process's OpenMP thread count (the runtime the oracle's parallel loops use);
+    returns the previous count, or None where the GNU OpenMP runtime cannot be loaded."""
+    import ctypes
+    try:
+        gomp = ctypes.CDLL("libgomp.so.1")
+    except OSError:
+        return None
+    old = gomp.omp_get_max_threads()
+    gomp.omp_set_num_threads(int(n))
+    return old
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(w, budget_s: float = 12.0):
     """The fp64 oracle on the host cores over the same decode batch, repeated
-    until about `budget_s` seconds of work."""
+    until about `budget_s` seconds of work; then once on a single core."""
     import oracle
     c = w.cache
     oracle.build()
@@ -660,10 +685,22 @@ def cpu_baseline(w, budget_s: float = 12.0):
     for _ in range(reps):
         oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
     el = time.perf_counter() - t0
-    return {"value": round(reps * w.kv_bytes() / el / 1e9, 3), "unit": "GB/s",
-            "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"the whole decode batch (64 sequences x 64 heads) x {reps} repetitions, "
-                      f"{el:.1f} s"}
+    r = {"value": round(reps * w.kv_bytes() / el / 1e9, 3), "unit": "GB/s",
+         "cores": oracle.max_threads(), "kind": "oracle", "cpu": _cpu_model(),
+         "sample": f"the whole decode batch (64 sequences x 64 heads) x {reps} repetitions, "
+                   f"{el:.1f} s"}
+    old = _omp_threads(1)
+    if old is not None:
+        try:
+            t0 = time.perf_counter()
+            oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
+            el1 = time.perf_counter() - t0
+            r["one_core"] = {"value": round(w.kv_bytes() / el1 / 1e9, 3), "unit": "GB/s",
+                             "cores": oracle.max_threads(),
+                             "sample": f"the whole decode batch once, {el1:.1f} s"}
+        finally:
+            _omp_threads(old)
+    return r
 
 
 # ----------------------------------------------------------------------------- reference
