@@ -59,6 +59,12 @@ def _load():
         lib.oracle_e4m3_codes.restype = None
         lib.oracle_e4m3_values.argtypes = [P, I64, P]
         lib.oracle_e4m3_values.restype = None
+        lib.oracle_rope_freqs.argtypes = [I, D, D, I, D, D, P, P]
+        lib.oracle_rope_freqs.restype = None
+        lib.oracle_rope.argtypes = [P, I64, I, I, P, D, D, I, D, D, P]
+        lib.oracle_rope.restype = None
+        lib.oracle_bf16_round_array.argtypes = [P, I64, P]
+        lib.oracle_bf16_round_array.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = I
         _lib = lib
@@ -266,6 +272,74 @@ def online(q, k, v, scale: float, sink: float, block: int, split_at: int = 0):
     return out, lse.value
 
 
+# gpt-oss's YaRN settings as TensorSharp gptoss.md section 3 gives them (original context
+# 4096, beta_fast 32, beta_slow 1); base and factor are the model's own (not on the pages)
+# and are arguments everywhere.
+ROPE_DEFAULTS = dict(original_context=4096, beta_fast=32.0, beta_slow=1.0)
+
+
+def rope_freqs(head_dim: int, base: float, factor: float, original_context: int = 4096,
+               beta_fast: float = 32.0, beta_slow: float = 1.0):
+    """YaRN-scaled rotation frequency of every pair (float64 [D/2]) and the magnitude
+    factor mscale (see sinkattn_oracle.c)."""
+    th = np.empty(head_dim // 2)
+    ms = ctypes.c_double()
+    _load().oracle_rope_freqs(head_dim, float(base), float(factor), int(original_context),
+                              float(beta_fast), float(beta_slow), _ptr(th), ctypes.byref(ms))
+    return th, ms.value
+
+
+def rope(x, positions, base: float, factor: float, original_context: int = 4096,
+         beta_fast: float = 32.0, beta_slow: float = 1.0) -> np.ndarray:
+    """NeoX rotary embedding with YaRN scaling of bf16 rows x [n, H, D], row r at
+    positions[r]; float64 [n, H, D], not rounded."""
+    xb = _bits(x)
+    n, H, D = xb.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64).reshape(n))
+    out = np.empty((n, H, D))
+    _load().oracle_rope(_ptr(xb), n, H, D, _ptr(pos), float(base), float(factor),
+                        int(original_context), float(beta_fast), float(beta_slow), _ptr(out))
+    return out
+
+
+def bf16_round(x) -> np.ndarray:
+    """Nearest bf16 (ties to even) of each float64 value, as uint16 bit patterns."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_bf16_round_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def decode_append_rope(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, sinks,
+                       scale: float, base: float, factor: float, original_context: int = 4096,
+                       beta_fast: float = 32.0, beta_slow: float = 1.0,
+                       select: Optional[np.ndarray] = None, window: int = 0):
+    """A decode step with rotary embedding and K/V append, in the pages' order
+    (TensorSharp gptoss.md section 3: RoPE on Q and K, append K and V to the cache, then
+    attention): q [B, Hq, D] and k_new [B, Hkv, D] (bf16, not yet rotated) are rotated at
+    the new token's position seq_lens[b] - 1 and rounded to bf16; the rotated key and
+    v_new are written to copies of the pages at that position (sequences with length 0
+    have no new token); then the rotated query attends the seq_lens[b] cached tokens.
+    Returns (out, lse, k_pages, v_pages, q_rot, k_rot) with the pages and the rotated rows
+    as uint16 bf16 bit arrays."""
+    lens = _i32(seq_lens)
+    B = lens.shape[0]
+    pos = np.maximum(lens.astype(np.int64) - 1, 0)
+    kw = dict(base=base, factor=factor, original_context=original_context, beta_fast=beta_fast,
+              beta_slow=beta_slow)
+    q_rot = bf16_round(rope(q, pos, **kw))
+    k_rot = bf16_round(rope(k_new, pos, **kw))
+    has = (lens > 0).astype(np.int64)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(has)
+    idx = np.nonzero(has)[0]
+    vb = _bits(v_new)
+    kp, vp = append_kv(np.ascontiguousarray(k_rot[idx]), np.ascontiguousarray(vb[idx]), cu,
+                       block_table, pos.astype(np.int32), k_pages, v_pages)
+    out, lse = decode(q_rot, kp, vp, block_table, lens, sinks, scale, select=select, window=window)
+    return out, lse, kp, vp, q_rot, k_rot
+
+
 class using_library:
     """Context manager: route this module's functions through another build of the
     oracle (used by the tests that plant a mistake in a copy of the oracle source)."""
@@ -280,7 +354,8 @@ class using_library:
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_decode", "oracle_prefill", "oracle_append_kv", "oracle_partial",
                      "oracle_merge", "oracle_online", "oracle_max_threads", "oracle_decode_fp8",
-                     "oracle_append_kv_fp8", "oracle_e4m3_codes", "oracle_e4m3_values"):
+                     "oracle_append_kv_fp8", "oracle_e4m3_codes", "oracle_e4m3_values",
+                     "oracle_rope_freqs", "oracle_rope", "oracle_bf16_round_array"):
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = lib

@@ -553,3 +553,89 @@ void oracle_e4m3_codes(const float *y, int64_t n, uint8_t *codes) {
 void oracle_e4m3_values(const uint8_t *codes, int64_t n, double *values) {
     for (int64_t i = 0; i < n; ++i) values[i] = oracle_e4m3_value(codes[i]);
 }
+
+/* ------------------------------------------------------------------------------
+ * Rotary position embedding, NeoX layout, with YaRN frequency scaling: the step the
+ * pages put on Q and K right before the K/V append and the attention (TensorSharp
+ * gptoss.md section 3 "Forward graph": RoPE_NeoX with YaRN scaling, original context
+ * 4096, freqScale = 1 / RopeScale, beta_fast = 32, beta_slow = 1; section 4.1
+ * "Attention"; "GPT-OSS on Day 0": YaRN position encoding as in DeepSeek-V3).  The pages
+ * name the parameters only.  The reading taken - the YaRN "by parts" interpolation as
+ * the rotary routine those pages call computes it:
+ *   - NeoX layout: element i < D/2 forms a pair with element i + D/2;
+ *   - base frequency of pair i: w_i = base^(-2i/D) radians per position;
+ *   - the pair index at which a full turn takes L0 / r positions (r turns over the
+ *     original context L0): c(r) = D ln(L0 / (2 pi r)) / (2 ln base);
+ *     lo = max(0, floor(c(beta_fast))), hi = min(D - 1, ceil(c(beta_slow)));
+ *   - blend over the pair index, y_i = clamp((i - lo) / max(0.001, hi - lo), 0, 1):
+ *     theta_i = (1 - y_i) w_i + y_i w_i / factor  (fast pairs keep their frequency,
+ *     slow pairs are interpolated by the factor, a linear ramp in between);
+ *   - magnitude: mscale = 1 + 0.1 ln(factor) multiplies both outputs of every pair;
+ *   - at position p, with a = p theta_i:
+ *       out[i]       = mscale (x[i] cos a - x[i + D/2] sin a)
+ *       out[i + D/2] = mscale (x[i + D/2] cos a + x[i] sin a).
+ * The rotated query and key are bf16 activations: rounded to the nearest bf16 value,
+ * ties to even, when they are used (oracle_bf16_round).
+ */
+void oracle_rope_freqs(int D, double base, double factor, int L0, double beta_fast,
+                       double beta_slow, double *theta, double *mscale) {
+    const double two_pi = 2.0 * acos(-1.0);
+    double lo = floor(D * log(L0 / (two_pi * beta_fast)) / (2.0 * log(base)));
+    double hi = ceil(D * log(L0 / (two_pi * beta_slow)) / (2.0 * log(base)));
+    if (lo < 0.0) lo = 0.0;
+    if (hi > D - 1) hi = D - 1;
+    const double span = (hi - lo) > 0.001 ? (hi - lo) : 0.001;
+    for (int i = 0; i < D / 2; ++i) {
+        const double w = pow(base, -2.0 * i / D);
+        double y = (i - lo) / span;
+        if (y < 0.0) y = 0.0;
+        if (y > 1.0) y = 1.0;
+        theta[i] = (1.0 - y) * w + y * (w / factor);
+    }
+    *mscale = 1.0 + 0.1 * log(factor);
+}
+
+/* Rotate rows x [n, H, D] (bf16 bits): row r at position pos[r], every head the same
+ * way; out [n, H, D] in double (not rounded). */
+void oracle_rope(const uint16_t *x, int64_t n, int H, int D, const int64_t *pos, double base,
+                 double factor, int L0, double beta_fast, double beta_slow, double *out) {
+    double *theta = malloc(sizeof(double) * (size_t)(D / 2));
+    double ms;
+    if (!theta) return;
+    oracle_rope_freqs(D, base, factor, L0, beta_fast, beta_slow, theta, &ms);
+    for (int64_t r = 0; r < n; ++r)
+        for (int h = 0; h < H; ++h) {
+            const uint16_t *xr = x + (r * H + h) * D;
+            double *o = out + (r * H + h) * D;
+            for (int i = 0; i < D / 2; ++i) {
+                const double a = (double)pos[r] * theta[i];
+                const double c = cos(a), s = sin(a);
+                const double x0 = bf16_to_double(xr[i]), x1 = bf16_to_double(xr[i + D / 2]);
+                o[i] = ms * (x0 * c - x1 * s);
+                o[i + D / 2] = ms * (x1 * c + x0 * s);
+            }
+        }
+    free(theta);
+}
+
+/* The bf16 value nearest to x (ties to the even significand), as its bit pattern:
+ * 8 significant bits, exponents down to the subnormal step 2^-133, +-inf past the
+ * largest finite value, NaN kept. */
+uint16_t oracle_bf16_round(double x) {
+    if (isnan(x)) return (uint16_t)0x7FC0;
+    if (x == 0.0) return signbit(x) ? (uint16_t)0x8000 : (uint16_t)0;
+    int e;
+    frexp(x, &e);            /* |x| = f 2^e, f in [0.5, 1): the leading bit is 2^(e-1) */
+    int ulp = e - 8;         /* 8 significant bits */
+    if (ulp < -133) ulp = -133;
+    double r = ldexp(rint(ldexp(x, -ulp)), ulp); /* rint: nearest, ties to even */
+    float f = (float)r;      /* exact: r has at most 8 significant bits */
+    if (fabs(r) > 3.3895313892515355e38) f = signbit(x) ? -INFINITY : INFINITY;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+void oracle_bf16_round_array(const double *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
+}

@@ -18,7 +18,13 @@ Each pin ties the oracle to something it does not share code with:
     (ties to the even code) and saturation; decode with power-of-two scales equal,
     bit for bit, to the bf16 decode of the same values; decode with arbitrary
     per-head scales against SDPA on torch-dequantised keys and values; the
-    quantising append against torch's cast, slot by slot.
+    quantising append against torch's cast, slot by slot;
+  * rotary embedding with YaRN scaling: at factor 1 the textbook rotation written as a
+    complex multiplication; position 0 and pair norms (the YaRN magnitude closed form);
+    scores that depend on the position offset only; a hand-derived example
+    (tests/golden/rope_yarn.json); bf16 rounding of every bf16 value, exact midpoints
+    and torch's float32 cast; the decode step with rotation and append against the
+    complex-form rotation, a contiguous copy of the keys and SDPA.
 
 test_planted_mistakes_are_caught compiles copies of the oracle source with one
 plausible mistake each (dropped sink term, wrong GQA head, off-by-one slot, sign
@@ -452,6 +458,138 @@ def pin_append_fp8(o):
     assert np.array_equal(kp.transpose(0, 2, 1, 3)[keep], old.transpose(0, 2, 1, 3)[keep])
 
 
+# ---------------------------------------------------------------- rotary embedding (YaRN)
+ROPE = dict(base=150000.0, factor=32.0, original_context=4096, beta_fast=32.0, beta_slow=1.0)
+
+
+def _rope_complex(x, pos, theta, mscale):
+    """Textbook form of the NeoX rotation: pair i is the complex number
+    x[i] + j x[i + D/2], multiplied by mscale e^(j p theta_i).  x [n, H, D] float64."""
+    half = x.shape[-1] // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    z = z * (mscale * np.exp(1j * np.asarray(pos, dtype=np.float64)[:, None, None] * theta))
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def pin_rope_plain_is_textbook(o):
+    # factor 1: no YaRN blend and mscale 1, plain NeoX rotary with w_i = base^(-2i/D)
+    for D in (64, 128):
+        x = inputs.normal_bf16((5, 3, D), seed=31, stream=1)
+        pos = np.array([0, 1, 17, 4095, 131071])
+        got = o.rope(x, pos, base=10000.0, factor=1.0)
+        theta = 10000.0 ** (-2.0 * np.arange(D // 2) / D)
+        want = _rope_complex(x.double().numpy(), pos, theta, 1.0)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-9)
+
+
+def pin_rope_position_zero_and_norms(o):
+    x = inputs.normal_bf16((4, 2, 64), seed=32, stream=1)
+    xd = x.double().numpy()
+    ms = 1.0 + 0.1 * math.log(ROPE["factor"])
+    got0 = o.rope(x, np.zeros(4, dtype=np.int64), **ROPE)
+    np.testing.assert_allclose(got0, ms * xd, rtol=1e-15, atol=0)
+    got = o.rope(x, np.array([3, 900, 20000, 131000]), **ROPE)
+    n_in = np.hypot(xd[..., :32], xd[..., 32:])
+    n_out = np.hypot(got[..., :32], got[..., 32:])
+    np.testing.assert_allclose(n_out, ms * n_in, rtol=1e-12, atol=1e-15)
+
+
+def pin_rope_relative_position(o):
+    # <R(m) q, R(n) k> = mscale <R(m - n) q, k>: the scores depend on the offset only
+    q = inputs.normal_bf16((1, 1, 64), seed=33, stream=1)
+    k = inputs.normal_bf16((1, 1, 64), seed=33, stream=2)
+    kd = k.double().numpy().reshape(-1)
+    ms = 1.0 + 0.1 * math.log(ROPE["factor"])
+    for m, n in ((10, 3), (5000, 4990), (131071, 65536), (7, 7)):
+        a = o.rope(q, [m], **ROPE).reshape(-1)
+        b = o.rope(k, [n], **ROPE).reshape(-1)
+        c = o.rope(q, [m - n], **ROPE).reshape(-1)
+        assert abs(a @ b - ms * (c @ kd)) <= 1e-9 * (1 + abs(a @ b)), (m, n)
+
+
+def pin_rope_golden(o):
+    g = json.load(open(os.path.join(GOLDEN, "rope_yarn.json")))
+    prm = g["params"]
+    D = prm["head_dim"]
+    env = {"log": math.log}
+    ms = eval(g["mscale"], {}, env)
+    kw = dict(base=prm["base"], factor=prm["factor"], original_context=prm["original_context"],
+              beta_fast=prm["beta_fast"], beta_slow=prm["beta_slow"])
+    theta, mscale = o.rope_freqs(D, **kw)
+    assert abs(mscale - ms) < 1e-15
+    for case in g["cases"]:
+        i, p = case["i"], case["p"]
+        th = eval(case["theta"], {}, env)
+        assert abs(theta[i] - th) <= 1e-15 * th, case
+        x = torch.zeros(2, 1, D, dtype=torch.bfloat16)
+        x[0, 0, i] = 1.0
+        x[1, 0, i + D // 2] = 1.0
+        got = o.rope(x, [p, p], **kw)
+        c, s = ms * math.cos(p * th), ms * math.sin(p * th)
+        np.testing.assert_allclose([got[0, 0, i], got[0, 0, i + D // 2]], [c, s], atol=1e-12)
+        np.testing.assert_allclose([got[1, 0, i], got[1, 0, i + D // 2]], [-s, c], atol=1e-12)
+        others = np.delete(got[0, 0], [i, i + D // 2])
+        assert np.all(others == 0.0)
+
+
+def pin_bf16_round(o):
+    # every bf16 value maps to itself
+    bits = np.arange(65536, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    finite = np.isfinite(vals)
+    got = o.bf16_round(vals[finite].astype(np.float64))
+    want = bits[finite].astype(np.uint16)
+    want[want == 0x8000] = 0x8000  # -0 stays -0
+    assert np.array_equal(got, want)
+    # exact midpoints between neighbours go to the even one; one double step off goes nearer
+    lo = (np.arange(0x0001, 0x7F7F, 97, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    hi = ((np.arange(0x0001, 0x7F7F, 97, dtype=np.uint32) + 1) << 16).view(np.float32).astype(np.float64)
+    mid = (lo + hi) / 2  # exact in double
+    lob = (lo.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    hib = lob + 1
+    even = np.where(lob % 2 == 0, lob, hib)
+    assert np.array_equal(o.bf16_round(mid), even)
+    assert np.array_equal(o.bf16_round(np.nextafter(mid, -np.inf)), lob)
+    assert np.array_equal(o.bf16_round(np.nextafter(mid, np.inf)), hib)
+    assert np.array_equal(o.bf16_round(-mid), even | 0x8000)
+    # float32 inputs: torch's float32 -> bfloat16 cast (round to nearest even) agrees
+    r = np.random.default_rng(3).standard_normal(200000).astype(np.float32) * 37.0
+    want = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o.bf16_round(r.astype(np.float64)), want)
+    assert o.bf16_round(np.array([3.4e38]))[0] == 0x7F80  # past the largest finite: inf
+
+
+def pin_decode_append_rope(o):
+    # the composed step against an independent path: the complex-number rotation with the
+    # (golden-pinned) YaRN frequencies, the (pinned) bf16 rounding, the new rows put into a
+    # contiguous copy of each sequence, and SDPA with the sink column
+    B, Hq, Hkv, D = 4, 8, 2, 64
+    w = inputs.make_decode([1, 17, 64, 300], B, Hq, Hkv, D, seed=34, sinks=True)
+    c = w.cache
+    kn, vn = inputs.new_rows(B, Hkv, D, seed=34)
+    out, lse, kp, vp, q_rot, k_rot = o.decode_append_rope(
+        w.q, kn, vn, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, **ROPE)
+    theta, ms = o.rope_freqs(D, **ROPE)
+    lens = c.lens.numpy()
+    pos = lens - 1
+    q_want = o.bf16_round(_rope_complex(w.q.double().numpy(), pos, theta, ms))
+    k_want = o.bf16_round(_rope_complex(kn.double().numpy(), pos, theta, ms))
+    assert np.array_equal(q_rot, q_want) and np.array_equal(k_rot, k_want)
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    for b in range(B):
+        k, v = contiguous_kv(c, b)
+        k, v = k.clone(), v.clone()
+        k[:, pos[b]] = to_t(k_want[b]).double()
+        v[:, pos[b]] = vn[b].double()
+        ref, ref_lse = sdpa_with_sink(to_t(q_want[b]).double()[:, None], k, v, w.scale, w.sinks)
+        np.testing.assert_allclose(out[b], ref[:, 0].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[b], ref_lse[:, 0].numpy(), rtol=0, atol=1e-10)
+        # the new slot holds the rotated key and the given value; nothing else changed
+        pg = int(c.block_table[b, pos[b] // 16])
+        assert np.array_equal(kp[pg, :, pos[b] % 16], k_want[b])
+        assert np.array_equal(vp[pg, :, pos[b] % 16], vn[b].view(torch.int16).numpy().view(np.uint16))
+
+
 PINS = {
     "decode_sdpa_nosink": lambda o: pin_decode_sdpa(o, False),
     "decode_sdpa_sink": lambda o: pin_decode_sdpa(o, True),
@@ -475,6 +613,12 @@ PINS = {
     "decode_fp8_pow2_is_bf16_decode": pin_decode_fp8_pow2_is_bf16_decode,
     "decode_fp8_sdpa": pin_decode_fp8_sdpa,
     "append_fp8": pin_append_fp8,
+    "rope_plain_is_textbook": pin_rope_plain_is_textbook,
+    "rope_position_zero_and_norms": pin_rope_position_zero_and_norms,
+    "rope_relative_position": pin_rope_relative_position,
+    "rope_golden": pin_rope_golden,
+    "bf16_round": pin_bf16_round,
+    "decode_append_rope": pin_decode_append_rope,
 }
 
 
@@ -534,6 +678,26 @@ MUTATIONS = [
      "const int64_t first = (window > 0 && L > window) ? L - window : 0;", "const int64_t first = 0;"),
     ("fp8 append quantises V with the K scale", "v_pages[off + d] = oracle_e4m3_code(vx / vs);",
      "v_pages[off + d] = oracle_e4m3_code(vx / ks);"),
+    ("rope pairs neighbours (GPT-J layout) instead of i, i + D/2",
+     "const double x0 = bf16_to_double(xr[i]), x1 = bf16_to_double(xr[i + D / 2]);",
+     "const double x0 = bf16_to_double(xr[(2 * i) % D]), x1 = bf16_to_double(xr[(2 * i + 1) % D]);"),
+    ("rope rotates the other way", "o[i] = ms * (x0 * c - x1 * s);", "o[i] = ms * (x0 * c + x1 * s);"),
+    ("rope frequency exponent i/D", "const double w = pow(base, -2.0 * i / D);",
+     "const double w = pow(base, -1.0 * i / D);"),
+    ("rope blend reversed", "theta[i] = (1.0 - y) * w + y * (w / factor);",
+     "theta[i] = y * w + (1.0 - y) * (w / factor);"),
+    ("rope correction dims not rounded",
+     "double lo = floor(D * log(L0 / (two_pi * beta_fast)) / (2.0 * log(base)));",
+     "double lo = (D * log(L0 / (two_pi * beta_fast)) / (2.0 * log(base)));"),
+    ("rope slow correction dim taken from beta_fast",
+     "double hi = ceil(D * log(L0 / (two_pi * beta_slow)) / (2.0 * log(base)));",
+     "double hi = ceil(D * log(L0 / (two_pi * beta_fast)) / (2.0 * log(base)));"),
+    ("rope without the YaRN magnitude", "*mscale = 1.0 + 0.1 * log(factor);", "*mscale = 1.0;"),
+    ("rope position off by one", "const double a = (double)pos[r] * theta[i];",
+     "const double a = (double)(pos[r] + 1) * theta[i];"),
+    ("bf16 rounding ties away from zero", "double r = ldexp(rint(ldexp(x, -ulp)), ulp);",
+     "double r = ldexp(round(ldexp(x, -ulp)), ulp);"),
+    ("bf16 rounding keeps 9 bits", "int ulp = e - 8;", "int ulp = e - 9;"),
     ("append writes the next slot",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)((pos + 1) % P));"),
