@@ -59,6 +59,9 @@ def _load():
         lib.oracle_e4m3_codes.restype = None
         lib.oracle_e4m3_values.argtypes = [P, I64, P]
         lib.oracle_e4m3_values.restype = None
+        lib.oracle_prefill_fp8.argtypes = [P, P, P, P, I, P, P, P, P, P, P, I64, I, P, D, I, I, I, I, I,
+                                           P, P, P]
+        lib.oracle_prefill_fp8.restype = I
         lib.oracle_rope_freqs.argtypes = [I, D, D, I, D, D, P, P]
         lib.oracle_rope_freqs.restype = None
         lib.oracle_rope.argtypes = [P, I64, I, I, P, D, D, I, D, D, P]
@@ -218,6 +221,32 @@ def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sin
     return out, lse
 
 
+def prefill_fp8(q, k, v, cu_seqlens, sinks, scale: float, k_pages, v_pages, k_scale, v_scale,
+                prefix_block_table, prefix_lens, select: Optional[np.ndarray] = None, window: int = 0):
+    """Chunked prefill over an FP8 E4M3 paged prefix: pages uint8 [num_pages, Hkv, P, D] of
+    codes (value scale[g] * e4m3(code), k_scale / v_scale fp32 [Hkv] or None for 1); the
+    new tokens' q, k, v bf16.  Returns (out [T, Hq, D], lse [T, Hq]) in float64."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    T, Hq, D = qb.shape
+    Hkv = kb.shape[1]
+    cu = _i32(cu_seqlens)
+    n = cu.shape[0] - 1
+    kp, vp = _u8(k_pages), _u8(v_pages)
+    num_pages, _, page_size, _ = kp.shape
+    pbt, pl = _i32(prefix_block_table), _i32(prefix_lens)
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
+    rc = lib.oracle_prefill_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), n, _ptr(kp), _ptr(vp),
+                                _ptr(_f32(k_scale)), _ptr(_f32(v_scale)), _ptr(pbt), _ptr(pl), num_pages,
+                                pbt.shape[1], _ptr(_f32(sinks)), float(scale), Hq, Hkv, D, page_size,
+                                int(window), _ptr(sel), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_fp8 rejected its inputs ({rc})")
+    return out, lse
+
+
 def append_kv_fp8(k, v, k_scale, v_scale, cu_seqlens, block_table, start_pos, k_pages, v_pages):
     """Quantise new bf16 rows to E4M3 codes (x / scale[g], nearest, saturating) and scatter
     them into copies of the uint8 pages; returns (k_pages, v_pages) as uint8 arrays."""
@@ -355,7 +384,8 @@ class using_library:
         for name in ("oracle_decode", "oracle_prefill", "oracle_append_kv", "oracle_partial",
                      "oracle_merge", "oracle_online", "oracle_max_threads", "oracle_decode_fp8",
                      "oracle_append_kv_fp8", "oracle_e4m3_codes", "oracle_e4m3_values",
-                     "oracle_rope_freqs", "oracle_rope", "oracle_bf16_round_array"):
+                     "oracle_rope_freqs", "oracle_rope", "oracle_bf16_round_array",
+                     "oracle_prefill_fp8"):
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = lib

@@ -639,3 +639,119 @@ uint16_t oracle_bf16_round(double x) {
 void oracle_bf16_round_array(const double *x, int64_t n, uint16_t *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
 }
+
+/* ------------------------------------------------------------------------------
+ * Chunked prefill over an FP8 E4M3 paged prefix: oracle_prefill with the prefix pages in
+ * the FP8 cache convention above (value = scale[g] * e4m3(code), per KV head, separately
+ * for K and V) and the new tokens' keys and values in bf16 as given.  Query t of request
+ * i at absolute position P_i + t sees the prefix keys 0 .. P_i - 1 and the new keys 0 .. t
+ * (with a window W > 0, only those at positions > P_i + t - W).
+ */
+static void attend_fp8_prefix(const uint16_t *q, int D, double scale, double sink, int64_t np,
+                              const uint8_t *const *kp, const uint8_t *const *vp, double ks, double vs,
+                              int64_t nn, const uint16_t *const *kn, const uint16_t *const *vn,
+                              double *s, double *out, double *lse) {
+    double m = sink;
+    for (int64_t j = 0; j < np; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * (ks * oracle_e4m3_value(kp[j][d]));
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    for (int64_t j = 0; j < nn; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(kn[j][d]);
+        s[np + j] = scale * dot;
+        if (s[np + j] > m) m = s[np + j];
+    }
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double z = exp(sink - m); /* the denominator, from the sink's term */
+    for (int64_t j = 0; j < np; ++j) {
+        double wt = exp(s[j] - m);
+        z += wt;
+        for (int d = 0; d < D; ++d) out[d] += wt * (vs * oracle_e4m3_value(vp[j][d]));
+    }
+    for (int64_t j = 0; j < nn; ++j) {
+        double wt = exp(s[np + j] - m);
+        z += wt;
+        for (int d = 0; d < D; ++d) out[d] += wt * bf16_to_double(vn[j][d]);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= z;
+    *lse = m + log(z);
+}
+
+int oracle_prefill_fp8(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const int32_t *cu_seqlens, int n, const uint8_t *k_pages,
+                       const uint8_t *v_pages, const float *k_scale, const float *v_scale,
+                       const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                       int64_t num_pages, int max_pages, const float *sinks, double scale, int Hq,
+                       int Hkv, int D, int P, int window, const uint8_t *select, double *out,
+                       double *lse) {
+    if (Hq % Hkv) return -1;
+    const int G = Hq / Hkv;
+    const int64_t T = cu_seqlens[n];
+    int32_t *seq_of = malloc(sizeof(int32_t) * (size_t)(T + 1));
+    if (!seq_of) return -2;
+    for (int i = 0; i < n; ++i) {
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) { free(seq_of); return -1; }
+        for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) seq_of[t] = i;
+        int Pi = prefix_lens[i];
+        if (Pi < 0 || (int64_t)Pi > (int64_t)max_pages * P) { free(seq_of); return -1; }
+        for (int j = 0; j < (Pi + P - 1) / P; ++j) {
+            int32_t pg = prefix_block_table[(int64_t)i * max_pages + j];
+            if (pg < 0 || pg >= num_pages) { free(seq_of); return -1; }
+        }
+    }
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t th = 0; th < T * Hq; ++th) {
+        if (select && !select[th]) continue;
+        const int64_t t = th / Hq;
+        const int h = (int)(th % Hq), i = seq_of[t], g = h / G;
+        const int64_t Pi = prefix_lens[i];
+        const int64_t tl = t - cu_seqlens[i];
+        const int64_t pos = Pi + tl;
+        const int64_t lo = (window > 0 && pos >= window) ? pos - window + 1 : 0; /* first visible */
+        /* visible prefix keys [lo, Pi) and new keys [max(lo, Pi) - Pi, tl] */
+        const int64_t np = lo < Pi ? Pi - lo : 0;
+        const int64_t n0 = lo > Pi ? lo - Pi : 0;
+        const int64_t nn = tl + 1 - n0;
+        const uint8_t **kp = malloc(sizeof(*kp) * (size_t)(np + 1));
+        const uint8_t **vp = malloc(sizeof(*vp) * (size_t)(np + 1));
+        const uint16_t **kn = malloc(sizeof(*kn) * (size_t)(nn + 1));
+        const uint16_t **vn = malloc(sizeof(*vn) * (size_t)(nn + 1));
+        double *s = malloc(sizeof(double) * (size_t)(np + nn + 1));
+        if (!kp || !vp || !kn || !vn || !s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+            for (int64_t j = 0; j < np; ++j) {
+                const int64_t key = lo + j;
+                const int64_t pg = prefix_block_table[(int64_t)i * max_pages + key / P];
+                const int64_t off = ((pg * Hkv + g) * (int64_t)P + key % P) * D;
+                kp[j] = k_pages + off;
+                vp[j] = v_pages + off;
+            }
+            for (int64_t j = 0; j < nn; ++j) {
+                const int64_t row = cu_seqlens[i] + n0 + j;
+                kn[j] = k + (row * Hkv + g) * D;
+                vn[j] = v + (row * Hkv + g) * D;
+            }
+            attend_fp8_prefix(q + th * D, D, scale, sink_of(sinks, h), np, kp, vp,
+                              k_scale == NULL ? 1.0 : (double)k_scale[g],
+                              v_scale == NULL ? 1.0 : (double)v_scale[g],
+                              nn, kn, vn, s, out + th * D, lse + th);
+        }
+        free(kp);
+        free(vp);
+        free(kn);
+        free(vn);
+        free(s);
+    }
+    free(seq_of);
+    return bad ? -2 : 0;
+}

@@ -288,10 +288,12 @@ class PrefillInputs:
 def make_prefill(new_lens: list[int], num_qo_heads: int, num_kv_heads: int, head_dim: int,
                  seed: int = 0, sinks: bool = True, scale: Optional[float] = None,
                  prefix_lens: Optional[list[int]] = None, poison: bool = True,
-                 extra_pages_per_seq: int = 0) -> PrefillInputs:
+                 extra_pages_per_seq: int = 0, prefix_kv_dtype: str = "bf16",
+                 fp8_unit_scales: bool = False) -> PrefillInputs:
     """Packed ragged prefill; with prefix_lens, each request already has that many
-    tokens in paged HND pages (chunked prefill).  extra_pages_per_seq widens each
-    block-table row so the new tokens can be appended after the prefix."""
+    tokens in paged HND pages (chunked prefill), bf16 or (prefix_kv_dtype "fp8") E4M3
+    codes with per-KV-head scales.  extra_pages_per_seq widens each block-table row so
+    the new tokens can be appended after the prefix."""
     T = sum(new_lens)
     cu = torch.zeros(len(new_lens) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(new_lens, dtype=torch.int64), 0).to(torch.int32)
@@ -304,7 +306,8 @@ def make_prefill(new_lens: list[int], num_qo_heads: int, num_kv_heads: int, head
     if prefix_lens is not None:
         maxp = max(1, max((P + PAGE_SIZE - 1) // PAGE_SIZE for P in prefix_lens)) + extra_pages_per_seq
         prefix = make_paged_cache(prefix_lens, num_kv_heads, head_dim, seed ^ 0x5EED, poison=poison,
-                                  max_pages_per_seq=maxp)
+                                  max_pages_per_seq=maxp, kv_dtype=prefix_kv_dtype,
+                                  fp8_unit_scales=fp8_unit_scales)
     return PrefillInputs(q, k, v, cu, list(new_lens), prefix, s, sc, num_qo_heads, num_kv_heads,
                          head_dim, list(prefix_lens) if prefix_lens is not None else [])
 
@@ -346,6 +349,10 @@ WORKLOADS = {
                            num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True),
     "longctx_chunked": dict(kind="chunked", lens=[512] * 8, prefix_lens=[16384] * 8,
                             num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True),
+    # the chunked prefill over an FP8 E4M3 prefix cache
+    "longctx_chunked_fp8": dict(kind="chunked", lens=[512] * 8, prefix_lens=[16384] * 8,
+                                num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,
+                                prefix_kv_dtype="fp8"),
     # the decode shapes over an FP8 E4M3 cache
     "gptoss_decode_fp8": dict(kind="decode", batch=64, lens=("uniform", 512, 8192),
                               num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,
@@ -371,5 +378,6 @@ def make_workload(name: str, seed: int = 0):
                             seed=seed, sinks=w["sinks"])
     if kind == "chunked":
         return make_prefill(w["lens"], w["num_qo_heads"], w["num_kv_heads"], w["head_dim"],
-                            seed=seed, sinks=w["sinks"], prefix_lens=w["prefix_lens"])
+                            seed=seed, sinks=w["sinks"], prefix_lens=w["prefix_lens"],
+                            prefix_kv_dtype=w.get("prefix_kv_dtype", "bf16"))
     raise ValueError(kind)

@@ -24,7 +24,10 @@ Each pin ties the oracle to something it does not share code with:
     scores that depend on the position offset only; a hand-derived example
     (tests/golden/rope_yarn.json); bf16 rounding of every bf16 value, exact midpoints
     and torch's float32 cast; the decode step with rotation and append against the
-    complex-form rotation, a contiguous copy of the keys and SDPA.
+    complex-form rotation, a contiguous copy of the keys and SDPA;
+  * chunked prefill over an FP8 prefix: with power-of-two scales equal, bit for bit, to the
+    bf16 prefill over the same values (also windowed); with arbitrary per-head scales
+    against SDPA on torch-dequantised prefix pages and the bf16 new keys.
 
 test_planted_mistakes_are_caught compiles copies of the oracle source with one
 plausible mistake each (dropped sink term, wrong GQA head, off-by-one slot, sign
@@ -590,6 +593,62 @@ def pin_decode_append_rope(o):
         assert np.array_equal(vp[pg, :, pos[b] % 16], vn[b].view(torch.int16).numpy().view(np.uint16))
 
 
+# ---------------------------------------------------------------- chunked prefill, FP8 prefix
+def _fp8_prefill_case(pow2: bool, seed: int):
+    p = inputs.make_prefill([70, 1, 33], 8, 2, 64, seed=seed, sinks=True, prefix_lens=[100, 37, 0],
+                            prefix_kv_dtype="fp8")
+    c = p.prefix
+    if pow2:
+        c.k_scale = torch.tensor([0.25, 2.0], dtype=torch.float32)
+        c.v_scale = torch.tensor([0.5, 0.125], dtype=torch.float32)
+    return p, c
+
+
+def _bf16_pages_from_fp8(pages_u8, scales):
+    vals = pages_u8.view(torch.float8_e4m3fn).float() * scales.view(1, -1, 1, 1)
+    return vals.to(torch.bfloat16)
+
+
+def pin_prefill_fp8_pow2_is_bf16_prefill(o):
+    # with power-of-two scales every prefix value is a bf16 number: the FP8 prefill must equal
+    # the bf16 prefill over pages holding those values, bit for bit (also with a window)
+    p, c = _fp8_prefill_case(True, 41)
+    kb, vb = _bf16_pages_from_fp8(c.k_pages, c.k_scale), _bf16_pages_from_fp8(c.v_pages, c.v_scale)
+    for window in (0, 50):
+        got = o.prefill_fp8(p.q, p.k, p.v, p.cu_seqlens, p.sinks, p.scale, c.k_pages, c.v_pages,
+                            c.k_scale, c.v_scale, c.block_table, c.lens, window=window)
+        want = o.prefill(p.q, p.k, p.v, p.cu_seqlens, p.sinks, p.scale, kb, vb, c.block_table, c.lens,
+                         window=window)
+        assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1]), window
+
+
+def pin_prefill_fp8_sdpa(o):
+    # arbitrary per-head scales: SDPA over [torch-dequantised prefix ; new bf16 keys] with the
+    # bottom-right causal mask and the sink column
+    p, c = _fp8_prefill_case(False, 42)
+    out, lse = o.prefill_fp8(p.q, p.k, p.v, p.cu_seqlens, p.sinks, p.scale, c.k_pages, c.v_pages,
+                             c.k_scale, c.v_scale, c.block_table, c.lens)
+    kd = c.k_pages.view(torch.float8_e4m3fn).double() * c.k_scale.double().view(1, -1, 1, 1)
+    vd = c.v_pages.view(torch.float8_e4m3fn).double() * c.v_scale.double().view(1, -1, 1, 1)
+    cu = p.cu_seqlens.tolist()
+    for i in range(3):
+        P, L = int(c.lens[i]), cu[i + 1] - cu[i]
+        npg = (P + 15) // 16
+        pages = c.block_table[i, :npg].long()
+        kpre = kd[pages].permute(1, 0, 2, 3).reshape(2, npg * 16, 64)[:, :P]
+        vpre = vd[pages].permute(1, 0, 2, 3).reshape(2, npg * 16, 64)[:, :P]
+        kn = p.k[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        vn = p.v[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        k = torch.cat([kpre, kn], 1)
+        v = torch.cat([vpre, vn], 1)
+        q = p.q[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+        pos = P + torch.arange(L)[:, None]
+        mask = torch.where(torch.arange(P + L)[None, :] <= pos, 0.0, -math.inf).double()
+        ref, ref_lse = sdpa_with_sink(q, k, v, p.scale, p.sinks, mask=mask)
+        np.testing.assert_allclose(out[cu[i]:cu[i + 1]], ref.permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], ref_lse.permute(1, 0).numpy(), rtol=0, atol=1e-10)
+
+
 PINS = {
     "decode_sdpa_nosink": lambda o: pin_decode_sdpa(o, False),
     "decode_sdpa_sink": lambda o: pin_decode_sdpa(o, True),
@@ -619,6 +678,8 @@ PINS = {
     "rope_golden": pin_rope_golden,
     "bf16_round": pin_bf16_round,
     "decode_append_rope": pin_decode_append_rope,
+    "prefill_fp8_pow2_is_bf16_prefill": pin_prefill_fp8_pow2_is_bf16_prefill,
+    "prefill_fp8_sdpa": pin_prefill_fp8_sdpa,
 }
 
 
@@ -698,6 +759,17 @@ MUTATIONS = [
     ("bf16 rounding ties away from zero", "double r = ldexp(rint(ldexp(x, -ulp)), ulp);",
      "double r = ldexp(round(ldexp(x, -ulp)), ulp);"),
     ("bf16 rounding keeps 9 bits", "int ulp = e - 8;", "int ulp = e - 9;"),
+    ("fp8 prefill ignores the prefix V scale",
+     "out[d] += wt * (vs * oracle_e4m3_value(vp[j][d]));", "out[d] += wt * oracle_e4m3_value(vp[j][d]);"),
+    ("fp8 prefill takes the V scale for the prefix keys",
+     "dot += bf16_to_double(q[d]) * (ks * oracle_e4m3_value(kp[j][d]));",
+     "dot += bf16_to_double(q[d]) * (vs * oracle_e4m3_value(kp[j][d]));"),
+    ("fp8 prefill drops the sink", "double z = exp(sink - m); /* the denominator",
+     "double z = 0.0; /* the denominator"),
+    ("fp8 prefill sees one new key too many", "const int64_t nn = tl + 1 - n0;",
+     "const int64_t nn = (tl + 2 <= cu_seqlens[i + 1] - cu_seqlens[i] ? tl + 2 : tl + 1) - n0;"),
+    ("fp8 prefill window ignored in the prefix", "const int64_t np = lo < Pi ? Pi - lo : 0;",
+     "const int64_t np = Pi;"),
     ("append writes the next slot",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)((pos + 1) % P));"),
