@@ -8,6 +8,7 @@
 // fixed size instead.  Every GPU that loads this library holds that array until
 // the process exits.
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include <mutex>
 
@@ -23,6 +24,8 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 std::mutex g_mu;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device, looked up once per
@@ -60,10 +63,31 @@ extern "C" int sinkattn_decode_noalloc(const void *q, const void *k_pages, const
     int rc = sinkattn_decode_workspace_size(desc, &need);
     if (rc) return rc;
     if (need > kScratchBytes) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
+    // every argument sinkattn_decode checks is checked here first, so a rejected call
+    // enqueues nothing (not even the status clear below) and leaves *status as it was
+    if (desc->num_seqs > 0) {
+        if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out)
+            return SINKATTN_ERR_INVALID_ARG;
+        if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+            !aligned(block_table, 4) || !aligned(seq_lens, 4) || (sinks && !aligned(sinks, 4)) ||
+            (lse && !aligned(lse, 4)))
+            return SINKATTN_ERR_INVALID_ARG;
+    }
+    if (status && !aligned(status, 4)) return SINKATTN_ERR_INVALID_ARG;
     void *scratch = nullptr;
     rc = scratch_address(&scratch);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (desc->num_seqs == 0) {  // an empty batch: nothing runs, its status is clear
+        if (status) {
+            cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+            if (e != cudaSuccess) {
+                sinkattn::record_cuda_error(e, "status clear");
+                return SINKATTN_ERR_CUDA;
+            }
+        }
+        return SINKATTN_OK;
+    }
     // The status word is the only scratch that must start at zero; everything
     // else the merge reads is written earlier in this call by the split-KV kernel.
     cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
