@@ -1,22 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of paged GQA attention with sinks on GB300.
 
-One JSON line on stdout (rank 0).  The headline workload is the gpt-oss-shape
-decode batch (64 sequences, 64 query / 8 KV heads, head_dim 64, KV lengths
-uniform in [512, 8192], page size 16, shuffled pages): a step is one decode
-pass - the split-KV kernel and the LSE merge - over that batch (the K timed steps
-run as one captured CUDA graph), and `value` is
-KV bytes read per second (every cached K and V byte once).  The prefill side
-of the metric (causal ragged prefill of 4 sequences {4096, 2048, 1024, 512}, the
-K/V append, and chunked prefill of 8 x 512 new tokens over 16384-token paged
-prefixes) and the other decode shapes are measured in the same run and reported
-under "rows".
+One JSON line on stdout (rank 0).  The workload is the long-context mixed batch of
+gpt-oss-shape attention (64 query / 8 KV heads, head_dim 64, page size 16): 256 decode
+sequences with KV lengths log-uniform in [128, 131072] (~10.4 GB of KV) plus 8
+chunked-prefill requests of 512 new tokens over 16384-token paged prefixes.  A timed
+step is one decode pass over the 256 sequences - the split-KV kernel and the LSE merge
+(the K timed steps run as one captured CUDA graph) - and `value` is KV bytes read per
+second (every cached K and V byte once).  The chunked-prefill half of the same batch is
+reported under "prefill" (TFLOP/s), both halves issued on two streams at once under
+"mixed", and the other shapes (gpt-oss decode and prefill, Qwen3-235B decode, FP8
+caches, appends, sliding windows) under "rows", each with the median and spread of
+50 timed repeats.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (attention has no exchange step); value = units of all ranks / max rank time.
-`--impl reference` times the fp64 CPU oracle on the same metric instead.
+`--impl reference` times the fp64 CPU oracle on the same metric and workload instead.
 """
 from __future__ import annotations
 
@@ -36,7 +37,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sink-attn decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of BF16 peak)"
-HEADLINE = "gptoss_decode"
+HEADLINE = "longctx_decode"            # the decode half of the long-context mixed batch
+HEADLINE_CHUNKED = "longctx_chunked"   # its chunked-prefill half
+WORKLOAD = ("long-context mixed batch, gpt-oss shapes (64 q / 8 KV heads, head_dim 64, page 16): "
+            "256 decode sequences with KV lengths log-uniform in [128, 131072] (split-KV + LSE "
+            "merge) plus 8 chunked-prefill requests of 512 new tokens over 16384-token paged "
+            "prefixes; bf16 N(0,1), fp32 sinks N(0,1)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -129,10 +135,9 @@ def gpu_identifier(torch, dev) -> str:
         return str(dev.index or 0)
 
 
-# ----------------------------------------------------------------------------- ours
-def time_loop(torch, fn, steps: int, stream, marks=None):
-    """Run fn() `steps` times between CUDA events on `stream`; returns total ms.
-    `marks`, if given, is a list that fn appends (start, end) event pairs to."""
+# ----------------------------------------------------------------------------- timing
+def time_loop(torch, fn, steps: int, stream):
+    """Run fn() `steps` times between CUDA events on `stream`; returns total ms."""
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
@@ -164,6 +169,73 @@ def time_graph(torch, g, stream) -> float:
     return start.elapsed_time(end)
 
 
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2, so the next timed call finds none of its
+    inputs there."""
+
+    def __init__(self, torch, dev):
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.v = 0
+
+    def __call__(self):
+        self.v = (self.v + 1) & 0xFF
+        self.buf.fill_(self.v)
+
+
+def repeat_stats(torch, fn, stream, reps: int = 50, calls: int = 10, flush=None) -> dict:
+    """Per-call time over `reps` timed repeats: median, 10th and 90th percentile (ms).
+    Without `flush` (inputs larger than L2) a repeat is one replay of a CUDA graph of
+    `calls` calls between CUDA events.  With it (inputs that fit in L2), a repeat replays a
+    graph of `calls` x (write a buffer larger than L2, call) and then a graph of the same
+    writes alone, and the difference divided by `calls` is the sample: each call starts
+    with its inputs out of L2, and short calls are charged the gap between two launches in
+    a graph, not the latency of launching a graph."""
+    if flush is None:
+        g = capture_steps(torch, fn, calls)
+        g.replay()  # the first replay uploads the graph
+        torch.cuda.synchronize()
+        marks = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            marks.append((a, b))
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) / calls for a, b in marks)
+    else:
+        def both():
+            flush()
+            fn()
+        g = capture_steps(torch, both, calls)
+        g0 = capture_steps(torch, flush, calls)
+        g.replay()
+        g0.replay()
+        torch.cuda.synchronize()
+        marks = []
+        for _ in range(reps):
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            g0.replay()
+            c.record(stream)
+            marks.append((a, b, c))
+        torch.cuda.synchronize()
+        t = sorted((a.elapsed_time(b) - b.elapsed_time(c)) / calls for a, b, c in marks)
+
+    def pct(f):
+        return t[min(len(t) - 1, int(round(f * (len(t) - 1))))]
+
+    return {"median_ms": round(statistics.median(t), 5), "p10_ms": round(pct(0.1), 5),
+            "p90_ms": round(pct(0.9), 5), "repeats": reps, "calls_per_repeat": calls,
+            "l2": ("each call preceded by a 256 MB write (graph of write + call minus graph of "
+                   "the writes alone)") if flush is not None else "inputs larger than L2"}
+
+
 def reduce_step_time(dist, ms: float, device) -> float:
     """The slowest rank's timed region, in ms, on every rank (all-reduce MAX); the
     value itself when there is a single process (dist is None)."""
@@ -181,8 +253,25 @@ def whole_job_value(units_per_rank: float, world: int, ms_per_step: float) -> fl
     return world * units_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
+def decode_device_args(w, dev):
+    c = w.cache
+    return dict(q=w.q.to(dev), kp=c.k_pages.to(dev), vp=c.v_pages.to(dev),
+                bt=c.block_table.to(dev), sl=c.lens.to(dev),
+                sk=None if w.sinks is None else w.sinks.to(dev))
+
+
+def prefill_device_args(p, dev):
+    kw = {}
+    if p.prefix is not None:
+        kw = dict(k_pages=p.prefix.k_pages.to(dev), v_pages=p.prefix.v_pages.to(dev),
+                  prefix_block_table=p.prefix.block_table.to(dev), prefix_lens=p.prefix.lens.to(dev))
+    args = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev),
+            None if p.sinks is None else p.sinks.to(dev), p.scale)
+    return args, kw
+
+
+# ----------------------------------------------------------------------------- ours
 def run_ours(args, rank, world, local_rank):
-    import numpy as np
     import torch
     from paged_gqa_attention_head_gb300 import build as libbuild, inputs, sinkattn as sa
 
@@ -196,18 +285,21 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    # ---- headline: decode of the gpt-oss-shape batch
+    # ---- headline: the decode half of the long-context mixed batch (256 sequences)
     w = inputs.make_workload(HEADLINE, seed=0)
     c = w.cache
-    d = dict(q=w.q.to(dev), kp=c.k_pages.to(dev), vp=c.v_pages.to(dev),
-             bt=c.block_table.to(dev), sl=c.lens.to(dev), sk=w.sinks.to(dev))
+    B = w.q.shape[0]
+    d = decode_device_args(w, dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
     kv_bytes = w.kv_bytes()
+    ws_dec = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        B, w.num_qo_heads, w.num_kv_heads, w.head_dim, c.num_pages, c.block_table.shape[1])),
+        dtype=torch.uint8, device=dev)
 
     def step():  # one decode pass: the split-KV kernel, then the LSE merge
         _, _, ws, desc = sa.decode_splitkv(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"],
-                                           w.scale, out=out, lse=lse)
+                                           w.scale, out=out, lse=lse, workspace_buf=ws_dec)
         sa.decode_merge(d["sl"], d["sk"], out, lse, desc, ws)
 
     gid = gpu_identifier(torch, dev)
@@ -220,10 +312,10 @@ def run_ours(args, rank, world, local_rank):
     t_end = time.time() + 1.0
     nwarm = max(3, args.warmup)
     while time.time() < t_end:
-        for _ in range(50):
+        for _ in range(10):
             step()
         torch.cuda.synchronize()
-        nwarm += 50
+        nwarm += 10
     # the timed region: a CUDA graph of K captured decode steps, replayed once (how a
     # serving loop issues its decode step; the work per step is the same as a direct call)
     graph = capture_steps(torch, step, args.steps)
@@ -236,25 +328,101 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     t_load1 = time.time()
     clocks = sampler.stop(t_load0, t_load1)
+    del graph
+
     # the split-KV kernel on its own, for the roofline: a graph of K launches of it alone,
     # between CUDA events on the launching stream
     def split_only():
         sa.decode_splitkv(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"], w.scale, out=out,
-                          lse=lse)
+                          lse=lse, workspace_buf=ws_dec)
 
     kgraph = capture_steps(torch, split_only, args.steps)
     time_graph(torch, kgraph, stream)
     split_ms = time_graph(torch, kgraph, stream) / args.steps
+    del kgraph
     ms = reduce_step_time(dist, ms, dev)
     ms_step = ms / args.steps
     value = whole_job_value(kv_bytes, world, ms_step)
     ach = kv_bytes / (split_ms * 1e-3) / 1e9
-    assert sa.get_status(sa.workspace(0, dev)) == 0, "device status reported a problem"
+    assert sa.get_status(ws_dec) == 0, "device status reported a problem"
+    step_stats = repeat_stats(torch, step, stream)
 
     # ---- e2e: the same decode through the C ABI with host buffers copied every step
-    # A step's inputs sit in one pinned staging buffer (q, block table, lengths, sinks at
-    # 256-byte aligned offsets) and go over in one copy; out and lse are views of one device
-    # buffer and come back in one copy.  Two slots of each: step k uses slot k % 2.
+    e2e = e2e_decode(torch, sa, d, w, dev, stream, dist, args.steps, kv_bytes, world)
+
+    # ---- the prefill half of the same batch: 8 chunked-prefill requests over paged prefixes
+    wp = inputs.make_workload(HEADLINE_CHUNKED, seed=0)
+    pargs, pkw = prefill_device_args(wp, dev)
+    pout = torch.empty_like(pargs[0])
+    plse = torch.empty(pargs[0].shape[:2], dtype=torch.float32, device=dev)
+    pws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    fp = lambda: sa.prefill(*pargs, **pkw, out=pout, lse=plse, workspace_buf=pws)  # noqa: E731
+    for _ in range(3):
+        fp()
+    pstats = repeat_stats(torch, fp, stream)
+    assert sa.get_status(pws) == 0, "device status reported a problem (chunked prefill)"
+    pflops = wp.flops()
+    ptf = pflops / (pstats["median_ms"] * 1e-3) / 1e12
+    prefill = {"workload": "8 chunked-prefill requests x 512 new tokens over 16384-token paged "
+                           "prefixes, 64 q / 8 KV heads, head_dim 64",
+               "kernel": "prefill_kernel", "ms": pstats["median_ms"], "TFLOP/s": round(ptf, 1),
+               "frac_bf16": round(ptf / pk["bf16_tflops"], 4), "flops": pflops,
+               "peak": pk["bf16_tflops"], "peak_source": f"{peak_src} bf16_tflops (burst)",
+               "traffic": traffic_for("prefill_kernel", HEADLINE_CHUNKED), **pstats}
+
+    # ---- both halves of the step on two streams at once
+    mixed = mixed_row(torch, sa, dev, stream, pk, d, w, ws_dec, out, lse, pargs, pkw, pout, plse,
+                      pws, kv_bytes, pflops)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": nwarm,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
+        "config": {"workload": WORKLOAD, "step": "the decode half: split-KV + LSE merge over the "
+                   "256 sequences (the chunked-prefill half is `prefill`, both halves on two "
+                   "streams are `mixed`)",
+                   "global_batch": B * world, "kv_tokens": int(c.lens.sum()), "kv_bytes": kv_bytes,
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 "
+                   f"({kv_bytes / 1e9:.1f} GB of KV per step vs 129 MB L2)"},
+        "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "launch": f"one CUDA graph of {args.steps} captured decode steps (split-KV + merge each), "
+                  "replayed once",
+        "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": round(ach, 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": traffic_for("decode_splitkv_kernel", HEADLINE),
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "kernel_ms": round(split_ms, 5)},
+        "step_repeats": step_stats,
+        "prefill": prefill,
+        "mixed": mixed,
+        "clocks": clocks,
+    }
+    del pargs, pkw, pout, plse
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, each timed on its own
+    if not args.no_rows:
+        result["rows"] = measure_rows(torch, sa, inputs, dev, stream, pk, peak_src)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def e2e_decode(torch, sa, d, w, dev, stream, dist, steps, kv_bytes, world):
+    """The decode through the public call with host buffers: every step copies q, the block
+    table, the lengths and the sinks in from pinned host memory (one copy) and reads out + lse
+    back into pinned host memory (one copy).  Step k+1's copy in and step k's copy out run on
+    two copy streams while step k decodes (two buffer slots, as a serving loop keeps them)."""
+    out_like = torch.empty_like(d["q"])
+    lse_like = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
     names = ("q", "bt", "sl", "sk")
     offs, n_in = {}, 0
     for k in names:
@@ -265,8 +433,8 @@ def run_ours(args, rank, world, local_rank):
         nb = like.numel() * like.element_size()
         return buf[offs[k]:offs[k] + nb].view(like.dtype).view(like.shape)
 
-    n_out = out.numel() * 2
-    n_res = n_out + lse.numel() * 4
+    n_out = out_like.numel() * 2
+    n_res = n_out + lse_like.numel() * 4
     host_in = [torch.empty(n_in, dtype=torch.uint8).pin_memory() for _ in range(2)]
     dev_in_buf = [torch.empty(n_in, dtype=torch.uint8, device=dev) for _ in range(2)]
     for hb in host_in:
@@ -274,13 +442,16 @@ def run_ours(args, rank, world, local_rank):
             view(hb, k, d[k]).copy_(d[k].cpu())
     dev_in = [{k: view(b, k, d[k]) for k in names} for b in dev_in_buf]
     dev_res = [torch.empty(n_res, dtype=torch.uint8, device=dev) for _ in range(2)]
-    out_v = [r[:n_out].view(torch.bfloat16).view(out.shape) for r in dev_res]
-    lse_v = [r[n_out:].view(torch.float32).view(lse.shape) for r in dev_res]
+    out_v = [r[:n_out].view(torch.bfloat16).view(out_like.shape) for r in dev_res]
+    lse_v = [r[n_out:].view(torch.float32).view(lse_like.shape) for r in dev_res]
     host_res = [torch.empty(n_res, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        d["q"].shape[0], d["q"].shape[1], d["kp"].shape[1], d["q"].shape[2], d["kp"].shape[0],
+        d["bt"].shape[1])), dtype=torch.uint8, device=dev)
 
     def decode_slot(s):
         sa.decode(dev_in[s]["q"], d["kp"], d["vp"], dev_in[s]["bt"], dev_in[s]["sl"], dev_in[s]["sk"],
-                  w.scale, out=out_v[s], lse=lse_v[s])
+                  w.scale, out=out_v[s], lse=lse_v[s], workspace_buf=ws)
 
     def e2e_serial(n):
         # copy in, decode, copy out, one after the other on the current stream
@@ -295,9 +466,6 @@ def run_ours(args, rank, world, local_rank):
     ev_back = [torch.cuda.Event() for _ in range(2)]  # the slot's result is on the host
 
     def e2e_pipelined(n):
-        # step k + 1's inputs go over on one copy stream while step k decodes on the current
-        # stream, and step k's result comes back on another; a slot is reused two steps later,
-        # once its decode (for the inputs) and its copy back (for the result) are done
         main = torch.cuda.current_stream(dev)
         h2d_stream.wait_stream(main)
         d2h_stream.wait_stream(main)
@@ -333,84 +501,47 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    # issued call by call from Python (host launch work included), then as one CUDA graph of
-    # the K steps (how a serving loop issues them; each replayed step still copies its inputs
-    # in and its results out)
-    e2e_direct_ms = reduce_step_time(dist, time_loop(torch, lambda: e2e_pipelined(args.steps), 1,
-                                                     stream), dev) / args.steps
-    egraph = capture_steps(torch, lambda: e2e_pipelined(args.steps), 1)
-    sgraph = capture_steps(torch, lambda: e2e_serial(args.steps), 1)
+    e2e_direct_ms = reduce_step_time(dist, time_loop(torch, lambda: e2e_pipelined(steps), 1,
+                                                     stream), dev) / steps
+    egraph = capture_steps(torch, lambda: e2e_pipelined(steps), 1)
+    sgraph = capture_steps(torch, lambda: e2e_serial(steps), 1)
     time_graph(torch, egraph, stream)
     time_graph(torch, sgraph, stream)
     if dist:
         dist.barrier()
-    e2e_ms = reduce_step_time(dist, time_graph(torch, egraph, stream), dev) / args.steps
+    e2e_ms = reduce_step_time(dist, time_graph(torch, egraph, stream), dev) / steps
     if dist:
         dist.barrier()
-    e2e_serial_ms = reduce_step_time(dist, time_graph(torch, sgraph, stream), dev) / args.steps
-    h2d = n_in
-    d2h = n_res
+    e2e_serial_ms = reduce_step_time(dist, time_graph(torch, sgraph, stream), dev) / steps
     torch.cuda.synchronize()
-    ref_out, _ = sa.decode(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"], w.scale)
+    ref_out, _ = sa.decode(d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"], w.scale,
+                           workspace_buf=ws)
     ref_host = ref_out.cpu()
     for s in range(2):  # both slots hold a replayed step's result
-        assert torch.equal(host_res[s][:n_out].view(torch.bfloat16).view(out.shape), ref_host), \
+        assert torch.equal(host_res[s][:n_out].view(torch.bfloat16).view(out_like.shape), ref_host), \
             "end-to-end decode differs from the device-resident one"
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": nwarm,
-        "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16, shuffled pages)",
-        "config": {"workload": "gpt-oss-shape decode: B=64, 64 q / 8 KV heads, head_dim 64, "
-                               "page 16, KV len ~ U[512, 8192], fp32 sinks",
-                   "global_batch": 64 * world, "kv_tokens": int(c.lens.sum()), "kv_bytes": kv_bytes,
-                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 "
-                   f"({kv_bytes / 1e6:.0f} MB of KV per step vs 129 MB L2)"},
-        "tokens_per_s": round(world * 64 / (ms_step * 1e-3), 1),
-        "e2e": {"value": round(whole_job_value(kv_bytes, world, e2e_ms), 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "note": "every step copies q, block table, lengths and sinks in from a pinned "
-                        "host buffer (one copy), runs the decode and reads out + lse back into "
-                        "pinned host memory (one copy); step k+1's copy in and step k's copy out "
-                        "run on two copy streams while step k decodes (two buffer slots); the K "
-                        "steps run as one captured CUDA graph; the KV cache is resident state",
-                "serial": {"value": round(whole_job_value(kv_bytes, world, e2e_serial_ms), 2),
-                           "ms_per_step": round(e2e_serial_ms, 5),
-                           "note": "copy in, decode, copy out one after the other on one stream"},
-                "direct_calls": {"value": round(whole_job_value(kv_bytes, world, e2e_direct_ms), 2),
-                                 "ms_per_step": round(e2e_direct_ms, 5),
-                                 "note": "the pipelined steps issued call by call from Python"}},
-        "gpu_launches": 2 * args.steps,
-        "launch": f"one CUDA graph of {args.steps} captured decode steps (split-KV + merge each), "
-                  "replayed once",
-        "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel", "achieved": round(ach, 1),
-                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                     "peak_source": f"{peak_src} hbm_gbs",
-                     "traffic": traffic_for("decode_splitkv_kernel", HEADLINE),
-                     "algorithmic_bytes_per_launch": kv_bytes,
-                     "kernel_ms": round(split_ms, 5)},
-        "clocks": clocks,
-    }
-
-    # ---- the other rows, each timed on its own (not part of the headline step)
-    if not args.no_rows:
-        result["rows"] = measure_rows(torch, sa, inputs, dev, stream, pk, peak_src)
-
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w)
-    if dist:
-        dist.destroy_process_group()
-    return result
+    del egraph, sgraph
+    return {"value": round(whole_job_value(kv_bytes, world, e2e_ms), 2), "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": n_in,
+            "d2h_bytes_per_step": n_res,
+            "note": "every step copies q, block table, lengths and sinks in from a pinned host "
+                    "buffer (one copy), runs the decode and reads out + lse back into pinned host "
+                    "memory (one copy); step k+1's copy in and step k's copy out run on two copy "
+                    "streams while step k decodes (two buffer slots); the K steps run as one "
+                    "captured CUDA graph; the KV cache is resident state",
+            "serial": {"value": round(whole_job_value(kv_bytes, world, e2e_serial_ms), 2),
+                       "ms_per_step": round(e2e_serial_ms, 5),
+                       "note": "copy in, decode, copy out one after the other on one stream"},
+            "direct_calls": {"value": round(whole_job_value(kv_bytes, world, e2e_direct_ms), 2),
+                             "ms_per_step": round(e2e_direct_ms, 5),
+                             "note": "the pipelined steps issued call by call from Python"}}
 
 
 def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     rows = {}
-    reps = 20
+    flush = L2Flush(torch, dev)
 
-    def decode_row(name, window=0, graph=False):
+    def decode_row(name, window=0, kernel_ms=False):
         w = inputs.make_workload(name, seed=0)
         c = w.cache
         q, sinks = w.q.to(dev), None if w.sinks is None else w.sinks.to(dev)
@@ -426,34 +557,36 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
             f = lambda: sa.decode(*args, out=out, lse=lse, window=window)  # noqa: E731
         for _ in range(3):
             f()
-        if window or graph:
-            # short GPU work: time a CUDA graph of the calls, not the host's launches
-            g = capture_steps(torch, f, reps)
-            time_graph(torch, g, stream)
-            ms = time_graph(torch, g, stream) / reps
-        else:
-            ms = time_loop(torch, f, reps, stream) / reps
         nbytes = w.kv_bytes(window)
+        st = repeat_stats(torch, f, stream, flush=flush if nbytes < L2_FLUSH_BYTES else None)
+        ms = st["median_ms"]
         gbs = nbytes / (ms * 1e-3) / 1e9
-        r = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
-             "kv_bytes": nbytes, "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1)}
+        r = {"ms": ms, "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+             "kv_bytes": nbytes, "tokens_per_s": round(w.q.shape[0] / (ms * 1e-3), 1), **st}
+        if kernel_ms:  # the split-KV kernel alone (graph of 20 launches)
+            g = lambda: sa.decode_splitkv(*args, out=out, lse=lse, window=window)  # noqa: E731
+            kg = capture_steps(torch, g, 20)
+            time_graph(torch, kg, stream)
+            kms = time_graph(torch, kg, stream) / 20
+            r["splitkv_kernel_ms"] = round(kms, 5)
+            r["splitkv_frac_hbm"] = round(nbytes / (kms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
+            r["traffic"] = traffic_for("decode_splitkv_kernel", name)
+            del kg
         if window:
             r["window"] = window
-        if window or graph:
-            r["launch"] = f"CUDA graph of {reps} calls"
         if c.fp8:
             r["kv_dtype"] = "fp8 e4m3 (per-KV-head scales)"
         del args, out, lse, w, q, sinks
         torch.cuda.empty_cache()
         return r
 
-    for name in ("qwen3_decode", "longctx_decode"):
-        rows[name] = decode_row(name)
+    rows["gptoss_decode"] = decode_row("gptoss_decode", kernel_ms=True)
+    rows["qwen3_decode"] = decode_row("qwen3_decode")
 
     # decode step with its K/V append: one call (the new rows written by the decode kernel)
-    # against two (the append kernel, then the decode); each a CUDA graph of `reps` steps
-    # over the same cache (every step rewrites the same slots with the same rows)
-    w = inputs.make_workload(HEADLINE, seed=0)
+    # against two (the append kernel, then the decode) over the same cache (every step
+    # rewrites the same slots with the same rows)
+    w = inputs.make_workload("gptoss_decode", seed=0)
     c = w.cache
     q, sinks = w.q.to(dev), w.sinks.to(dev)
     kp, vp, bt, sl = c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev)
@@ -474,24 +607,21 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     for key, f in (("fused", fused), ("append_then_decode", two_calls)):
         for _ in range(3):
             f()
-        g = capture_steps(torch, f, reps)
-        time_graph(torch, g, stream)
-        da[key] = time_graph(torch, g, stream) / reps
+        da[key] = repeat_stats(torch, f, stream)
     nbytes = w.kv_bytes()
+    ms = da["fused"]["median_ms"]
     rows["gptoss_decode_append"] = {
-        "ms": round(da["fused"], 5), "GB/s": round(nbytes / (da["fused"] * 1e-3) / 1e9, 1),
-        "frac_hbm": round(nbytes / (da["fused"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-        "append_then_decode_ms": round(da["append_then_decode"], 5), "kv_bytes": nbytes,
-        "launch": f"CUDA graph of {reps} steps (fused: split-KV with append + merge; two calls: "
-                  "append, split-KV, merge)"}
+        "ms": ms, "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+        "append_then_decode_ms": da["append_then_decode"]["median_ms"], "kv_bytes": nbytes,
+        **da["fused"], "append_then_decode": da["append_then_decode"]}
     del w, c, q, sinks, kp, vp, bt, sl, k_new, v_new, out, lse
     torch.cuda.empty_cache()
     # a gpt-oss sliding-window layer (128 positions): the last 128 keys of each sequence,
-    # ~9 MB of KV, so the launch and the first copies dominate
-    rows["gptoss_decode_window128"] = decode_row(HEADLINE, window=128)
+    # ~17 MB of KV, so the launch and the first copies dominate
+    rows["gptoss_decode_window128"] = decode_row("gptoss_decode", window=128)
     # the decode shapes over an FP8 E4M3 cache (half the KV bytes per token)
-    rows["gptoss_decode_fp8"] = decode_row("gptoss_decode_fp8", graph=True)
-    for name in ("qwen3_decode_fp8", "longctx_decode_fp8"):
+    for name in ("gptoss_decode_fp8", "qwen3_decode_fp8", "longctx_decode_fp8"):
         rows[name] = decode_row(name)
 
     # append of the prefill workload's K/V into HND pages
@@ -502,10 +632,12 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     f = lambda: sa.append_kv(*aargs)  # noqa: E731
     for _ in range(3):
         f()
-    ms = time_loop(torch, f, reps, stream) / reps
+    st = repeat_stats(torch, f, stream, flush=flush)
     moved = 2 * 2 * a.k.numel() * 2  # read k, v and write them
-    rows["gptoss_append"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
-                             "bytes": moved}
+    rows["gptoss_append"] = {"ms": st["median_ms"],
+                             "GB/s": round(moved / (st["median_ms"] * 1e-3) / 1e9, 1),
+                             "frac_hbm": round(moved / (st["median_ms"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                             "bytes": moved, **st}
     # the same append into an FP8 cache (quantising: read bf16, write one byte per element)
     a8 = inputs.make_append([4096, 2048, 1024, 512], [0, 0, 0, 0], 8, 64, seed=0, kv_dtype="fp8")
     c8 = a8.cache
@@ -515,74 +647,68 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
     f = lambda: sa.append_kv_fp8(*a8args)  # noqa: E731
     for _ in range(3):
         f()
-    ms = time_loop(torch, f, reps, stream) / reps
+    st = repeat_stats(torch, f, stream, flush=flush)
     moved = 2 * a8.k.numel() * (2 + 1)  # read k, v (bf16) and write their codes
-    rows["gptoss_append_fp8"] = {"ms": round(ms, 5), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1),
-                                 "bytes": moved}
+    rows["gptoss_append_fp8"] = {"ms": st["median_ms"],
+                                 "GB/s": round(moved / (st["median_ms"] * 1e-3) / 1e9, 1),
+                                 "bytes": moved, **st}
     del aargs, a8args
 
-    for name, window in (("gptoss_prefill", 0), ("longctx_chunked", 0), ("gptoss_prefill", 128)):
+    for name, window in (("gptoss_prefill", 0), ("gptoss_prefill", 128)):
         p = inputs.make_workload(name, seed=0)
         key = name if not window else f"{name}_window{window}"
-        kw = {}
-        if p.prefix is not None:
-            kw = dict(k_pages=p.prefix.k_pages.to(dev), v_pages=p.prefix.v_pages.to(dev),
-                      prefix_block_table=p.prefix.block_table.to(dev),
-                      prefix_lens=p.prefix.lens.to(dev))
-        pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+        pargs, kw = prefill_device_args(p, dev)
         kw["window"] = window
-        try:
-            sa.prefill(*pargs, **kw)
-        except sa.SinkAttnError as e:
-            rows[key] = {"unavailable": str(e)}
-            continue
         f = lambda: sa.prefill(*pargs, **kw)  # noqa: E731
         for _ in range(3):
             f()
-        ms = time_loop(torch, f, reps, stream) / reps
+        st = repeat_stats(torch, f, stream, flush=flush)
+        ms = st["median_ms"]
         flops = p.flops(window)
         tf = flops / (ms * 1e-3) / 1e12
-        rows[key] = {"ms": round(ms, 5), "TFLOP/s": round(tf, 1),
+        rows[key] = {"ms": ms, "TFLOP/s": round(tf, 1),
                      "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": flops,
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "traffic": None if window else traffic_for("prefill_kernel", name)}
+                     "traffic": None if window else traffic_for("prefill_kernel", name), **st}
         if window:
             rows[key]["window"] = window
-    rows["longctx_mixed"] = mixed_row(torch, sa, inputs, dev, stream, pk, reps)
+    # the long-context chunked prefill over an FP8 E4M3 prefix cache (the same FLOP)
+    p = inputs.make_workload("longctx_chunked_fp8", seed=0)
+    c = p.prefix
+    pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale,
+             c.k_pages.to(dev), c.v_pages.to(dev), c.k_scale.to(dev), c.v_scale.to(dev),
+             c.block_table.to(dev), c.lens.to(dev))
+    f = lambda: sa.prefill_fp8(*pargs)  # noqa: E731
+    for _ in range(3):
+        f()
+    st = repeat_stats(torch, f, stream)
+    flops = p.flops()
+    tf = flops / (st["median_ms"] * 1e-3) / 1e12
+    rows["longctx_chunked_fp8"] = {"ms": st["median_ms"], "TFLOP/s": round(tf, 1),
+                                   "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": flops,
+                                   "peak_source": f"{peak_src} bf16_tflops (burst)",
+                                   "prefix_dtype": "fp8 e4m3 (per-KV-head scales)", **st}
+    del pargs
+    torch.cuda.empty_cache()
     return rows
 
 
-def mixed_row(torch, sa, inputs, dev, stream, pk, reps):
+def mixed_row(torch, sa, dev, stream, pk, d, w, dws, dout, dlse, pargs, pkw, pout, plse, pws,
+              nbytes, flops):
     """The long-context mixed batch: the 256-sequence decode and the 8 chunked-prefill
     requests of one step issued on two streams at once, against the same two calls one
     after the other and the lower bound max(KV bytes / HBM peak, FLOP / bf16 peak)."""
-    wd = inputs.make_workload("longctx_decode", seed=0)
-    c = wd.cache
-    q = wd.q.to(dev)
-    dargs = (q, c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
-             wd.sinks.to(dev), wd.scale)
-    dout, dlse = torch.empty_like(q), torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-    dws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
-        q.shape[0], q.shape[1], c.k_pages.shape[1], q.shape[2], c.k_pages.shape[0],
-        c.block_table.shape[1])), dtype=torch.uint8, device=dev)
-    wp = inputs.make_workload("longctx_chunked", seed=0)
-    pre = wp.prefix
-    pargs = (wp.q.to(dev), wp.k.to(dev), wp.v.to(dev), wp.cu_seqlens.to(dev), wp.sinks.to(dev),
-             wp.scale)
-    pkw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
-               prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
-    pout = torch.empty_like(pargs[0])
-    plse = torch.empty(pargs[0].shape[:2], dtype=torch.float32, device=dev)
-    pws = torch.zeros(max(256, sa.prefill_workspace_size(sa.paged_desc(
-        wp.cu_seqlens.shape[0] - 1, wp.q.shape[1], wp.k.shape[1], wp.q.shape[2],
-        pre.k_pages.shape[0], pre.block_table.shape[1]))), dtype=torch.uint8, device=dev)
+    dargs = (d["q"], d["kp"], d["vp"], d["bt"], d["sl"], d["sk"], w.scale)
     fd = lambda: sa.decode(*dargs, out=dout, lse=dlse, workspace_buf=dws)  # noqa: E731
     fp = lambda: sa.prefill(*pargs, **pkw, out=pout, lse=plse, workspace_buf=pws)  # noqa: E731
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def both():
+        # fork from and join back into the stream current at call time (the capturing
+        # stream while a CUDA graph of these calls is recorded)
+        main = torch.cuda.current_stream(dev)
         ev = torch.cuda.Event()
-        ev.record(stream)
+        ev.record(main)
         s1.wait_event(ev)
         s2.wait_event(ev)
         with torch.cuda.stream(s1):
@@ -592,59 +718,25 @@ def mixed_row(torch, sa, inputs, dev, stream, pk, reps):
         e1, e2 = torch.cuda.Event(), torch.cuda.Event()
         e1.record(s1)
         e2.record(s2)
-        stream.wait_event(e1)
-        stream.wait_event(e2)
-
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-
-    def split(sp):
-        # the SMs shared out: prefill's persistent grid on sp SMs, issued first so its CTAs
-        # (one per SM) claim them, the decode grid on the other sms - sp
-        def f():
-            ev = torch.cuda.Event()
-            ev.record(stream)
-            s1.wait_event(ev)
-            s2.wait_event(ev)
-            with torch.cuda.stream(s2):
-                sa.prefill(*pargs, **pkw, out=pout, lse=plse, workspace_buf=pws, max_sms=sp)
-            with torch.cuda.stream(s1):
-                sa.decode(*dargs, out=dout, lse=dlse, workspace_buf=dws, max_sms=sms - sp)
-            e1, e2 = torch.cuda.Event(), torch.cuda.Event()
-            e1.record(s1)
-            e2.record(s2)
-            stream.wait_event(e1)
-            stream.wait_event(e2)
-        return f
+        main.wait_event(e1)
+        main.wait_event(e2)
 
     for f in (fd, fp, both):
         for _ in range(3):
             f()
+    reps = 20
     ms_d = time_loop(torch, fd, reps, stream) / reps
     ms_p = time_loop(torch, fp, reps, stream) / reps
-    ms_both = time_loop(torch, both, reps, stream) / reps
-    tried = {}
-    for sp in (sms * 9 // 16, sms * 5 // 8, sms * 11 // 16, sms * 3 // 4):
-        f = split(sp)
-        for _ in range(2):
-            f()
-        tried[sp] = time_loop(torch, f, reps, stream) / reps
-    sp_best = min(tried, key=tried.get)
-    ms_split = tried[sp_best]
-    nbytes, flops = wd.kv_bytes(), wp.flops()
+    st = repeat_stats(torch, both, stream, reps=30, calls=5)
+    ms_both = st["median_ms"]
+    eager_ms = time_loop(torch, both, reps, stream) / reps
     bound = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12)) * 1e3
-    best = min(ms_both, ms_split)
-    r = {"ms": round(best, 5), "decode_ms": round(ms_d, 5), "chunked_ms": round(ms_p, 5),
-         "sequential_ms": round(ms_d + ms_p, 5), "two_streams_whole_gpu_ms": round(ms_both, 5),
-         "sm_split": {"prefill_sms": sp_best, "decode_sms": sms - sp_best,
-                      "ms": round(ms_split, 5),
-                      "tried_ms": {f"{k}/{sms - k}": round(v, 5) for k, v in tried.items()}},
-         "lower_bound_ms": round(bound, 5), "frac_of_bound": round(bound / best, 4),
-         "kv_bytes": nbytes, "flops": flops,
-         "launch": "decode (split-KV + merge) and chunked prefill on two streams; "
-                   "whole-GPU grids, and grids sharing out the SMs (desc.max_sms)"}
-    del dargs, pargs, pkw, dws, pws
-    torch.cuda.empty_cache()
-    return r
+    return {"ms": ms_both, "decode_ms": round(ms_d, 5), "chunked_ms": round(ms_p, 5),
+            "sequential_ms": round(ms_d + ms_p, 5), "lower_bound_ms": round(bound, 5),
+            "frac_of_bound": round(bound / ms_both, 4), "eager_ms": round(eager_ms, 5),
+            "kv_bytes": nbytes, "flops": flops,
+            "launch": "decode (split-KV + merge) and chunked prefill on two streams, whole-GPU "
+                      "grids", **st}
 
 
 def _omp_threads(n: int):
@@ -671,41 +763,78 @@ def _cpu_model() -> str:
     return platform.machine()
 
 
-def cpu_baseline(w, budget_s: float = 12.0):
-    """The fp64 oracle on the host cores over the same decode batch, repeated
-    until about `budget_s` seconds of work; then once on a single core."""
-    import oracle
+def _sample_seqs(w, target_bytes: float) -> int:
+    """Smallest n such that the first n sequences of the batch hold >= target_bytes of KV
+    (at least 1, at most the whole batch)."""
+    per_tok = 2 * w.num_kv_heads * w.head_dim * 2
+    cum = 0
+    lens = [int(x) for x in w.cache.lens]
+    for n, L in enumerate(lens, 1):
+        cum += L * per_tok
+        if cum >= target_bytes:
+            return n
+    return len(lens)
+
+
+def _oracle_pass(oracle, w, nseq: int):
+    """One oracle decode of the first nseq sequences (all heads); returns (seconds, bytes)."""
+    import numpy as np
     c = w.cache
-    oracle.build()
+    B, Hq = w.q.shape[:2]
+    sel = np.zeros((B, Hq), dtype=bool)
+    sel[:nseq] = True
+    nbytes = int(c.lens[:nseq].long().sum()) * 2 * w.num_kv_heads * w.head_dim * 2
     t0 = time.perf_counter()
-    oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
-    one = time.perf_counter() - t0
-    reps = max(1, min(500, int(budget_s / max(one, 1e-3))))
+    oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, select=sel)
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The fp64 oracle on the host cores over a bounded sample of the same decode batch
+    (its first sequences, all heads) repeated for about `budget_s` seconds; then one pass
+    of a smaller sample on a single core."""
+    import oracle
+    oracle.build()
+    B = w.q.shape[0]
+    t, nb = _oracle_pass(oracle, w, min(B, 8))  # probe: the host's rate
+    rate = nb / max(t, 1e-6)
+    nseq = _sample_seqs(w, rate * 2.0)
+    one, nb = _oracle_pass(oracle, w, nseq)
+    reps = max(1, min(200, int(budget_s / max(one, 1e-3))))
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
+        _oracle_pass(oracle, w, nseq)
     el = time.perf_counter() - t0
-    r = {"value": round(reps * w.kv_bytes() / el / 1e9, 3), "unit": "GB/s",
+    r = {"value": round(reps * nb / el / 1e9, 3), "unit": "GB/s",
          "cores": oracle.max_threads(), "kind": "oracle", "cpu": _cpu_model(),
-         "sample": f"the whole decode batch (64 sequences x 64 heads) x {reps} repetitions, "
-                   f"{el:.1f} s"}
-    # one pass on a single core; a runtime that cannot be switched leaves the entry out
+         "sample": f"the first {nseq} of the {B} decode sequences (all 64 heads, "
+                   f"{nb / 1e9:.2f} GB of KV) x {reps} repetitions, {el:.1f} s"}
+    # one pass on a single core: the OpenMP thread count set to 1 for that pass and restored
+    reason = None
+    old = None
     try:
         old = _omp_threads(1)
-    except Exception:  # noqa: BLE001 - the baseline above stands without it
-        old = None
+    except Exception as e:  # noqa: BLE001 - the baseline above stands without it
+        reason = f"setting the OpenMP thread count failed: {type(e).__name__}: {e}"
+    if old is None and reason is None:
+        reason = "libgomp.so.1 could not be loaded to set the OpenMP thread count"
     if old is not None:
         try:
-            t0 = time.perf_counter()
-            oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
-            el1 = time.perf_counter() - t0
-            if oracle.max_threads() == 1:
-                r["one_core"] = {"value": round(w.kv_bytes() / el1 / 1e9, 3), "unit": "GB/s",
-                                 "cores": 1, "sample": f"the whole decode batch once, {el1:.1f} s"}
-        except Exception:  # noqa: BLE001 - the baseline above stands without it
-            pass
+            if oracle.max_threads() != 1:
+                reason = ("the oracle's OpenMP runtime is not the libgomp.so.1 this process "
+                          f"loaded (its thread count stayed {oracle.max_threads()})")
+            else:
+                n1 = _sample_seqs(w, rate / max(1, old) * 3.0)
+                el1, nb1 = _oracle_pass(oracle, w, n1)
+                r["one_core"] = {"value": round(nb1 / el1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                                 "sample": f"the first {n1} sequences once ({nb1 / 1e9:.2f} GB of "
+                                           f"KV), {el1:.1f} s"}
+        except Exception as e:  # noqa: BLE001 - the baseline above stands without it
+            reason = f"the one-core pass raised {type(e).__name__}: {e}"
         finally:
             _omp_threads(old)
+    if "one_core" not in r:
+        r["one_core"] = {"unavailable": reason}
     return r
 
 
@@ -716,31 +845,26 @@ def run_reference(args):
 
     oracle.build()
     w = inputs.make_workload(HEADLINE, seed=0)
-    c = w.cache
     B = w.q.shape[0]
-    t0 = time.perf_counter()
-    oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale)
-    one = time.perf_counter() - t0
+    t, nb = _oracle_pass(oracle, w, min(B, 8))
     # each step: a bounded sample of the batch (whole sequences x all heads) of about 2 s
-    nseq = max(1, min(B, int(B * 2.0 / max(one, 1e-3))))
-    sel = __import__("numpy").zeros((B, w.q.shape[1]), dtype=bool)
-    sel[:nseq] = True
-    sample_bytes = int(c.lens[:nseq].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    nseq = _sample_seqs(w, nb / max(t, 1e-6) * 2.0)
+    sample_bytes = _oracle_pass(oracle, w, nseq)[1]
     for _ in range(args.warmup):
-        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, select=sel)
+        _oracle_pass(oracle, w, nseq)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode(w.q, c.k_pages, c.v_pages, c.block_table, c.lens, w.sinks, w.scale, select=sel)
+        _oracle_pass(oracle, w, nseq)
     el = time.perf_counter() - t0
     value = args.steps * sample_bytes / el / 1e9
-    sample = f"first {nseq} of 64 sequences x all 64 heads per step"
+    sample = (f"the first {nseq} of the {B} decode sequences x all 64 heads per step "
+              f"({sample_bytes / 1e9:.2f} GB of KV)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gpt-oss-shape decode: B=64, 64 q / 8 KV heads, head_dim 64, "
-                               "page 16, KV len ~ U[512, 8192], fp32 sinks", "sample": sample},
+        "config": {"workload": WORKLOAD, "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -1,9 +1,13 @@
 """Run one named workload through the library a few times (for profilers).
 
-  python -m paged_gqa_attention_head_gb300.run_workload <workload> [--iters N] [--op decode|prefill|append]
+  python -m paged_gqa_attention_head_gb300.run_workload <workload> [--iters N] [--op auto|append]
+                                                         [--first N]
 
-Workloads are the seeded shapes in `inputs.WORKLOADS`.  Prints the mean time of
-the timed iterations (CUDA events); every launch goes through the C ABI.
+Workloads are the seeded shapes in `inputs.WORKLOADS`.  `--first N` (decode workloads) keeps
+the first N sequences of the batch, with the same lengths, in a pool of their own pages (a
+cut-down case whose device footprint suits a profiler capture).  Prints the mean time of
+the timed iterations (CUDA events) and the KV bytes one call reads; every launch goes
+through the C ABI.
 """
 from __future__ import annotations
 
@@ -19,9 +23,15 @@ def main() -> None:
     ap.add_argument("workload", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--op", choices=["auto", "append"], default="auto")
+    ap.add_argument("--first", type=int, default=0)
     args = ap.parse_args()
     dev = torch.device("cuda:0")
     w = inputs.make_workload(args.workload, seed=0)
+    if args.first and isinstance(w, inputs.DecodeInputs):
+        spec = inputs.WORKLOADS[args.workload]
+        lens = [int(x) for x in w.cache.lens[:args.first]]
+        w = inputs.make_decode(lens, len(lens), w.num_qo_heads, w.num_kv_heads, w.head_dim, seed=0,
+                               sinks=w.sinks is not None, kv_dtype=spec.get("kv_dtype", "bf16"))
     if args.op == "append":
         lens = w.new_lens
         a = inputs.make_append(lens, [0] * len(lens), w.num_kv_heads, w.head_dim, seed=0)
@@ -51,7 +61,8 @@ def main() -> None:
         fn()
     e1.record()
     torch.cuda.synchronize()
-    print(f"{args.workload}: {e0.elapsed_time(e1) / args.iters:.4f} ms per call")
+    extra = f", {w.kv_bytes()} KV bytes per call" if isinstance(w, inputs.DecodeInputs) else ""
+    print(f"{args.workload}: {e0.elapsed_time(e1) / args.iters:.4f} ms per call{extra}")
 
 
 if __name__ == "__main__":
