@@ -21,7 +21,8 @@
  *     token j of sequence b is slot j % page_size of page block_table[b][j / page_size]
  *     block_table: int32 [num_seqs, max_pages_per_seq], row-major
  *
- * Supported: bf16 data (and FP8 E4M3 KV caches for decode and append, see below),
+ * Supported: bf16 data (and FP8 E4M3 KV caches for decode, append and the prefix of a
+ * chunked prefill, see below),
  * fp32 sinks, head_dim 64 or 128, page_size 16, num_qo_heads / num_kv_heads in
  * {1, 2, 4, 8, 16}.
  *
@@ -98,6 +99,16 @@ typedef struct sinkattn_paged_desc {
                                 * results do not depend on it.  The decode workspace size
                                 * query takes it into account (a smaller grid needs fewer
                                 * partial-state slots). */
+    int32_t wait_limit_us;     /* watchdog of the kernels' pipeline waits (decode, FP8
+                                * decode, prefill), in microseconds: a wait that has not
+                                * completed after this long gives up, the kernel sets
+                                * SINKATTN_STATUS_WAIT_TIMEOUT, lets the copies and MMAs
+                                * it already issued finish, and returns (outputs are then
+                                * unspecified).  0 = the default, 2 seconds; negative:
+                                * SINKATTN_ERR_INVALID_ARG.  1 is the testing setting of
+                                * that path: a wait then gives up unless it is already
+                                * complete when first tested, which the first wait of
+                                * every kernel is not (its copy from HBM is in flight). */
 } sinkattn_paged_desc;
 
 /* Human-readable name of an error code (static string). */
@@ -140,7 +151,13 @@ int sinkattn_workspace_init(void *workspace, size_t ws_bytes, sinkattn_stream_t 
  * lse:         fp32 [B, Hq] natural-log normaliser including the sink, or NULL
  * workspace:   device scratch of ws_bytes (>= sinkattn_decode_workspace_size)
  *
- * Equivalent to sinkattn_decode_splitkv followed by sinkattn_decode_merge.
+ * Equivalent to sinkattn_decode_splitkv followed by sinkattn_decode_merge.  With a short
+ * sliding window (0 < desc->window <= 2032: every (sequence, KV head) then sees at most
+ * 128 pages) it runs a one-launch plan instead - one CTA per (sequence, KV head), its
+ * warps splitting the visible pages, their partial states merged in shared memory, no
+ * merge launch - whose results agree with the two-kernel plan within rounding (the sums
+ * are split differently) and do not depend on the grid; sinkattn_decode_append and
+ * sinkattn_decode_append_rope do the same.
  */
 int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
                     const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
@@ -195,6 +212,45 @@ int sinkattn_decode_append(const void *q, const void *k_new, const void *v_new, 
                            const float *sinks, float scale, void *out, float *lse,
                            const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                            sinkattn_stream_t stream);
+
+/* Rotary position embedding of gpt-oss: NeoX layout with YaRN frequency scaling
+ * (TensorSharp docs/models/gptoss.md, section 3 "Forward graph": RoPE_NeoX with YaRN
+ * scaling, original context 4096, freqScale = 1 / RopeScale, beta_fast 32, beta_slow 1;
+ * "GPT-OSS on Day 0": YaRN position encoding as in DeepSeek-V3).  For head_dim D, pair i
+ * (i < D/2) is elements i and i + D/2.  Its base frequency w_i = base^(-2i/D); with the
+ * correction dims c(r) = D ln(original_context / (2 pi r)) / (2 ln base),
+ * lo = max(0, floor(c(beta_fast))), hi = min(D - 1, ceil(c(beta_slow))) and the ramp
+ * y_i = clamp((i - lo) / max(0.001, hi - lo), 0, 1), the pair turns at the rate
+ * theta_i = (1 - y_i) w_i + y_i w_i / factor; at position p, with a = p theta_i,
+ *     x'[i]       = mscale (x[i] cos a - x[i + D/2] sin a)
+ *     x'[i + D/2] = mscale (x[i + D/2] cos a + x[i] sin a),    mscale = 1 + 0.1 ln(factor).
+ * factor = 1 is plain NeoX RoPE. */
+typedef struct sinkattn_rope_desc {
+    double base;              /* frequency base (> 1), e.g. 150000 for gpt-oss */
+    double factor;            /* YaRN scale factor (RopeScale) >= 1 */
+    int32_t original_context; /* context length before scaling (> 0), 4096 for gpt-oss */
+    double beta_fast;         /* > beta_slow > 0; 32 for gpt-oss */
+    double beta_slow;         /* 1 for gpt-oss */
+} sinkattn_rope_desc;
+
+/* Decode step with rotary embedding and K/V append, in the order of gptoss.md section 3
+ * (RoPE on Q and K, append K and V to the cache, attention): q [B, Hq, D] and k_new
+ * [B, Hkv, D] arrive NOT rotated; both are rotated at the new token's position
+ * seq_lens[b] - 1 and rounded to bf16, the rotated key and v_new are written to the cache
+ * at that position, and the rotated query attends the seq_lens[b] cached tokens - all in
+ * the launches of sinkattn_decode_append (no extra launch).  The rotation angles are
+ * reduced in float arithmetic that carries each theta_i as two floats, so positions up to
+ * 2^24 keep the angle within ~1e-6 rad; a rotated element can then differ from the bf16
+ * rounding of the exact rotation by one bf16 step when it lies within ~1e-7 (relative) of
+ * a rounding boundary.
+ * rope: the rotation's parameters (host pointer, read during the call only); positions
+ * (max_pages_per_seq * 16) must stay below 2^24 (else SINKATTN_ERR_UNSUPPORTED).
+ * Other arguments, results and errors as for sinkattn_decode_append. */
+int sinkattn_decode_append_rope(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                                void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                                const float *sinks, float scale, const sinkattn_rope_desc *rope,
+                                void *out, float *lse, const sinkattn_paged_desc *desc,
+                                void *workspace, size_t ws_bytes, sinkattn_stream_t stream);
 
 /* -------------------------------------------------------- FP8 E4M3 KV cache --
  * A KV cache of one byte per element.  The pages name an FP8 serving precision
@@ -259,8 +315,14 @@ int sinkattn_append_kv_fp8(const void *k, const void *v, const float *k_scale,
  * the library holds the array until the process exits.
  *
  * The first call on a device looks up the array's device address (once per device,
- * with that device current); make that first call before any stream capture.  The
- * call itself allocates nothing and calls no allocating routine.  All calls on a
+ * with that device current).  With CUDA's lazy module loading (the default) that
+ * lookup is also what loads the library's device code and so places the 32 MiB array
+ * in device memory: the driver allocates it inside that first call.  Callers that must
+ * not see any allocation after start-up therefore make one call at start-up (an empty
+ * batch, num_seqs = 0, is enough), and that first call must come before any stream
+ * capture.  Later calls allocate nothing and call no allocating routine.  Arguments
+ * are checked before anything is enqueued; a rejected call leaves *status untouched.
+ * All calls on a
  * device share the one array and it keeps the previous call's contents, so calls
  * that overlap on the GPU (different streams without ordering, or different host
  * threads) race; order them on one stream or synchronise.
@@ -307,6 +369,24 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
                      const float *sinks, float scale, void *out, float *lse,
                      const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                      sinkattn_stream_t stream);
+
+/* Chunked prefill over an FP8 E4M3 paged prefix: sinkattn_prefill with the prefix pages
+ * in the FP8 cache convention above (uint8 codes [num_pages, Hkv, 16, D], value =
+ * scale[g] * e4m3(code); k_scale / v_scale fp32 [Hkv] on the device, NULL = 1, positive
+ * and finite).  The new tokens' k, v stay bf16 (a serving step appends them to the FP8 cache
+ * with sinkattn_append_kv_fp8 for later steps).  The prefix tiles are copied as codes and
+ * converted in shared memory: K exactly to bf16 code values, the K scale multiplying those
+ * tiles' scores; V to fp16 of value * 2^-k per 32-key quarter (relative rounding <= 2^-11,
+ * the same as bf16 V tiles; a NaN code sets SINKATTN_STATUS_VALUE_RANGE).  All four prefix
+ * pointers and the prefix lengths are required; other arguments, workspace and errors as
+ * for sinkattn_prefill. */
+int sinkattn_prefill_fp8(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                         int32_t total_tokens, const void *k_pages, const void *v_pages,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                         const float *sinks, float scale, void *out, float *lse,
+                         const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                         sinkattn_stream_t stream);
 
 /* ------------------------------------------------------------------ append --
  * Write new K/V rows into the paged cache (each layer stores its K and V there before its

@@ -65,14 +65,18 @@ int encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dim
 
 // FP8 pages [num_pages, Hkv, 16, D] of uint8 codes: one box is a whole (page, head),
 // 16 rows of D bytes, swizzled by 64 bytes (D = 64) or 128 bytes (D = 128).
-int encode_pages_map_fp8(CUtensorMap *m, const void *pages, int num_pages, int Hkv, int D) {
+// swizzled: the decode's layout (64-byte swizzle at D = 64, 128-byte at D = 128); else rows
+// of D bytes one after the other (the prefill's staging of FP8 prefix pages).
+int encode_pages_map_fp8(CUtensorMap *m, const void *pages, int num_pages, int Hkv, int D,
+                         bool swizzled = true) {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)Hkv,
                                 (cuuint64_t)(num_pages > 0 ? num_pages : 1)};
     const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)kPageSize * D,
                                    (cuuint64_t)Hkv * kPageSize * D};
     const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kPageSize, 1, 1};
     return encode_map(m, pages, 4, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                      D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+                      !swizzled ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                : (D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B));
 }
 
 // Pages [num_pages, Hkv, 16, D]: dims {D, 16, Hkv, num_pages}; a box is one
@@ -97,7 +101,7 @@ int encode_rows_map(CUtensorMap *m, const void *base, int T, int H, int D, int r
 int check_heads(const sinkattn_paged_desc *d) {
     if (!d) return SINKATTN_ERR_INVALID_ARG;
     if (d->num_seqs < 0 || d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
-        d->num_pages < 0 || d->max_pages_per_seq < 0 || d->max_sms < 0)
+        d->num_pages < 0 || d->max_pages_per_seq < 0 || d->max_sms < 0 || d->wait_limit_us < 0)
         return SINKATTN_ERR_INVALID_ARG;
     if (d->num_qo_heads % d->num_kv_heads) return SINKATTN_ERR_INVALID_ARG;
     const int G = d->num_qo_heads / d->num_kv_heads;
@@ -205,6 +209,8 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.max_pages = desc->max_pages_per_seq;
     a.window = desc->window > 0 ? desc->window : 0;
     a.total_warps = P->layout.total_warps;
+    a.max_sms_cap = desc->max_sms;
+    a.wait_limit_ns = wait_limit_ns(desc->wait_limit_us);
     a.status = reinterpret_cast<uint32_t *>(ws);
     a.ws_prefix = reinterpret_cast<int32_t *>(ws + P->layout.prefix);
     a.ws_plan = reinterpret_cast<int64_t *>(ws + P->layout.plan);
@@ -216,7 +222,53 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.v_new = nullptr;
     a.k_pages_w = nullptr;
     a.v_pages_w = nullptr;
+    a.rope_on = 0;
+    a.rope_mscale = 1.f;
     return SINKATTN_OK;
+}
+
+// The YaRN-scaled frequency of every rotary pair (the formulas of sinkattn_rope_desc in
+// include/sinkattn.h), in double on the host - they depend on the parameters only - and
+// handed to the kernel as float pairs hi + lo.  Parameter checks first.
+bool rope_ok(const sinkattn_rope_desc *r) {
+    return r && r->base > 1.0 && r->base < INFINITY && r->factor >= 1.0 && r->factor < INFINITY &&
+           r->original_context > 0 && r->beta_slow > 0.0 && r->beta_fast > r->beta_slow &&
+           r->beta_fast < INFINITY;
+}
+
+int rope_table(const sinkattn_rope_desc *r, int D, DecodeArgs *a) {
+    if (!rope_ok(r)) return SINKATTN_ERR_INVALID_ARG;
+    if (D / 2 > 64) return SINKATTN_ERR_UNSUPPORTED;
+    const double two_pi = 6.283185307179586476925286766559;
+    const double lnb = log(r->base);
+    double lo = floor(D * log(r->original_context / (two_pi * r->beta_fast)) / (2.0 * lnb));
+    double hi = ceil(D * log(r->original_context / (two_pi * r->beta_slow)) / (2.0 * lnb));
+    if (lo < 0.0) lo = 0.0;
+    if (hi > D - 1) hi = D - 1;
+    const double span = (hi - lo) > 0.001 ? (hi - lo) : 0.001;
+    for (int i = 0; i < D / 2; ++i) {
+        const double w = pow(r->base, -2.0 * i / D);
+        double y = (i - lo) / span;
+        y = y < 0.0 ? 0.0 : (y > 1.0 ? 1.0 : y);
+        const double th = (1.0 - y) * w + y * (w / r->factor);
+        a->rope_hi[i] = (float)th;
+        a->rope_lo[i] = (float)(th - (double)a->rope_hi[i]);
+    }
+    a->rope_mscale = (float)(1.0 + 0.1 * log(r->factor));
+    a->rope_on = 1;
+    return SINKATTN_OK;
+}
+
+// A decode's launches once its arguments are prepared: the one-launch plan for a short
+// sliding window, else the split-KV kernel and the merge.
+int launch_decode_pair(const DecodePrep &P, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                       const sinkattn_paged_desc *desc, cudaStream_t stream, const char *what) {
+    if (decode_window_fits(desc->window))
+        return cuda_rc(launch_decode_window(desc->head_dim, P.args, kmap, vmap, stream), "sliding-window decode launch");
+    int rc = cuda_rc(launch_decode_splitkv(desc->head_dim, P.args, kmap, vmap, P.layout.ctas, P.layout.smem, stream),
+                     what);
+    if (rc) return rc;
+    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, stream), "merge launch");
 }
 
 int append_common(const void *k, const void *v, const int32_t *cu_seqlens, int32_t total_tokens,
@@ -282,7 +334,7 @@ const char *sinkattn_error_string(int code) {
     }
 }
 
-int sinkattn_version(void) { return 10000; }
+int sinkattn_version(void) { return 10100; }
 
 int sinkattn_decode_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes) {
     if (!bytes) return SINKATTN_ERR_INVALID_ARG;
@@ -343,6 +395,22 @@ int sinkattn_decode(const void *q, const void *k_pages, const void *v_pages,
                     const int32_t *block_table, const int32_t *seq_lens, const float *sinks,
                     float scale, void *out, float *lse, const sinkattn_paged_desc *desc,
                     void *workspace, size_t ws_bytes, sinkattn_stream_t stream) {
+    if (desc && desc->num_seqs > 0 && decode_window_fits(desc->window)) {
+        // a short sliding window: the one-launch plan
+        DecodePrep P;
+        int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
+                                ws_bytes, &P);
+        if (rc) return rc;
+        if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16))
+            return SINKATTN_ERR_INVALID_ARG;
+        CUtensorMap kmap, vmap;
+        rc = encode_pages_map(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+        if (rc) return rc;
+        rc = encode_pages_map(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+        if (rc) return rc;
+        return cuda_rc(launch_decode_window(desc->head_dim, P.args, kmap, vmap, (cudaStream_t)stream),
+                       "sliding-window decode launch");
+    }
     int rc = sinkattn_decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out,
                                      lse, desc, workspace, ws_bytes, stream);
     if (rc) return rc;
@@ -373,11 +441,38 @@ int sinkattn_decode_append(const void *q, const void *k_new, const void *v_new, 
     P.args.v_new = v_new;
     P.args.k_pages_w = k_pages;
     P.args.v_pages_w = v_pages;
-    rc = cuda_rc(launch_decode_splitkv(desc->head_dim, P.args, kmap, vmap, P.layout.ctas,
-                                       P.layout.smem, (cudaStream_t)stream),
-                 "split-KV decode with append launch");
+    return launch_decode_pair(P, kmap, vmap, desc, (cudaStream_t)stream, "split-KV decode with append launch");
+}
+
+int sinkattn_decode_append_rope(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                                void *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                                const float *sinks, float scale, const sinkattn_rope_desc *rope,
+                                void *out, float *lse, const sinkattn_paged_desc *desc,
+                                void *workspace, size_t ws_bytes, sinkattn_stream_t stream) {
+    // an empty batch is a no-op (its data pointers may be NULL)
+    if (desc && desc->num_seqs == 0) return check_decode_desc(desc);
+    if (!k_pages || !v_pages || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !k_new || !v_new ||
+        !aligned(k_new, 16) || !aligned(v_new, 16) || !rope_ok(rope))
+        return SINKATTN_ERR_INVALID_ARG;
+    DecodePrep P;
+    int rc = prepare_decode(q, block_table, seq_lens, sinks, scale, out, lse, desc, workspace,
+                            ws_bytes, &P);
     if (rc) return rc;
-    return cuda_rc(launch_decode_merge(desc->head_dim, P.args, (cudaStream_t)stream), "merge launch");
+    // positions up to max_pages * 16 - 1 must be exact floats for the angle reduction
+    if ((int64_t)desc->max_pages_per_seq * kPageSize > (int64_t)1 << 24) return SINKATTN_ERR_UNSUPPORTED;
+    rc = rope_table(rope, desc->head_dim, &P.args);
+    if (rc) return rc;
+    CUtensorMap kmap, vmap;
+    rc = encode_pages_map(&kmap, k_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    rc = encode_pages_map(&vmap, v_pages, desc->num_pages, desc->num_kv_heads, desc->head_dim);
+    if (rc) return rc;
+    P.args.k_new = k_new;
+    P.args.v_new = v_new;
+    P.args.k_pages_w = k_pages;
+    P.args.v_pages_w = v_pages;
+    return launch_decode_pair(P, kmap, vmap, desc, (cudaStream_t)stream,
+                              "split-KV decode with rotary embedding and append launch");
 }
 
 int sinkattn_decode_fp8_splitkv(const void *q, const void *k_pages, const void *v_pages,
@@ -429,12 +524,13 @@ int sinkattn_prefill_workspace_size(const sinkattn_paged_desc *desc, size_t *byt
     return SINKATTN_OK;
 }
 
-int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                     int32_t total_tokens, const void *k_pages, const void *v_pages,
-                     const int32_t *prefix_block_table, const int32_t *prefix_lens,
-                     const float *sinks, float scale, void *out, float *lse,
-                     const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
-                     sinkattn_stream_t stream) {
+namespace {
+int prefill_common(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                   int32_t total_tokens, const void *k_pages, const void *v_pages,
+                   const int32_t *prefix_block_table, const int32_t *prefix_lens, const float *sinks,
+                   float scale, void *out, float *lse, const sinkattn_paged_desc *desc, void *workspace,
+                   size_t ws_bytes, bool fp8, const float *k_scale, const float *v_scale,
+                   sinkattn_stream_t stream) {
     int rc = check_heads(desc);
     if (rc) return rc;
     if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
@@ -460,7 +556,12 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     if ((rc = encode_rows_map(&qmap, q, total_tokens, Hq, D, 128))) return rc;
     if ((rc = encode_rows_map(&kmap, k, total_tokens, Hkv, D, 128))) return rc;
     if ((rc = encode_rows_map(&vmap, v, total_tokens, Hkv, D, 128))) return rc;
-    if (has_prefix) {
+    if (fp8 && !has_prefix) return SINKATTN_ERR_INVALID_ARG;
+    if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4))) return SINKATTN_ERR_INVALID_ARG;
+    if (has_prefix && fp8) {
+        if ((rc = encode_pages_map_fp8(&kpmap, k_pages, desc->num_pages, Hkv, D, false))) return rc;
+        if ((rc = encode_pages_map_fp8(&vpmap, v_pages, desc->num_pages, Hkv, D, false))) return rc;
+    } else if (has_prefix) {
         if ((rc = encode_pages_map(&kpmap, k_pages, desc->num_pages, Hkv, D))) return rc;
         if ((rc = encode_pages_map(&vpmap, v_pages, desc->num_pages, Hkv, D))) return rc;
     } else {
@@ -487,10 +588,38 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     a.max_pages = has_prefix ? desc->max_pages_per_seq : 0;
     a.window = desc->window > 0 ? desc->window : 0;
     a.max_sms = desc->max_sms;
+    a.wait_limit_ns = wait_limit_ns(desc->wait_limit_us);
     a.status = static_cast<uint32_t *>(workspace);
+    a.fp8_prefix = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
     if (e == cudaErrorNotSupported) return SINKATTN_ERR_UNSUPPORTED;
     return cuda_rc(e, "prefill launch");
+}
+}  // namespace
+
+int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                     int32_t total_tokens, const void *k_pages, const void *v_pages,
+                     const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                     const float *sinks, float scale, void *out, float *lse,
+                     const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                     sinkattn_stream_t stream) {
+    return prefill_common(q, k, v, cu_seqlens, total_tokens, k_pages, v_pages, prefix_block_table,
+                          prefix_lens, sinks, scale, out, lse, desc, workspace, ws_bytes, false, nullptr,
+                          nullptr, stream);
+}
+
+int sinkattn_prefill_fp8(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                         int32_t total_tokens, const void *k_pages, const void *v_pages,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *prefix_block_table, const int32_t *prefix_lens,
+                         const float *sinks, float scale, void *out, float *lse,
+                         const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
+                         sinkattn_stream_t stream) {
+    return prefill_common(q, k, v, cu_seqlens, total_tokens, k_pages, v_pages, prefix_block_table,
+                          prefix_lens, sinks, scale, out, lse, desc, workspace, ws_bytes, true, k_scale,
+                          v_scale, stream);
 }
 
 int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,

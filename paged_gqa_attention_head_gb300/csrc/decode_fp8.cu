@@ -82,20 +82,6 @@ __device__ __forceinline__ int tok_row(int k) {
     return k;
 }
 
-// The two E4M3 codes in bits 0-15 (or 16-31) of w to an f16 pair, the lower byte in the
-// lower half: one cvt on a 16-bit half of the register, no repacking.
-__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
-        : "=r"(r) : "r"(w));
-    return r;
-}
-__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
-        : "=r"(r) : "r"(w));
-    return r;
-}
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
@@ -297,10 +283,12 @@ __global__ void __launch_bounds__(Fp8Cfg<D>::kThreads)
 
     for (int u = 0; u < n_units; ++u) {
         const int stage = u % S;
-        if (!mbar_wait_sleep(&wbar[stage], (uint32_t)((u / S) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&wbar[stage], (uint32_t)((u / S) & 1), a.wait_limit_ns))) {
+            // give up (all lanes together: the outcome is voted): record it, let the copies
+            // already issued land, leave
             if (lane == 0) set_status(a.status, SINKATTN_STATUS_WAIT_TIMEOUT);
             for (int v = u; v < min(n_units, u + S); ++v)
-                mbar_wait(&wbar[v % S], (uint32_t)((v / S) & 1), 100000000ull);
+                mbar_wait(&wbar[v % S], (uint32_t)((v / S) & 1), kDrainLimitNs);
             return;
         }
         // Take the unit's fragments into registers and hand the stage straight back to the

@@ -14,6 +14,9 @@ void record_cuda_error(cudaError_t e, const char *where);
 constexpr int kPageSize = 16;
 constexpr uint32_t kStatusBytes = 256;  // workspace header holding the status word
 
+// Give-up time of a pipeline wait for a descriptor (wait_limit_us; 0 = 2 s).
+inline uint64_t wait_limit_ns(int32_t us) { return us > 0 ? (uint64_t)us * 1000ull : 2000000000ull; }
+
 // Arguments of the two decode kernels (plain device pointers and sizes).
 struct DecodeArgs {
     const void *q;               // bf16 [B, Hq, D]
@@ -26,6 +29,8 @@ struct DecodeArgs {
     int B, Hq, Hkv, G, num_pages, max_pages;
     int window;             // sliding window (keys at the last `window` positions); 0: none
     int total_warps;        // warps of the split-KV grid
+    int max_sms_cap;        // SMs the sliding-window grid may use; 0: all
+    uint64_t wait_limit_ns; // give-up time of a pipeline wait
     uint32_t *status;       // workspace header
     int32_t *ws_prefix;     // [B + 1] pages-per-sequence prefix sum (written by CTA 0)
     int64_t *ws_plan;       // [2]: total page units, page units per warp
@@ -37,6 +42,14 @@ struct DecodeArgs {
     const void *v_new;
     void *k_pages_w;        // the cache the new rows are written into (decode with append)
     void *v_pages_w;
+    // Decode with append and rotary embedding (rope_on != 0): q and the new key are rotated
+    // at the new token's position before use.  Per pair i < D/2 the YaRN-scaled frequency
+    // theta_i as a float pair rope_hi[i] + rope_lo[i] (hi the nearest float, lo the rest),
+    // and the magnitude factor rope_mscale applied to both outputs of a pair.
+    int rope_on;
+    float rope_mscale;
+    float rope_hi[64];
+    float rope_lo[64];
 };
 
 // Grid and shared memory of the split-KV decode kernel for head_dim D and
@@ -47,6 +60,12 @@ cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap 
                                   const CUtensorMap &vmap, int ctas, int smem_bytes,
                                   cudaStream_t stream);
 cudaError_t launch_decode_merge(int D, const DecodeArgs &a, cudaStream_t stream);
+
+// Sliding-window decode in one launch (no merge, no workspace partials): used by the decode
+// entry points when decode_window_fits(window).
+bool decode_window_fits(int window);
+cudaError_t launch_decode_window(int D, const DecodeArgs &a, const CUtensorMap &kmap,
+                                 const CUtensorMap &vmap, cudaStream_t stream);
 
 // The same for the decode over an FP8 E4M3 cache (uint8 tensor maps, one box per page).
 cudaError_t decode_fp8_launch_shape(int D, int G, int B, int device, int *ctas, int *warps_per_cta,
@@ -79,7 +98,10 @@ struct PrefillArgs {
     int T, n, Hq, Hkv, G, D, num_pages, max_pages;
     int window;  // sliding window (keys at the query's last `window` positions); 0: none
     int max_sms;  // SMs the persistent grid may use; 0: all
+    uint64_t wait_limit_ns;  // give-up time of a pipeline wait
     uint32_t *status;
+    bool fp8_prefix;                   // the prefix pages are FP8 E4M3 codes (uint8)
+    const float *k_scale, *v_scale;    // FP8 prefix: [Hkv] per-KV-head scales, or nullptr (1)
 };
 // Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,

@@ -78,7 +78,7 @@ struct PrefillCfg {
     static constexpr bool kSplitP = D == 64;         // P in buffers of its own (else over S)
     static constexpr int kSBufs = 2;                 // S buffers (128 columns, fp32)
     static constexpr int kPBufs = 2;                 // P buffers (64 columns of fp16 pairs)
-    static constexpr int kNumBars = 2 + 4 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1;
+    static constexpr int kNumBars = 2 + 5 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 4 * kLocateMax * 4;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
@@ -90,33 +90,56 @@ struct PrefillCfg {
         return (kSplitP ? 128u * kSBufs + 64u * kPBufs : 128u * kSBufs) + D * x;
     }
     static_assert(kSplitP || kSBufs == kPBufs, "P over S needs one P buffer per S buffer");
+    // FP8 prefix pages (E4M3 codes, D bytes a row) are staged inside the stage they are
+    // converted into: page p of a tile in the bytes its own converted rows end in, so one
+    // warp converts a page in place (keys 16p .. 16p + 15: bf16 / fp16 rows of 128 bytes,
+    // one such block per 64 columns).
+    __host__ __device__ static constexpr uint32_t kOffFp8Page(int p) {
+        return D == 64 ? 2048u * p + 1024u : 16384u + 2048u * p;
+    }
     static_assert(kColO(2) <= 512, "TMEM columns");
 };
 
 struct Bars {
-    uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *kv_empty, *s_full, *s_free, *p_full,
-        *pv_done, *o_free, *drain;
+    uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *k_conv, *kv_empty, *s_full, *s_free,
+        *p_full, *pv_done, *o_free, *drain;
 };
 
-// Bounded wait that also gives up as soon as another role has given up.  With kSleep
-// the thread sleeps in the wait (for warps off the critical path: it leaves the issue
-// slots to the softmax warps, at ~50 cycles more wake-up latency).
+// Bounded wait (limit_ns of wall time, counted in SM cycles as in mbar_wait, checked every
+// 16 polls) that also gives up as soon as another role has
+// given up.  Every lane of a full warp calls it and all of them get the same answer (the
+// outcome is voted), so a warp never continues with some of its lanes gone - the
+// .sync.aligned instructions that follow need all 32.  With kSleep the warp sleeps in the
+// wait (for warps off the critical path: it leaves the issue slots to the softmax warps, at
+// ~50 cycles more wake-up latency); a sleep lasts at most 100 us, or the limit if shorter.
 template <bool kSleep = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                              uint32_t *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (kSleep) {
-            if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        } else {
-            for (int i = 0; i < 128; ++i)
-                if (mbar_try_wait(bar, parity)) return true;
-        }
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                              uint32_t *status, uint64_t limit_ns) {
+    if (limit_ns <= kImmediateLimitNs) {  // the smallest limit: one non-blocking test
+        if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+        if ((threadIdx.x & 31) == 0) {
             *abort = 1;
             set_status(status, SINKATTN_STATUS_WAIT_TIMEOUT);
+        }
+        return false;
+    }
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = clock64(), lim = limit_cycles(limit_ns);
+    const uint32_t hint = limit_ns < 100000ull ? (uint32_t)limit_ns : 100000u;
+    for (;;) {
+        bool done = false;
+        if (kSleep) {
+            done = mbar_try_wait_sleep(bar, parity, hint);
+        } else {
+            for (int i = 0; i < 16 && !done; ++i) done = mbar_try_wait(bar, parity);
+        }
+        if (__all_sync(0xffffffffu, done)) return true;
+        if (__any_sync(0xffffffffu, *abort != 0)) return false;
+        if (__any_sync(0xffffffffu, (uint64_t)clock64() - t0 >= lim)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort = 1;
+                set_status(status, SINKATTN_STATUS_WAIT_TIMEOUT);
+            }
             return false;
         }
     }
@@ -125,6 +148,105 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+
+// ---------------------------------------------------------------- FP8 prefix conversion
+// Two f16 values (a packed pair) to a bf16 pair (exact for E4M3 values).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return pack_bf16x2(lo, hi);
+}
+// The f16 value in the lower half of h, as float.
+__device__ __forceinline__ float f16lo_to_f32(uint32_t h) {
+    float lo;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(lo) : "r"(h));
+    return lo;
+}
+// Two f16 values times sc, rounded to an f16 pair.
+__device__ __forceinline__ uint32_t f16x2_scaled(uint32_t h, float sc) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return pack_f16x2(lo * sc, hi * sc);
+}
+
+// Eight E4M3 codes (two words) to one 16-byte vector: bf16 code values (kToBf16) or fp16
+// code values times sc.
+template <bool kToBf16>
+__device__ __forceinline__ uint4 codes8(uint32_t w0, uint32_t w1, float sc) {
+    const uint32_t h0 = e4m3x2_lo_to_f16x2(w0), h1 = e4m3x2_hi_to_f16x2(w0);
+    const uint32_t h2 = e4m3x2_lo_to_f16x2(w1), h3 = e4m3x2_hi_to_f16x2(w1);
+    if (kToBf16) return make_uint4(f16x2_to_bf16x2(h0), f16x2_to_bf16x2(h1), f16x2_to_bf16x2(h2), f16x2_to_bf16x2(h3));
+    return make_uint4(f16x2_scaled(h0, sc), f16x2_scaled(h1, sc), f16x2_scaled(h2, sc), f16x2_scaled(h3, sc));
+}
+
+// One converter warp's quarter of an FP8 prefix tile (keys 32q .. 32q + 31, pages 2q and
+// 2q + 1) from its staged codes to 128-byte swizzled rows in place: bf16 code values for K,
+// fp16 code values times sc for V.  Every lane reads its codes of a page (or half page)
+// before any lane writes, since the rows written cover the codes staged.
+template <int D, bool kToBf16>
+__device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane, float sc) {
+    using C = PrefillCfg<D>;
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+        const int p = 2 * q + i;
+        const uint8_t *src = t + C::kOffFp8Page(p);
+        if (D == 64) {
+            // lane: row r, codes 32h .. 32h + 31 -> 16-byte chunks 4h .. 4h + 3 of row 16p + r
+            const int r = lane >> 1, h = lane & 1;
+            const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 64 + h * 32);
+            const uint4 y = *reinterpret_cast<const uint4 *>(src + r * 64 + h * 32 + 16);
+            __syncwarp();
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 0)) = codes8<kToBf16>(x.x, x.y, sc);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 1)) = codes8<kToBf16>(x.z, x.w, sc);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 2)) = codes8<kToBf16>(y.x, y.y, sc);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 3)) = codes8<kToBf16>(y.z, y.w, sc);
+        } else {
+            // two passes of eight rows: lane: row r, codes 32 h4 .. 32 h4 + 31 -> column block
+            // h4 / 2, chunks 4 (h4 % 2) .. + 3 (the rows of block 1 are where the codes sit)
+#pragma unroll 1
+            for (int ps = 0; ps < 2; ++ps) {
+                const int r = ps * 8 + (lane >> 2), h4 = lane & 3;
+                const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + h4 * 32);
+                const uint4 y = *reinterpret_cast<const uint4 *>(src + r * 128 + h4 * 32 + 16);
+                __syncwarp();
+                uint8_t *blk = t + (h4 >> 1) * 16384;
+                const int c0 = 4 * (h4 & 1);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 0)) = codes8<kToBf16>(x.x, x.y, sc);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 1)) = codes8<kToBf16>(x.z, x.w, sc);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 2)) = codes8<kToBf16>(y.x, y.y, sc);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 3)) = codes8<kToBf16>(y.z, y.w, sc);
+                __syncwarp();
+            }
+        }
+    }
+}
+
+// Largest |E4M3 code| (its 7-bit magnitude; 0x7F is NaN) among the staged codes of a
+// quarter (pages 2q, 2q + 1), over the warp.
+template <int D>
+__device__ __forceinline__ uint32_t fp8_quarter_max(const uint8_t *t, int q, int lane) {
+    using C = PrefillCfg<D>;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(t + C::kOffFp8Page(2 * q + i));
+#pragma unroll
+        for (int e = 0; e < D / 32; ++e) {  // 16 x D bytes = 32 * (D / 32) vectors
+            const uint4 w = src[e * 32 + lane];
+            mx = __vmaxu4(mx, w.x & 0x7F7F7F7Fu);
+            mx = __vmaxu4(mx, w.y & 0x7F7F7F7Fu);
+            mx = __vmaxu4(mx, w.z & 0x7F7F7F7Fu);
+            mx = __vmaxu4(mx, w.w & 0x7F7F7F7Fu);
+        }
+    }
+    mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
+    return __reduce_max_sync(0xffffffffu, mx);
 }
 
 // Work list, in two parts.  (A) Requests with a paged prefix, request by request (each
@@ -345,8 +467,11 @@ __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it
 }
 
 // kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
-// window arithmetic.
-template <int D, bool kWindow>
+// window arithmetic.  kFp8: the paged prefix is an FP8 E4M3 cache (value = scale[g] *
+// e4m3(code)); its tiles are staged as codes and converted in shared memory by the
+// converter warps - K to bf16 code values (exact; the K scale joins the score scale of
+// those tiles), V to fp16 value * 2^-k like the bf16 V tiles.
+template <int D, bool kWindow, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kpmap,
@@ -367,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.k_full = bb + 2;
     bars.v_full = bars.k_full + NS;
     bars.v_conv = bars.v_full + NS;     // [NS] the stage's V tile is in fp16
-    bars.kv_empty = bars.v_conv + NS;
+    bars.k_conv = bars.v_conv + NS;     // [NS] FP8 prefix: the stage's K tile is in bf16
+    bars.kv_empty = bars.k_conv + NS;
     // Every wait below is for the next completion of its barrier or the one before,
     // never older: a parity wait cannot tell phases two apart.
     bars.s_full = bars.kv_empty + NS;      // [NBS] per S buffer: its S product is done
@@ -399,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.v_conv[s], 4);  // one arrive per converter warp
+            mbar_init(&bars.k_conv[s], 4);
             mbar_init(&bars.kv_empty[s], 1);
         }
         for (int b = 0; b < NBS; ++b) {
@@ -410,9 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.pv_done[p], 1);
         }
         for (int x = 0; x < 2; ++x) mbar_init(&bars.o_free[x], 4);
-        mbar_init(bars.drain, 2);  // one commit from each MMA-issuing warp
+        mbar_init(bars.drain, 64);  // one commit from every lane of the two MMA-issuing warps
         fence_mbar_init();
     }
+    // What the producer issued (for the drain after an abort): the Q tiles of items
+    // 0..q_issued and the K/V tiles 0..kv_issued-1 of the ring.
+    int q_issued = -1, kv_issued = 0;
     if (warp == 1) tc::alloc(s_tmem, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
@@ -439,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
             }
             // Q tiles of this item, once the previous item's last S products are done
-            if (k > 0 && !wait_or_abort<true>(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status)) {
+            if (k > 0 && !wait_or_abort<true>(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status, a.wait_limit_ns)) {
                 ok = false;
                 break;
             }
@@ -451,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sQ + x * C::kQBytes + hf * 16384, &qmap, bars.q_full, hf * 64,
                                     it.h0 + x, gm.row0 + it.qb * kBM);
             }
+            q_issued = k;
             for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int s = kv % NS, u = kv / NS;
                 const int tt = kWindow ? gm.t0 + j : j;  // key tile
@@ -469,13 +600,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (u > 0 &&
-                    !wait_or_abort<true>(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status)) {
+                    !wait_or_abort<true>(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status, a.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
                 uint8_t *kt = sK + s * C::kKVBytes;
                 uint8_t *vt = sV + s * C::kKVBytes;
-                if (tt < gm.n_pre) {
+                if (kFp8 && tt < gm.n_pre) {
+                    // eight FP8 pages of 16 tokens, as codes into their staging places: each
+                    // whole valid page by a TMA issued from its own lane (one box of 16 rows x D
+                    // bytes), the others by the warp (valid rows copied, the rest code 0 = 0.0)
+                    const bool full = nrow == kPageSize && pg >= 0;
+                    const uint32_t full_mask = __ballot_sync(0xffffffffu, full);
+                    const uint32_t other_mask = __ballot_sync(0xffffffffu, lane < 8 && !full);
+                    if (lane == 0) {
+                        const uint32_t bytes = (uint32_t)__popc(full_mask) * kPageSize * D;
+                        mbar_expect_tx(&bars.k_full[s], bytes);
+                        mbar_expect_tx(&bars.v_full[s], bytes);
+                    }
+                    if (full) {
+                        tma_load_4d(kt + C::kOffFp8Page(lane), &kpmap, &bars.k_full[s], 0, 0, gm.g, pg);
+                        tma_load_4d(vt + C::kOffFp8Page(lane), &vpmap, &bars.v_full[s], 0, 0, gm.g, pg);
+                    }
+                    for (uint32_t om = other_mask; om; om &= om - 1) {
+                        const int pp = __ffs(om) - 1;
+                        const int pgp = __shfl_sync(0xffffffffu, pg, pp);
+                        const int nv = pgp >= 0 ? __shfl_sync(0xffffffffu, nrow, pp) : 0;
+                        const uint8_t *kg = static_cast<const uint8_t *>(a.k_pages);
+                        const uint8_t *vg = static_cast<const uint8_t *>(a.v_pages);
+                        constexpr int kVec = D / 16;  // 16-byte vectors per row
+                        for (int e = lane; e < kPageSize * kVec; e += 32) {
+                            const int slot = e / kVec, c = e % kVec;
+                            uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
+                            if (slot < nv) {
+                                const int64_t off = (((int64_t)pgp * a.Hkv + gm.g) * kPageSize + slot) * D + c * 16;
+                                kx = *reinterpret_cast<const uint4 *>(kg + off);
+                                vx = *reinterpret_cast<const uint4 *>(vg + off);
+                            }
+                            const uint32_t o = C::kOffFp8Page(pp) + slot * D + c * 16;
+                            *reinterpret_cast<uint4 *>(kt + o) = kx;
+                            *reinterpret_cast<uint4 *>(vt + o) = vx;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bars.k_full[s]);
+                        mbar_arrive(&bars.v_full[s]);
+                    }
+                } else if (tt < gm.n_pre) {
                     // eight pages of 16 tokens: each whole valid page by a TMA issued from its
                     // own lane, the others (ragged tail, missing page) by the warp
                     const bool full = nrow == kPageSize && pg >= 0;
@@ -535,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int hf = 0; hf < C::kHalves; ++hf)
                         tma_load_3d(vt + hf * 16384, &vmap, &bars.v_full[s], hf * 64, gm.g, row);
                 }
+                kv_issued = kv + 1;
                 __syncwarp();
             }
         }
@@ -557,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all lanes wait; the outcome is made warp-uniform so that no lane is left behind
         // at the elect.sync below when a wait gives up
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status));
+            return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status, a.wait_limit_ns));
         };
         int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
         int n_kv = rank < n_items ? geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv : 0;
@@ -594,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !warp_wait(C::kSplitP ? &bars.s_free[b] : &bars.pv_done[b], (use - 1) & 1))
                     break;
                 if (j == 0 && x == 0 && !warp_wait(bars.q_full, (uint32_t)(k & 1))) break;
-                if (x == 0 && !warp_wait(&bars.k_full[st], sp)) break;
+                if (x == 0 && !warp_wait(kFp8 ? &bars.k_conv[st] : &bars.k_full[st], sp)) break;
                 const uint64_t q0 = dq + (uint64_t)((x * C::kQBytes) >> 4);
                 const uint64_t k0 = dk + (uint64_t)((st * C::kKVBytes) >> 4);
                 const bool last = j == n_kv - 1 && x == ntiles - 1;
@@ -646,13 +820,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kv = 0, k = 0;
         bool ok = true;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
-            const int n_kv = geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv;
-            for (int j = 0; j < n_kv; ++j, ++kv) {
+            const ItemGeom gm = geom_of<kWindow>(a, item_of(a, wl, rank));
+            const float vsc = kFp8 && a.v_scale ? a.v_scale[gm.g] : 1.f;
+            for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int st = kv % NS;
+                const bool fp8_tile = kFp8 && (kWindow ? gm.t0 + j : j) < gm.n_pre;
+                if (kFp8) {
+                    // K: the FP8 prefix tiles to bf16 code values (the S products wait for this)
+                    if (!wait_or_abort<true>(&bars.k_full[st], (uint32_t)((kv / NS) & 1), s_abort, a.status,
+                                             a.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (fp8_tile) convert_fp8_quarter<D, true>(sK + st * C::kKVBytes, q, lane, 1.f);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.k_conv[st]);
+                }
                 if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
-                                                            s_abort, a.status))) {
+                                                            s_abort, a.status, a.wait_limit_ns))) {
                     ok = false;
                     break;
+                }
+                if (fp8_tile) {
+                    // V: fp16 of value * 2^-k, value = scale * e4m3(code); k from the quarter's
+                    // largest |value| as for bf16 tiles (a NaN code counts as out of range)
+                    uint8_t *vt8 = sV + st * C::kKVBytes;
+                    const uint32_t mc = fp8_quarter_max<D>(vt8, q, lane);
+                    const float topv = f16lo_to_f32(e4m3x2_lo_to_f16x2(mc)) * vsc;
+                    int kexp = max(0, (int)((__float_as_uint(topv) >> 23) & 0xFFu) - 127 - 14);
+                    if (mc >= 0x7Fu || !(topv < INFINITY) || kexp > 7) {
+                        if (lane == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
+                        kexp = min(kexp, 7);
+                    }
+                    convert_fp8_quarter<D, false>(vt8, q, lane, vsc * __uint_as_float((uint32_t)(127 - kexp) << 23));
+                    if (lane == 0) s_vscale[st * 4 + q] = kexp;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.v_conv[st]);
+                    continue;
                 }
                 uint4 *vt = reinterpret_cast<uint4 *>(sV + st * C::kKVBytes + q * 4096) + lane;
                 // this lane's vectors: 8 per 64-column half, 512 bytes apart
@@ -724,6 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int h = it.h0 + x;
             const int t = it.qb * kBM + r;  // position among the request's new tokens
             const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+            // score scale of FP8 prefix tiles: their K holds code values, the K scale joins here
+            const float sc_pre = kFp8 && a.k_scale ? a.scale_log2 * a.k_scale[gm.g] : a.scale_log2;
             float m_used = sink2;                      // running max, seeded with the sink
             float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
             for (int j = 0; j < gm.n_kv; ++j) {
@@ -731,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = i % NBS, pb = i % NBP;
                 const uint32_t ts = tmem + lane_base + C::kColS(b);
                 const uint32_t tp = tmem + lane_base + C::kColP(pb);
-                if (!wait_or_abort(&bars.s_full[b], (i / NBS) & 1, s_abort, a.status)) {
+                if (!wait_or_abort(&bars.s_full[b], (i / NBS) & 1, s_abort, a.status, a.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -787,7 +995,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7]));
-                const float mt = mx * a.scale_log2;
+                const float sc = kFp8 && tt < gm.n_pre ? sc_pre : a.scale_log2;
+                const float mt = mx * sc;
                 if (j == 0) {
                     const float mn = fmaxf(m_used, mt);
                     l = (m_used == -INFINITY) ? 0.f : l * fast_exp2(m_used - mn);
@@ -798,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O_x must hold the P.V of this query tile's previous key tile,
                         // product i - ntiles (its P buffer's previous use is long done)
                         const uint32_t ip = i - ntiles;
-                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status)) {
+                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
                             ok = false;
                             break;
                         }
@@ -824,13 +1033,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter holding
                 // keys 32ch..32ch+31
                 const int vst = (tcount - 1) % NS;
-                if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status)) {
+                if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status, a.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
                 if (C::kSplitP && i >= (uint32_t)NBP) {
                     // the P buffer is free once the P.V of product i - NBP has completed
-                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status)) {
+                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -839,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
                 const bool k_uniform = kq.x == kq.y && kq.y == kq.z && kq.z == kq.w;  // warp-uniform
                 const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
-                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                const float2 sc2 = make_float2(sc, sc);
                 // running sums of keys c with c % 8 = 2q (.x) and 2q + 1 (.y)
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
@@ -880,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // epilogue: O / l for this row, once the item's last P.V has landed
             const uint32_t il = (tcount - 1) * ntiles + x;  // S product of the last key tile
-            if (!wait_or_abort(&bars.pv_done[il % NBP], (il / NBP) & 1, s_abort, a.status)) {
+            if (!wait_or_abort(&bars.pv_done[il % NBP], (il / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
                 ok = false;
                 break;
             }
@@ -914,35 +1123,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // all roles done: after an abort wait for MMAs still in flight, then free TMEM
+    // All roles done.  After an abort, before TMEM is freed and the CTA's shared memory is
+    // released: every MMA still in flight completes (each lane of the two MMA-issuing warps
+    // commits to the drain barrier; a commit arrives once the MMAs its thread issued have
+    // completed, at once for a thread that issued none), and every copy the producer issued
+    // lands - Q of the last item it loaded, and the last NS tiles of the K/V ring, each stage
+    // holding at most one copy that no consumer took (a stage is refilled only after its
+    // previous tile was consumed, so the parity of its last use names it).  These waits use
+    // their own limit, not the call's: what they wait for always completes.
     tc::fence_before_sync();
     __syncthreads();
-    if ((warp == 1 || warp == 2) && *s_abort) {
-        // a commit arrives once every MMA this warp issued has completed
-        if (lane == 0) {
+    if (*s_abort) {
+        if (warp == 1 || warp == 2) {
             tc::commit(bars.drain);
-            mbar_wait(bars.drain, 0, 100000000ull);
+            mbar_wait(bars.drain, 0, kDrainLimitNs);
+        } else if (warp == 0) {
+            if (q_issued >= 0) mbar_wait(bars.q_full, (uint32_t)(q_issued & 1), kDrainLimitNs);
+            for (int t = kv_issued > NS ? kv_issued - NS : 0; t < kv_issued; ++t) {
+                mbar_wait(&bars.k_full[t % NS], (uint32_t)((t / NS) & 1), kDrainLimitNs);
+                mbar_wait(&bars.v_full[t % NS], (uint32_t)((t / NS) & 1), kDrainLimitNs);
+            }
         }
-        __syncwarp();
+        tc::fence_before_sync();
+        __syncthreads();
     }
-    if (*s_abort) __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
         tc::dealloc(tmem, kTmemCols);
     }
-    if (warp == 0 && *s_abort) {
-        // let any TMA copy still in flight land before the CTA's shared memory is released
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 50000000ull) __nanosleep(1000);
-    }
 }
 
-template <int D, bool kWindow>
+template <int D, bool kWindow, bool kFp8>
 cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,
                      const CUtensorMap &vmap, const CUtensorMap &kpmap, const CUtensorMap &vpmap,
                      cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWindow>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWindow, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     int device = 0, sms = 0;
@@ -951,7 +1167,7 @@ cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtens
     // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more),
     // on at most max_sms SMs when the caller keeps the others for concurrent work
     if (a.max_sms > 0 && a.max_sms < sms) sms = a.max_sms;
-    prefill_kernel<D, kWindow><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
+    prefill_kernel<D, kWindow, kFp8><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
     return cudaGetLastError();
 }
 
@@ -961,12 +1177,21 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &qmap, const 
                            const CUtensorMap &vmap, const CUtensorMap &kpmap,
                            const CUtensorMap &vpmap, cudaStream_t stream) {
     const bool w = a.window > 0;
+    if (a.fp8_prefix) {
+        if (a.D == 64)
+            return w ? launch_d<64, true, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                     : launch_d<64, false, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        if (a.D == 128)
+            return w ? launch_d<128, true, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                     : launch_d<128, false, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        return cudaErrorNotSupported;
+    }
     if (a.D == 64)
-        return w ? launch_d<64, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
-                 : launch_d<64, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        return w ? launch_d<64, true, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                 : launch_d<64, false, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
     if (a.D == 128)
-        return w ? launch_d<128, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
-                 : launch_d<128, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        return w ? launch_d<128, true, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream)
+                 : launch_d<128, false, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
     return cudaErrorNotSupported;
 }
 

@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // As mbar_try_wait, but a thread whose phase is not yet complete sleeps until it
 // completes or `sleep_ns` have passed, instead of returning after a short fixed time
 // (so a waiting warp stops taking issue slots from the warps that work).
@@ -67,29 +80,47 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// A wait that gives up after about `limit_ns` of wall time (checked every 256
-// polls) instead of spinning forever.  Returns false on timeout.
+// Elapsed time of a wait is measured in SM cycles (clock64: fine-grained, where the
+// global nanosecond timer can tick in microsecond steps); a limit in nanoseconds becomes
+// twice as many cycles, which is at least that long at any SM clock up to 2 GHz.
+__device__ __forceinline__ uint64_t limit_cycles(uint64_t limit_ns) { return limit_ns * 2ull; }
+
+// A wait that gives up after about `limit_ns` of wall time (checked every 16 polls)
+// instead of spinning forever.  Returns false on timeout.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// A limit this short means: give up unless the phase is complete when first tested (a
+// non-blocking test).  try_wait may keep a thread suspended until its phase completes, so a
+// wait of a few microseconds hardly ever reports "not yet" for a clock check to see; the
+// smallest limit gives the give-up path a deterministic trigger instead (the first wait of a
+// kernel always finds its copy still in flight).
+constexpr uint64_t kImmediateLimitNs = 1000ull;
+// Limit of the waits a kernel makes after it has given up, for the copies and MMAs it
+// issued itself (these always complete; the limit only keeps the wait bounded).
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = clock64(), lim = limit_cycles(limit_ns);
     for (;;) {
-        for (int i = 0; i < 256; ++i)
+        for (int i = 0; i < 16; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if ((uint64_t)clock64() - t0 >= lim) return false;
     }
 }
 
-// As mbar_wait, sleeping in the wait (see mbar_try_wait_sleep) after one poll.
+// As mbar_wait, sleeping in the wait (see mbar_try_wait_sleep) after one poll; a sleep
+// lasts at most 20 us, or the limit if that is shorter.  With the smallest limit
+// (kImmediateLimitNs) it only tests once.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
                                                 uint64_t limit_ns = kWaitLimitNs) {
+    if (limit_ns <= kImmediateLimitNs) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = clock64(), lim = limit_cycles(limit_ns);
+    const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+        if ((uint64_t)clock64() - t0 >= lim) return false;
     }
 }
 
@@ -199,6 +230,21 @@ __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The two E4M3 codes in bits 0-15 (or 16-31) of w to an f16 pair (exact), the lower byte
+// in the lower half: one cvt on a 16-bit half of the register, no repacking.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r) : "r"(w));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
+        : "=r"(r) : "r"(w));
     return r;
 }
 

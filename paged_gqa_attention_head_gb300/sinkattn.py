@@ -30,7 +30,14 @@ _P, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_si
 class PagedDesc(ctypes.Structure):
     _fields_ = [("num_seqs", _I32), ("num_qo_heads", _I32), ("num_kv_heads", _I32),
                 ("head_dim", _I32), ("page_size", _I32), ("num_pages", _I32),
-                ("max_pages_per_seq", _I32), ("window", _I32), ("max_sms", _I32)]
+                ("max_pages_per_seq", _I32), ("window", _I32), ("max_sms", _I32),
+                ("wait_limit_us", _I32)]
+
+
+class RopeDesc(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_double), ("factor", ctypes.c_double),
+                ("original_context", _I32), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double)]
 
 
 _DP = ctypes.POINTER(PagedDesc)
@@ -45,10 +52,14 @@ SIGNATURES = {
     "sinkattn_decode_merge": (ctypes.c_int, [_P, _P, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_append": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ,
                                               _P]),
+    "sinkattn_decode_append_rope": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F,
+                                                   ctypes.POINTER(RopeDesc), _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _P]),
     "sinkattn_prefill_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
     "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
                                         _P, _SZ, _P]),
+    "sinkattn_prefill_fp8": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _F, _P,
+                                            _P, _DP, _P, _SZ, _P]),
     "sinkattn_append_kv": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _DP, _P, _SZ, _P]),
     "sinkattn_decode_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _DP, _P, _SZ,
                                            _P]),
@@ -130,13 +141,13 @@ def workspace(nbytes: int, device: torch.device, tag: str = "default") -> torch.
 
 
 def paged_desc(num_seqs, num_qo_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
-               page_size=PAGE_SIZE, window=0, max_sms=0) -> PagedDesc:
+               page_size=PAGE_SIZE, window=0, max_sms=0, wait_limit_us=0) -> PagedDesc:
     """window > 0: sliding window (each query sees the keys at its last `window`
     positions); 0: full attention.  max_sms > 0: the persistent decode and prefill grids
     use at most that many SMs (the rest stay free for concurrent work on other streams);
-    0: all SMs."""
+    0: all SMs.  wait_limit_us > 0: give-up time of the kernels' pipeline waits (0: 2 s)."""
     return PagedDesc(num_seqs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
-                     max_pages_per_seq, int(window), int(max_sms))
+                     max_pages_per_seq, int(window), int(max_sms), int(wait_limit_us))
 
 
 _ws_sizes: dict = {}
@@ -175,7 +186,7 @@ def _codes(t: torch.Tensor) -> torch.Tensor:
 
 
 def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
-                 want_lse, window=0, kv_dtype=torch.bfloat16, max_sms=0):
+                 want_lse, window=0, kv_dtype=torch.bfloat16, max_sms=0, wait_limit_us=0):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k_pages, "k_pages", kv_dtype, dev, 4)
@@ -201,7 +212,7 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
     elif lse is not None:
         _need(lse, "lse", torch.float32, dev, 2)
     desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window,
-                      max_sms=max_sms)
+                      max_sms=max_sms, wait_limit_us=wait_limit_us)
     nbytes = decode_workspace_size(desc)
     if ws is None:
         ws = workspace(nbytes, dev)
@@ -212,12 +223,12 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None, lse=None,
-           workspace_buf=None, return_lse=True, window=0, max_sms=0):
+           workspace_buf=None, return_lse=True, window=0, max_sms=0, wait_limit_us=0):
     """Split-KV paged decode with sinks (sinkattn_decode).  window > 0: sliding window;
     max_sms > 0: the split-KV grid on at most that many SMs.  Returns (out, lse)."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             max_sms=max_sms)
+                                             max_sms=max_sms, wait_limit_us=wait_limit_us)
     _check(load().sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                   _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                   ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(q.device)),
@@ -226,11 +237,11 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, o
 
 
 def decode_splitkv(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None,
-                   lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
+                   lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0, wait_limit_us=0):
     """First decode kernel only (sinkattn_decode_splitkv); follow with decode_merge."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             max_sms=max_sms)
+                                             max_sms=max_sms, wait_limit_us=wait_limit_us)
     _check(load().sinkattn_decode_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                           _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                           ctypes.byref(desc), _ptr(ws), ws.numel(),
@@ -248,7 +259,7 @@ def decode_merge(seq_lens, sinks, out, lse, desc, ws):
 
 def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
             prefix_block_table=None, prefix_lens=None, out=None, lse=None, workspace_buf=None,
-            return_lse=True, window=0, max_sms=0):
+            return_lse=True, window=0, max_sms=0, wait_limit_us=0):
     """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  window > 0:
     sliding window; max_sms > 0: the persistent grid on at most that many SMs.  Returns
     (out, lse)."""
@@ -275,7 +286,8 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
-    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window, max_sms=max_sms)
+    desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window, max_sms=max_sms,
+                      wait_limit_us=wait_limit_us)
     nbytes = prefill_workspace_size(desc)
     ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -283,6 +295,49 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
                                    _ptr(v_pages), _ptr(prefix_block_table), _ptr(prefix_lens),
                                    _ptr(sinks), scale, _ptr(out), _ptr(lse), ctypes.byref(desc),
                                    _ptr(ws), ws.numel(), _stream(dev)), "sinkattn_prefill")
+    return out, lse
+
+
+def prefill_fp8(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
+                k_scale=None, v_scale=None, prefix_block_table=None, prefix_lens=None, out=None,
+                lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0, wait_limit_us=0):
+    """Chunked prefill over an FP8 E4M3 paged prefix (sinkattn_prefill_fp8): k_pages / v_pages
+    uint8 (or float8_e4m3fn) [num_pages, Hkv, 16, D] codes, k_scale / v_scale float32 [Hkv] or
+    None (1); the new tokens' q, k, v bf16.  Returns (out, lse)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(k, "k", torch.bfloat16, dev, 3)
+    _need(v, "v", torch.bfloat16, dev, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D):
+        raise ValueError("k / v must be [T, Hkv, D] matching q")
+    if k_pages is None or v_pages is None or prefix_block_table is None or prefix_lens is None:
+        raise ValueError("prefill_fp8 needs the FP8 prefix pages, block table and lengths")
+    k_pages, v_pages = _codes(k_pages), _codes(v_pages)
+    _need(k_pages, "k_pages", torch.uint8, dev, 4)
+    _need(v_pages, "v_pages", torch.uint8, dev, 4)
+    _need(prefix_block_table, "prefix_block_table", torch.int32, dev, 2)
+    _need(prefix_lens, "prefix_lens", torch.int32, dev, 1)
+    _scales(k_scale, v_scale, Hkv, dev)
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, 1)
+    n = cu_seqlens.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
+    desc = paged_desc(n, Hq, Hkv, D, k_pages.shape[0], prefix_block_table.shape[1], window=window,
+                      max_sms=max_sms, wait_limit_us=wait_limit_us)
+    ws = workspace_buf if workspace_buf is not None else workspace(prefill_workspace_size(desc), dev,
+                                                                   "prefill")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().sinkattn_prefill_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), T, _ptr(k_pages),
+                                       _ptr(v_pages), _ptr(k_scale), _ptr(v_scale),
+                                       _ptr(prefix_block_table), _ptr(prefix_lens), _ptr(sinks), scale,
+                                       _ptr(out), _ptr(lse), ctypes.byref(desc), _ptr(ws), ws.numel(),
+                                       _stream(dev)), "sinkattn_prefill_fp8")
     return out, lse
 
 
@@ -316,13 +371,14 @@ def _scales(k_scale, v_scale, Hkv, dev):
 
 
 def decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None,
-                  out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
+                  out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0,
+                  wait_limit_us=0):
     """Decode step with its K/V append (sinkattn_decode_append): the new rows k_new / v_new
     [B, Hkv, D] go into the cache at position seq_lens - 1 (seq_lens counts them) and are
     attended in the same pass.  k_pages / v_pages are written in place.  Returns (out, lse)."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             max_sms=max_sms)
+                                             max_sms=max_sms, wait_limit_us=wait_limit_us)
     B, Hkv, D = q.shape[0], k_pages.shape[1], q.shape[2]
     for name, t in (("k_new", k_new), ("v_new", v_new)):
         _need(t, name, torch.bfloat16, q.device, 3)
@@ -336,15 +392,50 @@ def decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, sink
     return out, lse
 
 
+def rope_desc(base: float, factor: float = 1.0, original_context: int = 4096,
+              beta_fast: float = 32.0, beta_slow: float = 1.0) -> RopeDesc:
+    """Rotary-embedding parameters (NeoX layout, YaRN scaling; factor 1 = plain RoPE)."""
+    return RopeDesc(float(base), float(factor), int(original_context), float(beta_fast),
+                    float(beta_slow))
+
+
+def decode_append_rope(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, sinks=None,
+                       scale=None, rope: Optional[RopeDesc] = None, out=None, lse=None,
+                       workspace_buf=None, return_lse=True, window=0, max_sms=0,
+                       wait_limit_us=0):
+    """Decode step with rotary embedding and K/V append (sinkattn_decode_append_rope): q and
+    k_new (not yet rotated) are rotated at position seq_lens - 1, the rotated key and v_new go
+    into the cache there, and the rotated query attends.  rope: a RopeDesc (rope_desc(...)).
+    k_pages / v_pages are written in place.  Returns (out, lse)."""
+    if not isinstance(rope, RopeDesc):
+        raise TypeError("rope must be a RopeDesc (see rope_desc)")
+    desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
+                                             scale, out, lse, workspace_buf, return_lse, window,
+                                             max_sms=max_sms, wait_limit_us=wait_limit_us)
+    B, Hkv, D = q.shape[0], k_pages.shape[1], q.shape[2]
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, torch.bfloat16, q.device, 3)
+        if tuple(t.shape) != (B, Hkv, D):
+            raise ValueError(f"{name} must be [B, Hkv, D] = {(B, Hkv, D)}")
+    _check(load().sinkattn_decode_append_rope(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages),
+                                              _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                              _ptr(sinks), scale, ctypes.byref(rope), _ptr(out),
+                                              _ptr(lse), ctypes.byref(desc), _ptr(ws), ws.numel(),
+                                              _stream(q.device)), "sinkattn_decode_append_rope")
+    return out, lse
+
+
 def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None, scale=None,
-               out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0):
+               out=None, lse=None, workspace_buf=None, return_lse=True, window=0, max_sms=0,
+               wait_limit_us=0):
     """Split-KV paged decode over an FP8 E4M3 cache (sinkattn_decode_fp8).  k_pages / v_pages:
     uint8 (or float8_e4m3fn) [num_pages, Hkv, 16, D] codes; k_scale / v_scale: float32 [Hkv]
     per-KV-head scales or None (1).  Returns (out, lse)."""
     k_pages, v_pages = _codes(k_pages), _codes(v_pages)
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             kv_dtype=torch.uint8, max_sms=max_sms)
+                                             kv_dtype=torch.uint8, max_sms=max_sms,
+                                             wait_limit_us=wait_limit_us)
     _scales(k_scale, v_scale, k_pages.shape[1], q.device)
     _check(load().sinkattn_decode_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                       _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(sinks),
@@ -355,12 +446,13 @@ def decode_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sin
 
 def decode_fp8_splitkv(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, sinks=None,
                        scale=None, out=None, lse=None, workspace_buf=None, return_lse=True, window=0,
-                       max_sms=0):
+                       max_sms=0, wait_limit_us=0):
     """First kernel of decode_fp8 only (sinkattn_decode_fp8_splitkv); follow with decode_merge."""
     k_pages, v_pages = _codes(k_pages), _codes(v_pages)
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             kv_dtype=torch.uint8, max_sms=max_sms)
+                                             kv_dtype=torch.uint8, max_sms=max_sms,
+                                             wait_limit_us=wait_limit_us)
     _scales(k_scale, v_scale, k_pages.shape[1], q.device)
     _check(load().sinkattn_decode_fp8_splitkv(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(k_scale),
                                               _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),

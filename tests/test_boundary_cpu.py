@@ -56,7 +56,7 @@ def _desc(sa, **kw):
     (dict(head_dim=96), 2), (dict(num_qo_heads=12, num_kv_heads=4), 2),   # G = 3
     (dict(num_qo_heads=9), 1), (dict(num_pages=0), 1), (dict(max_pages_per_seq=0), 1),
     (dict(num_kv_heads=0), 1), (dict(num_qo_heads=64, num_kv_heads=2), 2),  # G = 32
-    (dict(max_sms=-1), 1),
+    (dict(max_sms=-1), 1), (dict(wait_limit_us=-1), 1),
 ])
 def test_decode_workspace_size_rejects(sa, bad, code):
     n = ctypes.c_size_t()
@@ -143,6 +143,30 @@ def test_desc_layout_matches_the_header(sa):
     fields = re.findall(r"int32_t\s+(\w+)\s*;", body)
     assert [f for f, _ in sa.PagedDesc._fields_] == fields
     assert ctypes.sizeof(sa.PagedDesc) == 4 * len(fields)
+
+
+def test_rope_desc_layout_matches_the_header(sa):
+    """The binding's rotary-parameter struct has the header's fields, in order and type."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct sinkattn_rope_desc \{(.*?)\} sinkattn_rope_desc;", text,
+                     flags=re.S).group(1)
+    fields = re.findall(r"(double|int32_t)\s+(\w+)\s*;", body)
+    ctype = {"double": ctypes.c_double, "int32_t": ctypes.c_int32}
+    assert [(f, t) for f, t in sa.RopeDesc._fields_] == [(n, ctype[t]) for t, n in fields]
+
+
+def test_rope_decode_rejects_bad_parameters_before_cuda(sa):
+    """Parameter checks of the rotary decode come before anything touches the device."""
+    d = _desc(sa)
+    good = sa.rope_desc(150000.0, 32.0)
+    lib = sa.load()
+    for rope in (sa.rope_desc(150000.0, 0.5), sa.rope_desc(1.0, 32.0), sa.rope_desc(150000.0, 32.0, 0),
+                 sa.rope_desc(150000.0, 32.0, 4096, 1.0, 1.0), None):
+        rc = lib.sinkattn_decode_append_rope(16, 16, 16, 16, 16, 16, 16, None, ctypes.c_float(1.0),
+                                             None if rope is None else ctypes.byref(rope), 16, None,
+                                             ctypes.byref(d), 256, 1 << 20, None)
+        assert rc == sa.ERR_INVALID_ARG, rc
+    assert good.factor == 32.0
 
 
 def test_header_compiles_as_c99_and_cpp17(tmp_path):

@@ -129,3 +129,67 @@ def test_gptoss_prefill_window_128_full_config_sampled(sa, oracle_mod, cuda_dev)
     ro, rl = _oracle_prefill(oracle_mod, p, 128, select=sel)
     check_out(out, ro, mask=sel)
     check_lse(lse, rl, mask=sel)
+
+
+# ---- the one-launch plan of short sliding windows (W <= 2032: a CTA per (sequence, KV head),
+# its four warps splitting the visible pages, merged in shared memory) against the two-stage
+# split-KV plan (sinkattn_decode_splitkv + sinkattn_decode_merge) and the oracle
+@pytest.mark.parametrize("D,window", [(64, 16), (64, 128), (128, 128), (64, 2032), (128, 1000)])
+def test_window_one_launch_matches_split_kv_plan(sa, oracle_mod, cuda_dev, D, window):
+    lens = [0, 1, 15, 16, 17, 127, 128, 129, 2049, 5000]
+    Hkv = 2
+    w = inputs.make_decode(lens, len(lens), Hkv * (8 if D == 64 else 16), Hkv, D, seed=90 + window,
+                           sinks=True)
+    c = w.cache
+    dev = cuda_dev
+    q, kp, vp, bt, sl, sk = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
+                             c.lens.to(dev), w.sinks.to(dev))
+    out, lse = sa.decode(q, kp, vp, bt, sl, sk, w.scale, window=window)
+    o2, l2, ws, desc = sa.decode_splitkv(q, kp, vp, bt, sl, sk, w.scale, window=window)
+    sa.decode_merge(sl, sk, o2, l2, desc, ws)
+    torch.cuda.synchronize()
+    assert sa.get_status(sa.workspace(0, dev)) == 0
+    ro, rl = _oracle_decode(oracle_mod, w, window)
+    check_out(out, ro, what="one-launch window decode")
+    check_lse(lse, rl, what="one-launch window lse")
+    check_out(o2, ro, what="split-KV window decode")
+    check_lse(l2, rl, what="split-KV window lse")
+
+
+def test_window_one_launch_independent_of_the_grid(sa, cuda_dev):
+    # each (sequence, KV head) is done by one CTA the same way whatever the grid: bitwise
+    lens = [3, 128, 129, 500, 7000, 64, 1, 0] * 4
+    w = inputs.make_decode(lens, len(lens), 16, 2, 64, seed=95, sinks=True)
+    c = w.cache
+    dev = cuda_dev
+    args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
+            w.sinks.to(dev), w.scale)
+    a_out, a_lse = sa.decode(*args, window=128)
+    b_out, b_lse = sa.decode(*args, window=128, max_sms=3)
+    torch.cuda.synchronize()
+    assert torch.equal(a_out.view(torch.int16), b_out.view(torch.int16))
+    assert torch.equal(a_lse.view(torch.int32), b_lse.view(torch.int32))
+
+
+def test_window_one_launch_bad_page_and_length(sa, oracle_mod, cuda_dev):
+    lens = [40, 300, 17, 1000]
+    w = inputs.make_decode(lens, 4, 16, 2, 64, seed=96, sinks=True)
+    c = w.cache
+    dev = cuda_dev
+    bt = c.block_table.clone()
+    bt[1, 18] = c.num_pages + 3          # inside sequence 1's window of 128 keys
+    sl = c.lens.clone()
+    sl[3] = c.block_table.shape[1] * 16 + 5  # beyond the table
+    ws = sa.workspace(0, dev)
+    sa.get_status(ws)
+    out, lse = sa.decode(w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), bt.to(dev), sl.to(dev),
+                         w.sinks.to(dev), w.scale, window=128)
+    torch.cuda.synchronize()
+    st = sa.get_status(ws)
+    assert st & sa.STATUS_BAD_PAGE and st & sa.STATUS_BAD_LENGTH
+    # the untouched sequences stay exact
+    ro, rl = _oracle_decode(oracle_mod, w, 128)
+    keep = np.zeros((4, 16), dtype=bool)
+    keep[[0, 2]] = True
+    check_out(out, ro, mask=keep, what="sequences beside a bad page")
+    check_lse(lse, rl, mask=keep)
