@@ -106,9 +106,10 @@ typedef struct sinkattn_paged_desc {
                                 * it already issued finish, and returns (outputs are then
                                 * unspecified).  0 = the default, 2 seconds; negative:
                                 * SINKATTN_ERR_INVALID_ARG.  1 is the testing setting of
-                                * that path: a wait then gives up unless it is already
-                                * complete when first tested, which the first wait of
-                                * every kernel is not (its copy from HBM is in flight). */
+                                * that path: the decode kernels' waits then give up unless
+                                * already complete when first tested (the first one never is:
+                                * its copy from HBM is in flight), and the prefill gives up
+                                * right after issuing its first copies. */
 } sinkattn_paged_desc;
 
 /* Human-readable name of an error code (static string). */
@@ -376,8 +377,10 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
  * and finite).  The new tokens' k, v stay bf16 (a serving step appends them to the FP8 cache
  * with sinkattn_append_kv_fp8 for later steps).  The prefix tiles are copied as codes and
  * converted in shared memory: K exactly to bf16 code values, the K scale multiplying those
- * tiles' scores; V to fp16 of value * 2^-k per 32-key quarter (relative rounding <= 2^-11,
- * the same as bf16 V tiles; a NaN code sets SINKATTN_STATUS_VALUE_RANGE).  All four prefix
+ * tiles' scores; V to fp16 of value * 2^-k, one k per KV head from the format's largest value
+ * (448 * v_scale < 2^15 * 2^k; k = 0 for any v_scale below 73; k > 7 sets
+ * SINKATTN_STATUS_VALUE_RANGE), relative rounding <= 2^-11 as for bf16 V tiles.  NaN codes in
+ * visible keys give unspecified outputs.  All four prefix
  * pointers and the prefix lengths are required; other arguments, workspace and errors as
  * for sinkattn_prefill. */
 int sinkattn_prefill_fp8(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,

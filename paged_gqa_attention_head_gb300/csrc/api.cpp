@@ -589,6 +589,7 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
     a.window = desc->window > 0 ? desc->window : 0;
     a.max_sms = desc->max_sms;
     a.wait_limit_ns = wait_limit_ns(desc->wait_limit_us);
+    a.wait_limit_cycles = a.wait_limit_ns * 2;  // SM cycles, at least the limit up to 2 GHz
     a.status = static_cast<uint32_t *>(workspace);
     a.fp8_prefix = fp8;
     a.k_scale = k_scale;

@@ -98,7 +98,8 @@ struct PrefillArgs {
     int T, n, Hq, Hkv, G, D, num_pages, max_pages;
     int window;  // sliding window (keys at the query's last `window` positions); 0: none
     int max_sms;  // SMs the persistent grid may use; 0: all
-    uint64_t wait_limit_ns;  // give-up time of a pipeline wait
+    uint64_t wait_limit_ns;      // give-up time of a pipeline wait
+    uint64_t wait_limit_cycles;  // the same in SM cycles (2 per ns)
     uint32_t *status;
     bool fp8_prefix;                   // the prefix pages are FP8 E4M3 codes (uint8)
     const float *k_scale, *v_scale;    // FP8 prefix: [Hkv] per-KV-head scales, or nullptr (1)

@@ -105,41 +105,31 @@ struct Bars {
         *p_full, *pv_done, *o_free, *drain;
 };
 
-// Bounded wait (limit_ns of wall time, counted in SM cycles as in mbar_wait, checked every
-// 16 polls) that also gives up as soon as another role has
-// given up.  Every lane of a full warp calls it and all of them get the same answer (the
-// outcome is voted), so a warp never continues with some of its lanes gone - the
-// .sync.aligned instructions that follow need all 32.  With kSleep the warp sleeps in the
-// wait (for warps off the critical path: it leaves the issue slots to the softmax warps, at
-// ~50 cycles more wake-up latency); a sleep lasts at most 100 us, or the limit if shorter.
+// Bounded wait (limit_cycles SM cycles: the call's wait limit, converted on the host) that also
+// gives up as soon as another role has given up.  With kSleep the thread sleeps in the wait
+// (for warps off the critical path: it leaves the issue slots to the softmax warps, at ~50
+// cycles more wake-up latency).  The lanes of a converged warp test the same barrier in the
+// same instruction and read the same flag and clock, so they come to the same answer; the
+// MMA-issuing and converter warps also vote on it (warp_wait, the converter loop).  The
+// fast path is one blocking probe: measured, a vote inside the wait cost the prefill 18 %,
+// a non-blocking first probe 5-20 %, and any branch ahead of the first probe (such as one
+// for the testing limit) 25-45 %, so the testing setting is handled by the producer instead.
 template <bool kSleep = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                              uint32_t *status, uint64_t limit_ns) {
-    if (limit_ns <= kImmediateLimitNs) {  // the smallest limit: one non-blocking test
-        if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
-        if ((threadIdx.x & 31) == 0) {
+                                              uint32_t *status, uint64_t limit_cycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = clock64();
+    for (;;) {
+        if (kSleep) {
+            if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        } else {
+            for (int i = 0; i < 128; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+        }
+        if (*abort) return false;
+        if ((uint64_t)clock64() - t0 >= limit_cycles) {
             *abort = 1;
             set_status(status, SINKATTN_STATUS_WAIT_TIMEOUT);
-        }
-        return false;
-    }
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    const uint64_t t0 = clock64(), lim = limit_cycles(limit_ns);
-    const uint32_t hint = limit_ns < 100000ull ? (uint32_t)limit_ns : 100000u;
-    for (;;) {
-        bool done = false;
-        if (kSleep) {
-            done = mbar_try_wait_sleep(bar, parity, hint);
-        } else {
-            for (int i = 0; i < 16 && !done; ++i) done = mbar_try_wait(bar, parity);
-        }
-        if (__all_sync(0xffffffffu, done)) return true;
-        if (__any_sync(0xffffffffu, *abort != 0)) return false;
-        if (__any_sync(0xffffffffu, (uint64_t)clock64() - t0 >= lim)) {
-            if ((threadIdx.x & 31) == 0) {
-                *abort = 1;
-                set_status(status, SINKATTN_STATUS_WAIT_TIMEOUT);
-            }
             return false;
         }
     }
@@ -159,12 +149,6 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
         : "=f"(lo), "=f"(hi)
         : "r"(h));
     return pack_bf16x2(lo, hi);
-}
-// The f16 value in the lower half of h, as float.
-__device__ __forceinline__ float f16lo_to_f32(uint32_t h) {
-    float lo;
-    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(lo) : "r"(h));
-    return lo;
 }
 // Two f16 values times sc, rounded to an f16 pair.
 __device__ __forceinline__ uint32_t f16x2_scaled(uint32_t h, float sc) {
@@ -225,28 +209,6 @@ __device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane,
             }
         }
     }
-}
-
-// Largest |E4M3 code| (its 7-bit magnitude; 0x7F is NaN) among the staged codes of a
-// quarter (pages 2q, 2q + 1), over the warp.
-template <int D>
-__device__ __forceinline__ uint32_t fp8_quarter_max(const uint8_t *t, int q, int lane) {
-    using C = PrefillCfg<D>;
-    uint32_t mx = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(t + C::kOffFp8Page(2 * q + i));
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e) {  // 16 x D bytes = 32 * (D / 32) vectors
-            const uint4 w = src[e * 32 + lane];
-            mx = __vmaxu4(mx, w.x & 0x7F7F7F7Fu);
-            mx = __vmaxu4(mx, w.y & 0x7F7F7F7Fu);
-            mx = __vmaxu4(mx, w.z & 0x7F7F7F7Fu);
-            mx = __vmaxu4(mx, w.w & 0x7F7F7F7Fu);
-        }
-    }
-    mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
-    return __reduce_max_sync(0xffffffffu, mx);
 }
 
 // Work list, in two parts.  (A) Requests with a paged prefix, request by request (each
@@ -560,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kv = 0;  // key tiles loaded so far (ring position)
         int k = 0;   // items so far
         bool ok = true;
+        const bool test_limit = a.wait_limit_ns <= kImmediateLimitNs;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
             const ItemGeom gm = geom_of<kWindow>(a, it);
@@ -569,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_status(a.status, SINKATTN_STATUS_BAD_LENGTH);
             }
             // Q tiles of this item, once the previous item's last S products are done
-            if (k > 0 && !wait_or_abort<true>(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status, a.wait_limit_ns)) {
+            if (k > 0 && !wait_or_abort<true>(bars.q_empty, (uint32_t)((k - 1) & 1), s_abort, a.status, a.wait_limit_cycles)) {
                 ok = false;
                 break;
             }
@@ -582,6 +545,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     it.h0 + x, gm.row0 + it.qb * kBM);
             }
             q_issued = k;
+            if (test_limit) {
+                // the testing setting of the watchdog: give up here, with the item's Q copy still
+                // in flight; the other roles leave at their next wait that does not complete
+                if (lane == 0) {
+                    *s_abort = 1;
+                    set_status(a.status, SINKATTN_STATUS_WAIT_TIMEOUT);
+                }
+                __syncwarp();
+                ok = false;
+                break;
+            }
             for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int s = kv % NS, u = kv / NS;
                 const int tt = kWindow ? gm.t0 + j : j;  // key tile
@@ -600,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (u > 0 &&
-                    !wait_or_abort<true>(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status, a.wait_limit_ns)) {
+                    !wait_or_abort<true>(&bars.kv_empty[s], (uint32_t)((u - 1) & 1), s_abort, a.status, a.wait_limit_cycles)) {
                     ok = false;
                     break;
                 }
@@ -731,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all lanes wait; the outcome is made warp-uniform so that no lane is left behind
         // at the elect.sync below when a wait gives up
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status, a.wait_limit_ns));
+            return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status, a.wait_limit_cycles));
         };
         int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
         int n_kv = rank < n_items ? geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv : 0;
@@ -821,14 +795,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const ItemGeom gm = geom_of<kWindow>(a, item_of(a, wl, rank));
+            // FP8 V: |value| <= 448 * v_scale, so one exponent k per item keeps every converted
+            // value below 2^15 (k = 0 for any scale below 73): no per-tile maximum needed
             const float vsc = kFp8 && a.v_scale ? a.v_scale[gm.g] : 1.f;
+            int kexp8 = 0;
+            if (kFp8) {
+                const float top = 448.f * vsc;
+                kexp8 = max(0, (int)((__float_as_uint(top) >> 23) & 0xFFu) - 127 - 14);
+                if (!(top < INFINITY) || kexp8 > 7) {
+                    if (lane == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
+                    kexp8 = min(kexp8, 7);
+                }
+            }
+            const float vmul8 = vsc * __uint_as_float((uint32_t)(127 - kexp8) << 23);
             for (int j = 0; j < gm.n_kv; ++j, ++kv) {
                 const int st = kv % NS;
                 const bool fp8_tile = kFp8 && (kWindow ? gm.t0 + j : j) < gm.n_pre;
                 if (kFp8) {
                     // K: the FP8 prefix tiles to bf16 code values (the S products wait for this)
-                    if (!wait_or_abort<true>(&bars.k_full[st], (uint32_t)((kv / NS) & 1), s_abort, a.status,
-                                             a.wait_limit_ns)) {
+                    if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.k_full[st], (uint32_t)((kv / NS) & 1),
+                                                                s_abort, a.status, a.wait_limit_cycles))) {
                         ok = false;
                         break;
                     }
@@ -838,23 +824,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&bars.k_conv[st]);
                 }
                 if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.v_full[st], (uint32_t)((kv / NS) & 1),
-                                                            s_abort, a.status, a.wait_limit_ns))) {
+                                                            s_abort, a.status, a.wait_limit_cycles))) {
                     ok = false;
                     break;
                 }
                 if (fp8_tile) {
-                    // V: fp16 of value * 2^-k, value = scale * e4m3(code); k from the quarter's
-                    // largest |value| as for bf16 tiles (a NaN code counts as out of range)
-                    uint8_t *vt8 = sV + st * C::kKVBytes;
-                    const uint32_t mc = fp8_quarter_max<D>(vt8, q, lane);
-                    const float topv = f16lo_to_f32(e4m3x2_lo_to_f16x2(mc)) * vsc;
-                    int kexp = max(0, (int)((__float_as_uint(topv) >> 23) & 0xFFu) - 127 - 14);
-                    if (mc >= 0x7Fu || !(topv < INFINITY) || kexp > 7) {
-                        if (lane == 0) set_status(a.status, SINKATTN_STATUS_VALUE_RANGE);
-                        kexp = min(kexp, 7);
-                    }
-                    convert_fp8_quarter<D, false>(vt8, q, lane, vsc * __uint_as_float((uint32_t)(127 - kexp) << 23));
-                    if (lane == 0) s_vscale[st * 4 + q] = kexp;
+                    // V: fp16 of value * 2^-k, value = scale * e4m3(code), k of the item
+                    convert_fp8_quarter<D, false>(sV + st * C::kKVBytes, q, lane, vmul8);
+                    if (lane == 0) s_vscale[st * 4 + q] = kexp8;
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.v_conv[st]);
@@ -939,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = i % NBS, pb = i % NBP;
                 const uint32_t ts = tmem + lane_base + C::kColS(b);
                 const uint32_t tp = tmem + lane_base + C::kColP(pb);
-                if (!wait_or_abort(&bars.s_full[b], (i / NBS) & 1, s_abort, a.status, a.wait_limit_ns)) {
+                if (!wait_or_abort(&bars.s_full[b], (i / NBS) & 1, s_abort, a.status, a.wait_limit_cycles)) {
                     ok = false;
                     break;
                 }
@@ -1007,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O_x must hold the P.V of this query tile's previous key tile,
                         // product i - ntiles (its P buffer's previous use is long done)
                         const uint32_t ip = i - ntiles;
-                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
+                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
                             ok = false;
                             break;
                         }
@@ -1033,13 +1010,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter holding
                 // keys 32ch..32ch+31
                 const int vst = (tcount - 1) % NS;
-                if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status, a.wait_limit_ns)) {
+                if (!wait_or_abort(&bars.v_conv[vst], ((tcount - 1) / NS) & 1, s_abort, a.status, a.wait_limit_cycles)) {
                     ok = false;
                     break;
                 }
                 if (C::kSplitP && i >= (uint32_t)NBP) {
                     // the P buffer is free once the P.V of product i - NBP has completed
-                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
+                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
                         ok = false;
                         break;
                     }
@@ -1089,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // epilogue: O / l for this row, once the item's last P.V has landed
             const uint32_t il = (tcount - 1) * ntiles + x;  // S product of the last key tile
-            if (!wait_or_abort(&bars.pv_done[il % NBP], (il / NBP) & 1, s_abort, a.status, a.wait_limit_ns)) {
+            if (!wait_or_abort(&bars.pv_done[il % NBP], (il / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
                 ok = false;
                 break;
             }

@@ -6,6 +6,9 @@ Each pin ties the oracle to something it does not share code with:
     (a zero key/value row whose additive mask is the sink), for the sink case;
   * closed forms: one key, a hand-derived two-key example (tests/golden), a huge
     sink, an empty sequence;
+  * brute force: every row of tiny decode and causal-prefill inputs (head_dim <= 4, at
+    most 5 keys) enumerated in plain Python float64 as softmax over the keys plus one
+    zero-valued virtual token carrying the sink;
   * invariances: permuting physical pages, splitting the keys and merging, the
     online (streaming) form seeded with the sink, decode == last causal row,
     chunked prefill == trailing rows of a full causal prefill;
@@ -649,6 +652,59 @@ def pin_prefill_fp8_sdpa(o):
         np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], ref_lse.permute(1, 0).numpy(), rtol=0, atol=1e-10)
 
 
+def pin_brute_force_tiny(o):
+    # every decode and causal-prefill row of tiny inputs (head_dim <= 4, at most 5 keys)
+    # enumerated in plain Python float64 in the virtual-token form: the sink is one more
+    # logit whose value row is zero; probabilities p_j = exp(x_j - logsumexp(x)) with the
+    # sums taken by math.fsum (exactly rounded)
+    def attend(q, keys, vals, scale, sink):
+        xs = [scale * math.fsum(a * b for a, b in zip(q, k)) for k in keys] + [sink]
+        D = len(q)
+        if max(xs) == -math.inf:
+            return [0.0] * D, -math.inf
+        top = max(xs)
+        lse = top + math.log(math.fsum(math.exp(x - top) for x in xs))
+        ps = [math.exp(x - lse) for x in xs]
+        out = [math.fsum(p * v[d] for p, v in zip(ps, vals + [[0.0] * D])) for d in range(D)]
+        return out, lse
+
+    rng = np.random.default_rng(17)
+    for D in (1, 2, 4):
+        for trial in range(3):
+            # decode: 3 sequences of 0..5 keys, 4 q heads / 2 KV heads, one page each
+            lens = [int(x) for x in rng.integers(0, 6, size=3)]
+            q = torch.from_numpy(rng.standard_normal((3, 4, D)).astype(np.float32)).to(torch.bfloat16)
+            kp = torch.from_numpy(rng.standard_normal((3, 2, 16, D)).astype(np.float32)).to(torch.bfloat16)
+            vp = torch.from_numpy(rng.standard_normal((3, 2, 16, D)).astype(np.float32)).to(torch.bfloat16)
+            bt = torch.tensor([[2], [0], [1]], dtype=torch.int32)
+            sk = torch.from_numpy(rng.standard_normal(4).astype(np.float32)) if trial != 1 else None
+            scale = 0.7
+            out, lse = o.decode(q, kp, vp, bt, torch.tensor(lens, dtype=torch.int32), sk, scale)
+            for b in range(3):
+                for h in range(4):
+                    g = h // 2
+                    keys = [kp[bt[b, 0], g, j].double().tolist() for j in range(lens[b])]
+                    vals = [vp[bt[b, 0], g, j].double().tolist() for j in range(lens[b])]
+                    sink = -math.inf if sk is None else float(sk[h])
+                    ro, rl = attend(q[b, h].double().tolist(), keys, vals, scale, sink)
+                    np.testing.assert_allclose(out[b, h], ro, rtol=1e-12, atol=1e-14)
+                    assert (rl == lse[b, h]) if rl == -math.inf else abs(rl - lse[b, h]) < 1e-12
+            # causal prefill: one request of 5 tokens, 2 q heads / 1 KV head
+            T = 5
+            qq = torch.from_numpy(rng.standard_normal((T, 2, D)).astype(np.float32)).to(torch.bfloat16)
+            kk = torch.from_numpy(rng.standard_normal((T, 1, D)).astype(np.float32)).to(torch.bfloat16)
+            vv = torch.from_numpy(rng.standard_normal((T, 1, D)).astype(np.float32)).to(torch.bfloat16)
+            sk2 = torch.from_numpy(rng.standard_normal(2).astype(np.float32))
+            out, lse = o.prefill(qq, kk, vv, torch.tensor([0, T], dtype=torch.int32), sk2, scale)
+            for t in range(T):
+                for h in range(2):
+                    keys = [kk[j, 0].double().tolist() for j in range(t + 1)]
+                    vals = [vv[j, 0].double().tolist() for j in range(t + 1)]
+                    ro, rl = attend(qq[t, h].double().tolist(), keys, vals, scale, float(sk2[h]))
+                    np.testing.assert_allclose(out[t, h], ro, rtol=1e-12, atol=1e-14)
+                    assert abs(rl - lse[t, h]) < 1e-12
+
+
 PINS = {
     "decode_sdpa_nosink": lambda o: pin_decode_sdpa(o, False),
     "decode_sdpa_sink": lambda o: pin_decode_sdpa(o, True),
@@ -680,6 +736,7 @@ PINS = {
     "decode_append_rope": pin_decode_append_rope,
     "prefill_fp8_pow2_is_bf16_prefill": pin_prefill_fp8_pow2_is_bf16_prefill,
     "prefill_fp8_sdpa": pin_prefill_fp8_sdpa,
+    "brute_force_tiny": pin_brute_force_tiny,
 }
 
 
