@@ -43,6 +43,8 @@ def _load():
         lib.oracle_decode.restype = I
         lib.oracle_prefill.argtypes = [P, P, P, P, I, P, P, P, P, I64, I, P, D, I, I, I, I, I, P, P, P]
         lib.oracle_prefill.restype = I
+        lib.oracle_prefill_noncausal.argtypes = [P, P, P, P, I, P, D, I, I, I, P, P, P]
+        lib.oracle_prefill_noncausal.restype = I
         lib.oracle_append_kv.argtypes = [P, P, P, I, P, P, I, I64, I, I, I, P, P]
         lib.oracle_append_kv.restype = I
         lib.oracle_partial.argtypes = [P, P, P, I, D, I64, I64, P, P, P]
@@ -165,6 +167,25 @@ def prefill(q, k, v, cu_seqlens, sinks, scale: float, k_pages=None, v_pages=None
                             page_size, int(window), _ptr(sel), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_prefill rejected its inputs ({rc})")
+    return out, lse
+
+
+def prefill_noncausal(q, k, v, cu_seqlens, sinks, scale: float, select: Optional[np.ndarray] = None):
+    """Non-causal ragged prefill without a KV cache: query t of sequence i sees every token
+    of sequence i.  Returns (out [T,Hq,D], lse [T,Hq])."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    T, Hq, D = qb.shape
+    Hkv = kb.shape[1]
+    cu = _i32(cu_seqlens)
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    sel = None if select is None else np.ascontiguousarray(select, dtype=np.uint8)
+    rc = lib.oracle_prefill_noncausal(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), cu.shape[0] - 1,
+                                      _ptr(_f32(sinks)), float(scale), Hq, Hkv, D, _ptr(sel),
+                                      _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_noncausal rejected its inputs ({rc})")
     return out, lse
 
 
@@ -385,7 +406,7 @@ class using_library:
                      "oracle_merge", "oracle_online", "oracle_max_threads", "oracle_decode_fp8",
                      "oracle_append_kv_fp8", "oracle_e4m3_codes", "oracle_e4m3_values",
                      "oracle_rope_freqs", "oracle_rope", "oracle_bf16_round_array",
-                     "oracle_prefill_fp8"):
+                     "oracle_prefill_fp8", "oracle_prefill_noncausal"):
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = lib

@@ -25,7 +25,8 @@
  *
  *   J is: decode - every cached token [0, L_b); causal prefill - tokens 0..t of the
  *   same sequence; chunked prefill - all P_i prefix tokens plus new tokens 0..t,
- *   the new token t sitting at absolute position P_i + t.
+ *   the new token t sitting at absolute position P_i + t; non-causal prefill (an
+ *   encoder without a KV cache) - every token of the same sequence.
  *
  *   Sliding window W > 0 (gptoss.md section 4: even layers attend a local window of
  *   128 positions, odd layers the full causal range; the window is passed per call to
@@ -230,6 +231,60 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         free(s);
     }
     free(seq_of);
+    return bad ? -2 : 0;
+}
+
+/*
+ * Non-causal prefill over packed ragged sequences, without a KV cache: the attention of
+ * an embedding (encoder) model served through ragged kernels with no KV cache ("Fast
+ * embeddings on GPUs", the section on attention kernels).  The pages give no mask for
+ * it; the reading here is the plain bidirectional one: query t of sequence i sees
+ * every token of sequence i, before and after it, and nothing outside it.
+ *   q [T, Hq, D]; k, v [T, Hkv, D]; cu_seqlens [n + 1]; out [T, Hq, D]; lse [T, Hq].
+ */
+int oracle_prefill_noncausal(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const int32_t *cu_seqlens, int n, const float *sinks, double scale,
+                             int Hq, int Hkv, int D, const uint8_t *select, double *out,
+                             double *lse) {
+    if (Hq % Hkv) return -1;
+    for (int i = 0; i < n; ++i)
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) return -1;
+    const int G = Hq / Hkv;
+    int bad = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t first = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
+        if (len == 0) continue;
+        /* the same key set for every query of the sequence */
+        const uint16_t **krow = malloc(sizeof(*krow) * (size_t)len * Hkv);
+        const uint16_t **vrow = malloc(sizeof(*vrow) * (size_t)len * Hkv);
+        if (!krow || !vrow) {
+            free(krow);
+            free(vrow);
+            return -2;
+        }
+        for (int g = 0; g < Hkv; ++g)
+            for (int64_t j = 0; j < len; ++j) {
+                krow[g * len + j] = k + ((first + j) * Hkv + g) * D;
+                vrow[g * len + j] = v + ((first + j) * Hkv + g) * D;
+            }
+#pragma omp parallel for schedule(dynamic, 4)
+        for (int64_t e = 0; e < len * Hq; ++e) {
+            const int64_t th = first * Hq + e; /* (token, head) pair */
+            if (select && !select[th]) continue;
+            const int h = (int)(e % Hq);
+            double *s = malloc(sizeof(double) * (size_t)len);
+            if (!s) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            attend(q + th * D, D, scale, sink_of(sinks, h), len, krow + (h / G) * len,
+                   vrow + (h / G) * len, s, out + th * D, lse + th);
+            free(s);
+        }
+        free(krow);
+        free(vrow);
+    }
     return bad ? -2 : 0;
 }
 

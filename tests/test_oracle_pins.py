@@ -653,7 +653,7 @@ def pin_prefill_fp8_sdpa(o):
 
 
 def pin_brute_force_tiny(o):
-    # every decode and causal-prefill row of tiny inputs (head_dim <= 4, at most 5 keys)
+    # every decode, causal-prefill and non-causal-prefill row of tiny inputs (head_dim <= 4, at most 5 keys)
     # enumerated in plain Python float64 in the virtual-token form: the sink is one more
     # logit whose value row is zero; probabilities p_j = exp(x_j - logsumexp(x)) with the
     # sums taken by math.fsum (exactly rounded)
@@ -703,6 +703,57 @@ def pin_brute_force_tiny(o):
                     ro, rl = attend(qq[t, h].double().tolist(), keys, vals, scale, float(sk2[h]))
                     np.testing.assert_allclose(out[t, h], ro, rtol=1e-12, atol=1e-14)
                     assert abs(rl - lse[t, h]) < 1e-12
+            # non-causal prefill of the same request: every row sees all 5 keys
+            out, lse = o.prefill_noncausal(qq, kk, vv, torch.tensor([0, T], dtype=torch.int32), sk2, scale)
+            keys = [kk[j, 0].double().tolist() for j in range(T)]
+            vals = [vv[j, 0].double().tolist() for j in range(T)]
+            for t in range(T):
+                for h in range(2):
+                    ro, rl = attend(qq[t, h].double().tolist(), keys, vals, scale, float(sk2[h]))
+                    np.testing.assert_allclose(out[t, h], ro, rtol=1e-12, atol=1e-14)
+                    assert abs(rl - lse[t, h]) < 1e-12
+
+
+def pin_noncausal_sdpa(o):
+    # every query of a sequence sees all of its tokens: SDPA with no mask beyond the
+    # sequence boundary, with sinks and without
+    new = [5, 33, 1, 20]
+    for sinks_on in (True, False):
+        w = inputs.make_prefill(new, 8, 2, 64, seed=12, sinks=sinks_on)
+        out, lse = o.prefill_noncausal(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale)
+        cu = w.cu_seqlens.tolist()
+        for i in range(len(new)):
+            q = w.q[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+            k = w.k[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+            v = w.v[cu[i]:cu[i + 1]].double().permute(1, 0, 2)
+            ro, rl = sdpa_with_sink(q, k, v, w.scale, w.sinks)
+            np.testing.assert_allclose(out[cu[i]:cu[i + 1]], ro.permute(1, 0, 2).numpy(), rtol=RTOL, atol=ATOL)
+            np.testing.assert_allclose(lse[cu[i]:cu[i + 1]], rl.T.numpy(), rtol=RTOL, atol=ATOL)
+
+
+def pin_noncausal_vs_causal_and_permutation(o):
+    # (a) the last query of a sequence sees the same keys either way, so its row equals the
+    # causal prefill's; (b) permuting a sequence's key/value rows together leaves every
+    # output unchanged (the key set is the whole sequence), while the queries' outputs
+    # move with the queries
+    new = [40, 17, 1]
+    w = inputs.make_prefill(new, 8, 2, 64, seed=13, sinks=True)
+    out, lse = o.prefill_noncausal(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale)
+    cout, clse = o.prefill(w.q, w.k, w.v, w.cu_seqlens, w.sinks, w.scale)
+    cu = w.cu_seqlens.tolist()
+    for i in range(len(new)):
+        t = cu[i + 1] - 1
+        np.testing.assert_allclose(out[t], cout[t], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[t], clse[t], rtol=1e-12, atol=1e-14)
+    assert not np.allclose(out[cu[0]], cout[cu[0]], rtol=1e-3, atol=1e-3)  # first row differs
+    perm = torch.arange(w.q.shape[0])
+    perm[cu[0]:cu[1]] = cu[0] + torch.randperm(new[0], generator=torch.Generator().manual_seed(1))
+    pout, plse = o.prefill_noncausal(w.q, w.k[perm], w.v[perm], w.cu_seqlens, w.sinks, w.scale)
+    np.testing.assert_allclose(pout, out, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(plse, lse, rtol=1e-12, atol=1e-14)
+    qout, qlse = o.prefill_noncausal(w.q[perm], w.k, w.v, w.cu_seqlens, w.sinks, w.scale)
+    np.testing.assert_allclose(qout, out[perm.numpy()], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(qlse, lse[perm.numpy()], rtol=1e-12, atol=1e-14)
 
 
 PINS = {
@@ -737,6 +788,8 @@ PINS = {
     "prefill_fp8_pow2_is_bf16_prefill": pin_prefill_fp8_pow2_is_bf16_prefill,
     "prefill_fp8_sdpa": pin_prefill_fp8_sdpa,
     "brute_force_tiny": pin_brute_force_tiny,
+    "noncausal_sdpa": pin_noncausal_sdpa,
+    "noncausal_vs_causal_and_permutation": pin_noncausal_vs_causal_and_permutation,
 }
 
 
@@ -827,6 +880,12 @@ MUTATIONS = [
      "const int64_t nn = (tl + 2 <= cu_seqlens[i + 1] - cu_seqlens[i] ? tl + 2 : tl + 1) - n0;"),
     ("fp8 prefill window ignored in the prefix", "const int64_t np = lo < Pi ? Pi - lo : 0;",
      "const int64_t np = Pi;"),
+    ("non-causal prefill masks the keys after the query", "len, krow + (h / G) * len",
+     "e / Hq + 1, krow + (h / G) * len"),
+    ("non-causal prefill GQA head taken modulo", "krow + (h / G) * len", "krow + (h % Hkv) * len"),
+    ("non-causal prefill drops the sink", "sink_of(sinks, h), len,", "-INFINITY, len,"),
+    ("non-causal prefill reads keys one row late", "krow[g * len + j] = k + ((first + j) * Hkv + g) * D;",
+     "krow[g * len + j] = k + ((first + j + 1 < cu_seqlens[n] ? first + j + 1 : first + j) * Hkv + g) * D;"),
     ("append writes the next slot",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)(pos % P));",
      "uint16_t *kd = (uint16_t *)page_row(k_pages, pg, Hkv, P, D, g, (int)((pos + 1) % P));"),
