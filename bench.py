@@ -672,6 +672,21 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
                      "traffic": None if window else traffic_for("prefill_kernel", name), **st}
         if window:
             rows[key]["window"] = window
+    # an embedding model's batch through the non-causal ragged prefill (no KV cache)
+    p = inputs.make_workload("encoder_ragged", seed=0)
+    pargs, _ = prefill_device_args(p, dev)
+    f = lambda: sa.prefill_noncausal(*pargs)  # noqa: E731
+    for _ in range(3):
+        f()
+    st = repeat_stats(torch, f, stream, flush=flush)
+    flops = p.noncausal_flops()
+    tf = flops / (st["median_ms"] * 1e-3) / 1e12
+    rows["encoder_noncausal"] = {"ms": st["median_ms"], "TFLOP/s": round(tf, 1),
+                                 "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": flops,
+                                 "peak_source": f"{peak_src} bf16_tflops (burst)",
+                                 "workload": "encoder_ragged: 2 x 4096 + 12 x 512 + 32 x 128 tokens, "
+                                             "16 / 8 heads, head_dim 128, no sinks", **st}
+    del pargs
     # the long-context chunked prefill over an FP8 E4M3 prefix cache (the same FLOP)
     p = inputs.make_workload("longctx_chunked_fp8", seed=0)
     c = p.prefix

@@ -371,6 +371,24 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
                      const sinkattn_paged_desc *desc, void *workspace, size_t ws_bytes,
                      sinkattn_stream_t stream);
 
+/* Non-causal prefill over packed ragged sequences, without a KV cache: the attention of an
+ * embedding (encoder) model served through ragged kernels that instantiate no KV cache
+ * ("Fast embeddings on GPUs", section on attention kernels).  The pages give no mask for it;
+ * this is the plain bidirectional reading: query t of request i attends every token of
+ * request i (cu_seqlens[i] <= j < cu_seqlens[i+1]), before and after it, and nothing else.
+ * The same tcgen05 kernel as sinkattn_prefill, with the diagonal mask replaced by the
+ * request's end; sinks, fp16 P.V and SINKATTN_STATUS_VALUE_RANGE as there.
+ *
+ * q, k, v, cu_seqlens, sinks, scale, out, lse: as for sinkattn_prefill (no prefix)
+ * desc:       num_seqs, heads, head_dim, page_size; num_pages and max_pages_per_seq are
+ *             ignored; window must be <= 0 (SINKATTN_ERR_INVALID_ARG otherwise)
+ * workspace:  at least sinkattn_prefill_workspace_size bytes (status header only)
+ * Errors as for sinkattn_prefill. */
+int sinkattn_prefill_noncausal(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int32_t total_tokens, const float *sinks, float scale, void *out,
+                               float *lse, const sinkattn_paged_desc *desc, void *workspace,
+                               size_t ws_bytes, sinkattn_stream_t stream);
+
 /* Chunked prefill over an FP8 E4M3 paged prefix: sinkattn_prefill with the prefix pages
  * in the FP8 cache convention above (uint8 codes [num_pages, Hkv, 16, D], value =
  * scale[g] * e4m3(code); k_scale / v_scale fp32 [Hkv] on the device, NULL = 1, positive

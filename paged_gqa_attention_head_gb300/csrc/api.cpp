@@ -334,7 +334,7 @@ const char *sinkattn_error_string(int code) {
     }
 }
 
-int sinkattn_version(void) { return 10100; }
+int sinkattn_version(void) { return 10200; }
 
 int sinkattn_decode_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes) {
     if (!bytes) return SINKATTN_ERR_INVALID_ARG;
@@ -530,9 +530,10 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
                    const int32_t *prefix_block_table, const int32_t *prefix_lens, const float *sinks,
                    float scale, void *out, float *lse, const sinkattn_paged_desc *desc, void *workspace,
                    size_t ws_bytes, bool fp8, const float *k_scale, const float *v_scale,
-                   sinkattn_stream_t stream) {
+                   bool causal, sinkattn_stream_t stream) {
     int rc = check_heads(desc);
     if (rc) return rc;
+    if (!causal && desc->window > 0) return SINKATTN_ERR_INVALID_ARG;
     if (total_tokens < 0) return SINKATTN_ERR_INVALID_ARG;
     if (desc->num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;  // no tokens: a no-op
     if (!(scale > 0.f) || !(scale < INFINITY)) return SINKATTN_ERR_INVALID_ARG;
@@ -592,6 +593,7 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
     a.wait_limit_cycles = a.wait_limit_ns * 2;  // SM cycles, at least the limit up to 2 GHz
     a.status = static_cast<uint32_t *>(workspace);
     a.fp8_prefix = fp8;
+    a.causal = causal;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);
@@ -608,7 +610,16 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
                      sinkattn_stream_t stream) {
     return prefill_common(q, k, v, cu_seqlens, total_tokens, k_pages, v_pages, prefix_block_table,
                           prefix_lens, sinks, scale, out, lse, desc, workspace, ws_bytes, false, nullptr,
-                          nullptr, stream);
+                          nullptr, true, stream);
+}
+
+int sinkattn_prefill_noncausal(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int32_t total_tokens, const float *sinks, float scale, void *out,
+                               float *lse, const sinkattn_paged_desc *desc, void *workspace,
+                               size_t ws_bytes, sinkattn_stream_t stream) {
+    return prefill_common(q, k, v, cu_seqlens, total_tokens, nullptr, nullptr, nullptr, nullptr, sinks,
+                          scale, out, lse, desc, workspace, ws_bytes, false, nullptr, nullptr, false,
+                          stream);
 }
 
 int sinkattn_prefill_fp8(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
@@ -620,7 +631,7 @@ int sinkattn_prefill_fp8(const void *q, const void *k, const void *v, const int3
                          sinkattn_stream_t stream) {
     return prefill_common(q, k, v, cu_seqlens, total_tokens, k_pages, v_pages, prefix_block_table,
                           prefix_lens, sinks, scale, out, lse, desc, workspace, ws_bytes, true, k_scale,
-                          v_scale, stream);
+                          v_scale, true, stream);
 }
 
 int sinkattn_append_kv(const void *k, const void *v, const int32_t *cu_seqlens,

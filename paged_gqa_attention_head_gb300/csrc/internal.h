@@ -102,6 +102,7 @@ struct PrefillArgs {
     uint64_t wait_limit_cycles;  // the same in SM cycles (2 per ns)
     uint32_t *status;
     bool fp8_prefix;                   // the prefix pages are FP8 E4M3 codes (uint8)
+    bool causal;                       // false: every query sees its whole request (no prefix, no window)
     const float *k_scale, *v_scale;    // FP8 prefix: [Hkv] per-KV-head scales, or nullptr (1)
 };
 // Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.

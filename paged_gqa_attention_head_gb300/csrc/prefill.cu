@@ -216,10 +216,13 @@ __device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane,
 // read one request's prefix run close together in time and share its pages in L2.
 // (B) Requests without a prefix: query blocks ordered by their index inside the request
 // (the number of causal key tiles they see), largest first, then by request, then by head
-// pair.  Items are dealt to the persistent CTAs in rounds (see item_rank).
+// pair.  Without the causal mask every block of a request sees all of its key tiles: the
+// requests are taken from the most blocks to the fewest, each one's blocks in order, then
+// by head pair.  Items are dealt to the persistent CTAs in rounds (see item_rank).
 // Set-up, once per CTA: s_nq[i] = query blocks of request i if it is in part B, else 0;
 // s_aend[i] = part-A query blocks of requests 0..i; s_cnt[lev] = part-B requests with more
-// than lev query blocks; s_cum[lev] = part-B query blocks at levels above lev.
+// than lev query blocks (non-causal: the blocks of the requests of exactly lev + 1 blocks);
+// s_cum[lev] = part-B query blocks at levels above lev.
 struct WorkList {
     const int *nq, *cnt, *cum, *aend;
     int n, levels, tiles, tiles_a, heads_per_item, groups;  // groups = items per query block
@@ -276,7 +279,10 @@ __device__ void worklist_setup(const PrefillArgs &a, int *s_nq, int *s_cnt, int 
     if (fast_lv)
         for (int lev = tid; lev < levels; lev += blockDim.x) {
             int c = 0;
-            for (int i = 0; i < a.n; ++i) c += s_nq[i] > lev;
+            if (a.causal)
+                for (int i = 0; i < a.n; ++i) c += s_nq[i] > lev;
+            else  // non-causal: level lev holds every block of the requests of lev + 1 blocks
+                for (int i = 0; i < a.n; ++i) c += s_nq[i] == lev + 1 ? lev + 1 : 0;
             s_cnt[lev] = c;
         }
     __syncthreads();
@@ -365,12 +371,23 @@ __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
                 lo = mid + 1;
         }
         int k = tr - wl.cum[lo];
-        for (int i = 0; i < wl.n; ++i)
-            if (wl.nq[i] > lo && k-- == 0) {
-                it.req = i;
-                break;
-            }
-        it.qb = lo;
+        if (a.causal) {
+            for (int i = 0; i < wl.n; ++i)
+                if (wl.nq[i] > lo && k-- == 0) {
+                    it.req = i;
+                    break;
+                }
+            it.qb = lo;
+        } else {
+            // the (k / (lo + 1))-th request of lo + 1 blocks, its block k % (lo + 1)
+            it.qb = k % (lo + 1);
+            k /= lo + 1;
+            for (int i = 0; i < wl.n; ++i)
+                if (wl.nq[i] == lo + 1 && k-- == 0) {
+                    it.req = i;
+                    break;
+                }
+        }
         return it;
     }
     // slow path: walk the levels of part B from the top over global memory
@@ -379,12 +396,16 @@ __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
         if (!has_prefix(a, i)) mq = max(mq, query_blocks(a, i));
     int r = tr;
     for (int lev = mq - 1; lev >= 0; --lev)
-        for (int i = 0; i < a.n; ++i)
-            if (!has_prefix(a, i) && query_blocks(a, i) > lev && r-- == 0) {
+        for (int i = 0; i < a.n; ++i) {
+            if (has_prefix(a, i)) continue;
+            const int q = query_blocks(a, i);
+            if (a.causal ? q > lev && r-- == 0 : q == lev + 1 && r < q) {
                 it.req = i;
-                it.qb = lev;
+                it.qb = a.causal ? lev : r;
                 return it;
             }
+            if (!a.causal && q == lev + 1) r -= q;
+        }
     return it;
 }
 
@@ -400,12 +421,13 @@ __device__ __forceinline__ int item_rank(int k) {
 // Key tiles of an item: prefix tiles 0..n_pre-1 (keys 128t .. 128t+127 of the prefix),
 // then the new-token tiles n_pre + k (keys P + 128k ..), up to the diagonal n_pre + qb.
 // A sliding window hides every tile before t0 from all 128 rows: the item visits tiles
-// t0 .. n_pre + qb, n_kv of them.
+// t0 .. n_pre + qb, n_kv of them.  Without the causal mask (an encoder's attention: no
+// prefix, no window) the item visits all new-token tiles of its request.
 struct ItemGeom {
     int row0, L, P, n_pre, t0, n_kv, g;
 };
 
-template <bool kWindow>
+template <bool kWindow, bool kCausal>
 __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it) {
     ItemGeom q;
     q.row0 = a.cu_seqlens[it.req];
@@ -423,17 +445,19 @@ __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it
         const int lb = q.P + it.qb * kBM - a.window + 1;
         if (lb > 0) q.t0 = lb < q.P ? lb / kBN : q.n_pre + (lb - q.P) / kBN;
     }
-    q.n_kv = q.n_pre + it.qb + 1 - q.t0;
+    // non-causal (no prefix, no window): every new-token tile of the request
+    q.n_kv = kCausal ? q.n_pre + it.qb + 1 - q.t0 : (q.L + kBN - 1) / kBN;
     q.g = it.h0 / a.G;
     return q;
 }
 
 // kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
-// window arithmetic.  kFp8: the paged prefix is an FP8 E4M3 cache (value = scale[g] *
+// window arithmetic.  kCausal = false: the non-causal variant (no prefix, no window), in
+// which each query row sees all keys of its request.  kFp8: the paged prefix is an FP8 E4M3 cache (value = scale[g] *
 // e4m3(code)); its tiles are staged as codes and converted in shared memory by the
 // converter warps - K to bf16 code values (exact; the K scale joins the score scale of
 // those tiles), V to fp16 value * 2^-k like the bf16 V tiles.
-template <int D, bool kWindow, bool kFp8>
+template <int D, bool kWindow, bool kFp8, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap kpmap,
@@ -525,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool test_limit = a.wait_limit_ns <= kImmediateLimitNs;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of<kWindow>(a, it);
+            const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
             if (lane == 0 && a.prefix_lens) {
                 const int Praw = a.prefix_lens[it.req];
                 if (Praw < 0 || Praw > a.max_pages * kPageSize)
@@ -708,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status, a.wait_limit_cycles));
         };
         int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
-        int n_kv = rank < n_items ? geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv : 0;
+        int n_kv = rank < n_items ? geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv : 0;
         uint32_t i = 0;
         int b = 0, pb = 0;            // i % NBS, i % NBP
         uint32_t use = 0, use_p = 0;  // i / NBS, i / NBP
@@ -774,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++j == n_kv) {
                     j = 0;
                     rank = item_rank(++k);
-                    if (rank < n_items) n_kv = geom_of<kWindow>(a, item_of(a, wl, rank)).n_kv;
+                    if (rank < n_items) n_kv = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv;
                 }
             }
             continue;
@@ -794,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kv = 0, k = 0;
         bool ok = true;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
-            const ItemGeom gm = geom_of<kWindow>(a, item_of(a, wl, rank));
+            const ItemGeom gm = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank));
             // FP8 V: |value| <= 448 * v_scale, so one exponent k per item keeps every converted
             // value below 2^15 (k = 0 for any scale below 73): no per-tile maximum needed
             const float vsc = kFp8 && a.v_scale ? a.v_scale[gm.g] : 1.f;
@@ -903,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = x < ntiles;
         for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
             const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of<kWindow>(a, it);
+            const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
             const int h = it.h0 + x;
             const int t = it.qb * kBM + r;  // position among the request's new tokens
             const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
@@ -925,7 +949,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tt = kWindow ? gm.t0 + j : j;  // key tile
                 // keys lo .. ncols-1 of this tile are the row's to see
                 int ncols;
-                if (tt < gm.n_pre)
+                if (!kCausal)
+                    ncols = min(kBN, gm.L - tt * kBN);  // the request's ragged end
+                else if (tt < gm.n_pre)
                     ncols = min(kBN, gm.P - tt * kBN);
                 else if (tt - gm.n_pre == it.qb)
                     ncols = r + 1;  // diagonal tile: keys 0..r
@@ -1130,12 +1156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kWindow, bool kFp8>
+template <int D, bool kWindow, bool kFp8, bool kCausal = true>
 cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtensorMap &kmap,
                      const CUtensorMap &vmap, const CUtensorMap &kpmap, const CUtensorMap &vpmap,
                      cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWindow, kFp8>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, kWindow, kFp8, kCausal>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     int device = 0, sms = 0;
@@ -1144,7 +1170,7 @@ cudaError_t launch_d(const PrefillArgs &a, const CUtensorMap &qmap, const CUtens
     // persistent: one CTA per SM (shared memory and the 512 TMEM columns allow no more),
     // on at most max_sms SMs when the caller keeps the others for concurrent work
     if (a.max_sms > 0 && a.max_sms < sms) sms = a.max_sms;
-    prefill_kernel<D, kWindow, kFp8><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
+    prefill_kernel<D, kWindow, kFp8, kCausal><<<sms, kThreads, C::kSmemBytes, stream>>>(qmap, kmap, vmap, kpmap, vpmap, a);
     return cudaGetLastError();
 }
 
@@ -1154,6 +1180,12 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &qmap, const 
                            const CUtensorMap &vmap, const CUtensorMap &kpmap,
                            const CUtensorMap &vpmap, cudaStream_t stream) {
     const bool w = a.window > 0;
+    if (!a.causal) {  // no prefix, no window
+        if (a.fp8_prefix || w || a.prefix_lens) return cudaErrorInvalidValue;
+        if (a.D == 64) return launch_d<64, false, false, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        if (a.D == 128) return launch_d<128, false, false, false>(a, qmap, kmap, vmap, kpmap, vpmap, stream);
+        return cudaErrorNotSupported;
+    }
     if (a.fp8_prefix) {
         if (a.D == 64)
             return w ? launch_d<64, true, true>(a, qmap, kmap, vmap, kpmap, vpmap, stream)

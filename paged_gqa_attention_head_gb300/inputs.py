@@ -284,6 +284,10 @@ class PrefillInputs:
         """2 flops per multiply-add, for Q.K^T and P.V over the visited pairs."""
         return 4 * self.head_dim * self.num_qo_heads * self.causal_pairs(window)
 
+    def noncausal_flops(self) -> int:
+        """The same count when every query sees its whole request (L^2 pairs per request)."""
+        return 4 * self.head_dim * self.num_qo_heads * sum(L * L for L in self.new_lens)
+
 
 def make_prefill(new_lens: list[int], num_qo_heads: int, num_kv_heads: int, head_dim: int,
                  seed: int = 0, sinks: bool = True, scale: Optional[float] = None,
@@ -353,6 +357,11 @@ WORKLOADS = {
     "longctx_chunked_fp8": dict(kind="chunked", lens=[512] * 8, prefix_lens=[16384] * 8,
                                 num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,
                                 prefix_kv_dtype="fp8"),
+    # an embedding model's batch without a KV cache: documents of 4096, 512 and 128 tokens
+    # (the lengths of the embedding benchmarks), attention heads of the Qwen3 family's small
+    # models (16 query / 8 KV heads, head_dim 128), no sinks; non-causal attention
+    "encoder_ragged": dict(kind="prefill", lens=[4096] * 2 + [512] * 12 + [128] * 32,
+                           num_qo_heads=16, num_kv_heads=8, head_dim=128, sinks=False),
     # the decode shapes over an FP8 E4M3 cache
     "gptoss_decode_fp8": dict(kind="decode", batch=64, lens=("uniform", 512, 8192),
                               num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,

@@ -58,6 +58,8 @@ SIGNATURES = {
     "sinkattn_prefill_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(_SZ)]),
     "sinkattn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _F, _P, _P, _DP,
                                         _P, _SZ, _P]),
+    "sinkattn_prefill_noncausal": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _F, _P, _P, _DP, _P, _SZ,
+                                                  _P]),
     "sinkattn_prefill_fp8": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _F, _P,
                                             _P, _DP, _P, _SZ, _P]),
     "sinkattn_append_kv": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _DP, _P, _SZ, _P]),
@@ -295,6 +297,36 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
                                    _ptr(v_pages), _ptr(prefix_block_table), _ptr(prefix_lens),
                                    _ptr(sinks), scale, _ptr(out), _ptr(lse), ctypes.byref(desc),
                                    _ptr(ws), ws.numel(), _stream(dev)), "sinkattn_prefill")
+    return out, lse
+
+
+def prefill_noncausal(q, k, v, cu_seqlens, sinks=None, scale=None, out=None, lse=None,
+                      workspace_buf=None, return_lse=True, max_sms=0, wait_limit_us=0):
+    """Non-causal ragged prefill without a KV cache (sinkattn_prefill_noncausal): query t of
+    request i attends every token of request i.  Returns (out, lse)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(k, "k", torch.bfloat16, dev, 3)
+    _need(v, "v", torch.bfloat16, dev, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, 1)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D):
+        raise ValueError("k / v must be [T, Hkv, D] matching q")
+    n = cu_seqlens.shape[0] - 1
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, dev, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
+    desc = paged_desc(n, Hq, Hkv, D, 0, 0, max_sms=max_sms, wait_limit_us=wait_limit_us)
+    nbytes = prefill_workspace_size(desc)
+    ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(load().sinkattn_prefill_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), T, _ptr(sinks),
+                                             scale, _ptr(out), _ptr(lse), ctypes.byref(desc), _ptr(ws),
+                                             ws.numel(), _stream(dev)), "sinkattn_prefill_noncausal")
     return out, lse
 
 

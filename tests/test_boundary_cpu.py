@@ -135,6 +135,22 @@ def test_prefix_arguments_all_or_nothing(sa):
     assert rc == 1
 
 
+def test_noncausal_prefill_rejects_before_cuda(sa):
+    """No tokens: OK at once; NULL data or a sliding window: SINKATTN_ERR_INVALID_ARG, all
+    before any CUDA call (a window has no meaning without the causal order)."""
+    lib = sa.load()
+    d = _desc(sa)
+    assert lib.sinkattn_prefill_noncausal(None, None, None, None, 0, None, 0.125, None, None,
+                                          ctypes.byref(d), None, 0, None) == 0
+    assert lib.sinkattn_prefill_noncausal(None, None, None, None, 8, None, 0.125, None, None,
+                                          ctypes.byref(d), None, 0, None) == 1
+    buf = (ctypes.c_uint8 * 4096)()
+    p = (ctypes.addressof(buf) + 255) // 256 * 256
+    dw = _desc(sa, window=128)
+    assert lib.sinkattn_prefill_noncausal(p, p, p, p, 8, None, 0.125, p, None, ctypes.byref(dw), p,
+                                          256, None) == 1
+
+
 def test_desc_layout_matches_the_header(sa):
     """The binding's struct has the header's fields, in order, all int32."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)

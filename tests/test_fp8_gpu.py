@@ -191,3 +191,23 @@ def test_fp8_full_configs_sampled(sa, oracle_mod, cuda_dev, name):
     check_out(out, ro, mask=sel)
     check_lse(lse, rl, mask=sel)
     assert sa.get_status(sa.workspace(0, cuda_dev)) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_fp8_q_at_the_edge_of_fp16(sa, oracle_mod, cuda_dev, D):
+    """The FP8 decode forms q.k with q in fp16: exact for |q| in [2^-14, 65504].  Rows whose
+    entries reach 60000 and rows of tiny entries (2^-13) must still match the oracle."""
+    lens = [17, 300, 2000, 1]
+    w = inputs.make_decode(lens, len(lens), 16, 2, D, seed=70 + D, sinks=True, kv_dtype="fp8")
+    q = w.q.float()
+    q[0, :, ::7] = 60000.0
+    q[1, 3] = 2.0 ** -13 * torch.sign(q[1, 3])
+    q[2, :, 1] = -65000.0
+    w.q = q.to(torch.bfloat16)
+    assert float(w.q.float().abs().max()) < 65504
+    # a small K scale keeps the logits moderate (an lse near 1e5 would be beyond fp32's 1e-3)
+    w.cache.k_scale = torch.full_like(w.cache.k_scale, 2e-6)
+    out, lse = _decode(sa, w, cuda_dev)
+    ro, rl = _oracle(oracle_mod, w)
+    check_out(out, ro, what="fp8 decode, q at the edge of fp16")
+    check_lse(lse, rl, what="fp8 decode lse, q at the edge of fp16")

@@ -118,3 +118,27 @@ def test_prefill_fp8_bad_prefix_page(sa, oracle_mod, cuda_dev):
     keep[64:] = True  # request 1 is untouched
     check_out(out, ro, mask=keep, what="request beside a bad prefix page")
     check_lse(lse, rl, mask=keep)
+
+
+def test_prefill_fp8_large_v_scale(sa, oracle_mod, cuda_dev):
+    """V scales large enough that 448 * scale passes 2^15: the converted V takes a power-of-two
+    exponent k > 0 (k = 4 and 7 here) and must still match the oracle; a scale past k = 7 sets
+    SINKATTN_STATUS_VALUE_RANGE.  The prefix values are the N(0,1) data times c = the new
+    scale over the old one, so the absolute part of the bar is taken c times larger."""
+    p = inputs.make_prefill([100, 30], 8, 2, 64, seed=140, sinks=True, prefix_lens=[300, 129],
+                            prefix_kv_dtype="fp8")
+    c = p.prefix
+    old = c.v_scale.clone()
+    c.v_scale = torch.tensor([700.0, 9000.0], dtype=torch.float32)
+    mag = (c.v_scale / old).double().repeat_interleave(4).numpy()[None, :, None]  # [1, Hq, 1]
+    d = _dev_prefill(p, cuda_dev)
+    ws = sa.workspace(256, cuda_dev, "prefill")
+    sa.get_status(ws)
+    out, lse = _run(sa, p, d)
+    assert sa.get_status(ws) == 0
+    ro, rl = _oracle(oracle_mod, p)
+    check_out(out, ro, what="fp8-prefix prefill, large V scales", v_mag=mag)
+    check_lse(lse, rl, what="fp8-prefix lse, large V scales")
+    d["vs"] = torch.tensor([700.0, 20000.0], dtype=torch.float32, device=cuda_dev)
+    _run(sa, p, d)
+    assert sa.get_status(ws) & sa.STATUS_VALUE_RANGE

@@ -146,9 +146,10 @@ def test_prefill_row_equals_decode(sa, cuda_dev):
 
 
 def _large_rows(n, lo_exp, seed):
-    """n x D-independent positive bf16 magnitudes in [2^lo_exp, 2^(lo_exp + 1))."""
+    """n x D-independent positive magnitudes in [2^lo_exp, 2^(lo_exp + 1)), still below
+    2^(lo_exp + 1) once rounded to bf16."""
     g = torch.Generator().manual_seed(seed)
-    return (2.0 ** lo_exp) * (1.0 + torch.rand(n, generator=g))
+    return (2.0 ** lo_exp) * (1.0 + 0.99 * torch.rand(n, generator=g))
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -191,6 +192,31 @@ def test_chunked_prefill_prefix_v_quarters_with_different_scales(sa, oracle_mod,
     check_out(out, ro)
     check_lse(lse, rl)
     assert sa.get_status(ws) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_v_at_the_top_of_the_supported_range(sa, oracle_mod, cuda_dev, D):
+    """The edge of the documented range: a 32-key quarter of V in [2^21, 2^22) takes the
+    largest power-of-two scale (k = 7) and must still match the oracle, with no status; one
+    value at 2^22 is past it and sets SINKATTN_STATUS_VALUE_RANGE."""
+    p = inputs.make_prefill([200, 130], 8, 2, D, seed=60 + D, sinks=True)
+    cu = p.cu_seqlens.tolist()
+    for i in range(len(cu) - 1):
+        for t in range(cu[i], cu[i + 1]):
+            if (t - cu[i]) % 128 < 32:
+                row = _large_rows(D, 21, t) * torch.where(torch.arange(D) % 3 == 0, -1.0, 1.0)
+                p.v[t] = row.to(torch.bfloat16).expand(p.v.shape[1], D)
+    assert float(p.v.abs().max()) < 2.0 ** 22
+    ws = sa.workspace(0, cuda_dev, "prefill")
+    sa.get_status(ws)
+    out, lse = run_prefill(sa, p, cuda_dev)
+    assert sa.get_status(ws) == 0
+    ro, rl = oracle_prefill(oracle_mod, p)
+    check_out(out, ro)
+    check_lse(lse, rl)
+    p.v[5, 0, 3] = 2.0 ** 22
+    run_prefill(sa, p, cuda_dev)
+    assert sa.get_status(ws) & sa.STATUS_VALUE_RANGE
 
 
 def test_prefill_v_beyond_fp16_range_sets_status(sa, cuda_dev):

@@ -13,13 +13,18 @@ import torch
 ATOL, RTOL, LSE_ATOL = 2e-3, 1e-2, 1e-3
 
 
-def check_out(gpu_out: torch.Tensor, ref: np.ndarray, mask=None, what="out"):
+def check_out(gpu_out: torch.Tensor, ref: np.ndarray, mask=None, what="out", v_mag=1.0):
+    """v_mag: how much larger than the N(0,1) data the values V are (a number, or an array
+    that broadcasts against out).  The output is linear in V, so V multiplied by c
+    multiplies the output and every rounding error in it by c: the absolute part of the
+    bar scales with it, the relative part stays."""
     g = gpu_out.detach().float().cpu().numpy().astype(np.float64)
+    vm = np.broadcast_to(np.asarray(v_mag, dtype=np.float64), ref.shape)
     if mask is not None:
-        g, ref = g[mask], ref[mask]
+        g, ref, vm = g[mask], ref[mask], vm[mask]
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
     err = np.abs(g - ref)
-    bound = ATOL + RTOL * np.abs(ref)
+    bound = ATOL * vm + RTOL * np.abs(ref)
     bad = err > bound
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
                            f"max err {err.max():.3e}, worst excess {(err - bound).max():.3e}")
