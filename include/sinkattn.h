@@ -360,7 +360,11 @@ int sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pa
  * out:        bf16 [T, Hq, D]
  * desc:       num_seqs, heads, head_dim, page_size; num_pages and max_pages_per_seq
  *             describe the prefix pages (ignored without a prefix)
- * workspace:  at least sinkattn_prefill_workspace_size bytes (status header only)
+ * workspace:  at least sinkattn_prefill_workspace_size bytes: the 256-byte header only,
+ *             holding the status word and the counters the persistent grid takes its work
+ *             items from.  Zero it once before the first call (sinkattn_workspace_init);
+ *             every call leaves the counters at zero.  Calls that share one workspace must
+ *             be ordered on the GPU (same stream, or synchronised).
  */
 int sinkattn_prefill_workspace_size(const sinkattn_paged_desc *desc, size_t *bytes);
 

@@ -594,6 +594,7 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
     a.status = static_cast<uint32_t *>(workspace);
     a.fp8_prefix = fp8;
     a.causal = causal;
+    a.sched = static_cast<uint32_t *>(workspace) + 16;  // header bytes 64..71
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     cudaError_t e = launch_prefill(a, qmap, kmap, vmap, kpmap, vpmap, (cudaStream_t)stream);

@@ -103,6 +103,7 @@ struct PrefillArgs {
     uint32_t *status;
     bool fp8_prefix;                   // the prefix pages are FP8 E4M3 codes (uint8)
     bool causal;                       // false: every query sees its whole request (no prefix, no window)
+    uint32_t *sched;                   // [2] in the workspace header: next item, CTAs done (zero between calls)
     const float *k_scale, *v_scale;    // FP8 prefix: [Hkv] per-KV-head scales, or nullptr (1)
 };
 // Tensor maps: q [T, Hq, D], k/v [T, Hkv, D] (new tokens), kp/vp prefix pages.

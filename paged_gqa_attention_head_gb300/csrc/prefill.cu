@@ -11,9 +11,9 @@
 // HND pages).  Query t of request i sits at absolute position P_i + t and sees
 // every prefix key and new keys 0..t.
 //
-// GB300 design.  A persistent grid (one CTA per SM) walks work items, heaviest
-// first.  An item is one 128-row query block of one request for TWO query heads
-// of the same KV head (tiles A and B), so every K/V tile in shared memory feeds
+// GB300 design.  A persistent grid (one CTA per SM) takes work items, heaviest first,
+// from a counter shared by the grid.  An item is one 128-row query block of one request
+// for TWO query heads of the same KV head (tiles A and B), so every K/V tile in shared memory feeds
 // two S = Q K^T products and the two softmax warpgroups run side by side while
 // the tensor core alternates between them.  Key tiles: prefix tiles first, then
 // the causal new-token tiles up to the diagonal; fully masked tiles are skipped.
@@ -64,6 +64,12 @@ static_assert(128 * kRegsSide + 128 * kRegsConvert + 256 * kRegsSoftmax <= kThre
               "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLocateMax = 1024;  // requests / levels of the shared-memory tile lookup
+// Items reach the CTA's roles through a ring of slots.  Every role is within a few items of
+// the producer (it loads a K/V stage only after the P.V that last read it, which follows that
+// tile's S product, softmax and V conversion; a Q tile only after the last S product of the
+// item before), at most the ring depth of NS <= 4 tiles, so a slot is read by every role before
+// the producer posts to it again.
+constexpr int kItemRing = 16;
 
 template <int D>
 struct PrefillCfg {
@@ -78,7 +84,7 @@ struct PrefillCfg {
     static constexpr bool kSplitP = D == 64;         // P in buffers of its own (else over S)
     static constexpr int kSBufs = 2;                 // S buffers (128 columns, fp32)
     static constexpr int kPBufs = 2;                 // P buffers (64 columns of fp16 pairs)
-    static constexpr int kNumBars = 2 + 5 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1;
+    static constexpr int kNumBars = 2 + 5 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1 + kItemRing;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 4 * kLocateMax * 4;
     static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
@@ -102,7 +108,7 @@ struct PrefillCfg {
 
 struct Bars {
     uint64_t *q_full, *q_empty, *k_full, *v_full, *v_conv, *k_conv, *kv_empty, *s_full, *s_free,
-        *p_full, *pv_done, *o_free, *drain;
+        *p_full, *pv_done, *o_free, *drain, *item_full;
 };
 
 // Bounded wait (limit_cycles SM cycles: the call's wait limit, converted on the host) that also
@@ -218,7 +224,8 @@ __device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane,
 // (the number of causal key tiles they see), largest first, then by request, then by head
 // pair.  Without the causal mask every block of a request sees all of its key tiles: the
 // requests are taken from the most blocks to the fewest, each one's blocks in order, then
-// by head pair.  Items are dealt to the persistent CTAs in rounds (see item_rank).
+// by head pair.  The persistent CTAs take items in this order from a counter in the workspace
+// header, each as its producer gets to it, so a CTA that ran faster takes more of them.
 // Set-up, once per CTA: s_nq[i] = query blocks of request i if it is in part B, else 0;
 // s_aend[i] = part-A query blocks of requests 0..i; s_cnt[lev] = part-B requests with more
 // than lev query blocks (non-causal: the blocks of the requests of exactly lev + 1 blocks);
@@ -409,13 +416,16 @@ __device__ Item item_of(const PrefillArgs &a, const WorkList &wl, int rank) {
     return it;
 }
 
-// Rank of this CTA's k-th item: items are dealt in rounds of gridDim.x, in alternating
-// direction, so that with items sorted by size the CTAs' totals come out close.  Every
-// rank below n_items belongs to exactly one (CTA, k), and a CTA's ranks only grow, so
-// its items end at the first rank >= n_items.
-__device__ __forceinline__ int item_rank(int k) {
-    const int G = gridDim.x, b = blockIdx.x;
-    return k * G + ((k & 1) ? G - 1 - b : b);
+// A CTA has taken its last item: count it; the last CTA of the grid puts the work-list
+// counters back to zero for the next call on this workspace (calls on one workspace are
+// ordered on the GPU).  Every item fetch of every CTA comes before its count.
+__device__ __forceinline__ void cta_done(uint32_t *sched) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+        sched[0] = 0;
+        sched[1] = 0;
+        __threadfence();
+    }
 }
 
 // Key tiles of an item: prefix tiles 0..n_pre-1 (keys 128t .. 128t+127 of the prefix),
@@ -488,11 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.pv_done = bars.p_full + NBP;      // [NBP] per P buffer: the P.V reading it is done
     bars.o_free = bars.pv_done + NBP;      // [2] per query tile: O was read (once per item)
     bars.drain = bars.o_free + 2;
+    bars.item_full = bars.drain + 1;     // [kItemRing] per slot: the producer posted an item
     int *s_loc = reinterpret_cast<int *>(smem + C::kOffLoc);
     int *misc = reinterpret_cast<int *>(smem + C::kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 1;
     int *s_vscale = misc + 32;  // [NS][4] exponent k of each 32-key quarter of each V tile
+    int *s_item = misc + 48;    // [kItemRing] the rank of the CTA's k-th item in slot k % kItemRing
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -500,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     worklist_setup(a, s_loc, s_loc + kLocateMax, s_loc + 2 * kLocateMax, s_loc + 3 * kLocateMax, misc + 4,
                    &wl);
     const int n_items = wl.tiles * wl.groups;
-    if ((int)blockIdx.x >= n_items) return;  // CTA-uniform, before any allocation
+    if ((int)blockIdx.x >= n_items) {  // CTA-uniform, before any allocation
+        if (tid == 0) cta_done(a.sched);
+        return;
+    }
     const int ntiles = wl.heads_per_item;    // query tiles per item (1 or 2)
 
     if (tid == 0) {
@@ -524,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) mbar_init(&bars.o_free[x], 4);
         mbar_init(bars.drain, 64);  // one commit from every lane of the two MMA-issuing warps
+        for (int s = 0; s < kItemRing; ++s) mbar_init(&bars.item_full[s], 1);
         fence_mbar_init();
     }
     // What the producer issued (for the drain after an abort): the Q tiles of items
@@ -547,7 +563,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         int k = 0;   // items so far
         bool ok = true;
         const bool test_limit = a.wait_limit_ns <= kImmediateLimitNs;
-        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
+        // the next item from the work-list counter (items in rank order: heaviest first), posted
+        // in slot kk % kItemRing for the other roles; a rank >= n_items ends the CTA's work
+        auto fetch = [&](int kk) {
+            int r = 0;
+            if (lane == 0) {
+                r = min((int)atomicAdd(a.sched, 1u), n_items);
+                s_item[kk % kItemRing] = r;
+                mbar_arrive(&bars.item_full[kk % kItemRing]);
+            }
+            return __shfl_sync(0xffffffffu, r, 0);
+        };
+        for (int rank = fetch(0); ok && rank < n_items; rank = fetch(++k)) {
             const Item it = item_of(a, wl, rank);
             const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
             if (lane == 0 && a.prefix_lens) {
@@ -731,13 +758,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
             return __all_sync(0xffffffffu, wait_or_abort<true>(bar, parity, s_abort, a.status, a.wait_limit_cycles));
         };
-        int rank = item_rank(0), k = 0, j = 0, x = 0, kv = 0;
+        auto take = [&](int kk) {
+            if (!warp_wait(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1))) return -1;
+            return s_item[kk % kItemRing];
+        };
+        int k = 0, j = 0, x = 0, kv = 0;
+        int rank = take(0);
         int n_kv = rank < n_items ? geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv : 0;
         uint32_t i = 0;
         int b = 0, pb = 0;            // i % NBS, i % NBP
         uint32_t use = 0, use_p = 0;  // i / NBS, i / NBP
         bool ok = true;
-        while (ok && rank < n_items) {
+        while (ok && rank >= 0 && rank < n_items) {
             const int st = kv % NS;
             const uint32_t sp = (uint32_t)((kv / NS) & 1);
             if (pv_role) {
@@ -797,7 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++kv;
                 if (++j == n_kv) {
                     j = 0;
-                    rank = item_rank(++k);
+                    rank = take(++k);
+                    if (rank < 0) break;
                     if (rank < n_items) n_kv = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv;
                 }
             }
@@ -817,7 +850,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp - 12;
         int kv = 0, k = 0;
         bool ok = true;
-        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
+        auto take = [&](int kk) {
+            if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1),
+                                                        s_abort, a.status, a.wait_limit_cycles)))
+                return n_items;
+            return s_item[kk % kItemRing];
+        };
+        for (int rank = take(0); ok && rank < n_items; rank = take(++k)) {
             const ItemGeom gm = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank));
             // FP8 V: |value| <= 448 * v_scale, so one exponent k per item keeps every converted
             // value below 2^15 (k = 0 for any scale below 73): no per-tile maximum needed
@@ -925,7 +964,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tcount = 0;  // key tiles this query tile has processed (over all items)
         int k = 0;
         bool ok = x < ntiles;
-        for (int rank = item_rank(0); ok && rank < n_items; rank = item_rank(++k)) {
+        auto take = [&](int kk) {
+            if (!wait_or_abort(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1), s_abort, a.status,
+                               a.wait_limit_cycles))
+                return n_items;
+            return s_item[kk % kItemRing];
+        };
+        for (int rank = ok ? take(0) : n_items; ok && rank < n_items; rank = take(++k)) {
             const Item it = item_of(a, wl, rank);
             const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
             const int h = it.h0 + x;
@@ -1154,6 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::dealloc(tmem, kTmemCols);
     }
+    if (tid == 0) cta_done(a.sched);
 }
 
 template <int D, bool kWindow, bool kFp8, bool kCausal = true>
