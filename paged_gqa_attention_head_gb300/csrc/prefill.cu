@@ -87,7 +87,8 @@ struct PrefillCfg {
     static constexpr int kNumBars = 2 + 5 * kStages + 2 * kSBufs + 2 * kPBufs + 2 + 1 + kItemRing;
     static constexpr int kOffLoc = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
     static constexpr int kOffMisc = kOffLoc + 4 * kLocateMax * 4;
-    static constexpr int kSmemBytes = 1024 + kOffMisc + 256;
+    static constexpr int kOffSlot = kOffMisc + 256;  // [kItemRing] ItemSlot, 64 bytes each
+    static constexpr int kSmemBytes = 1024 + kOffSlot + kItemRing * 64;
     __host__ __device__ static constexpr uint32_t kColS(int b) { return 128u * b; }
     __host__ __device__ static constexpr uint32_t kColP(int p) {
         return kSplitP ? 128u * kSBufs + 64u * p : 128u * p;
@@ -461,6 +462,17 @@ __device__ __forceinline__ ItemGeom geom_of(const PrefillArgs &a, const Item &it
     return q;
 }
 
+// What the producer posts for an item: its rank and what the other roles derive from it, so
+// that they read it from shared memory instead of computing it again from global memory.
+struct alignas(16) ItemSlot {
+    int rank;           // >= n_items: no more items
+    Item it;
+    ItemGeom gm;
+    float sink2[2];     // per query tile: sink * log2(e), -inf without sinks
+    float kscale, vscale;  // FP8 prefix: the KV head's scales (1 if not given)
+};
+static_assert(sizeof(ItemSlot) == 64, "item slot");
+
 // kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
 // window arithmetic.  kCausal = false: the non-causal variant (no prefix, no window), in
 // which each query row sees all keys of its request.  kFp8: the paged prefix is an FP8 E4M3 cache (value = scale[g] *
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc);
     volatile int *s_abort = misc + 1;
     int *s_vscale = misc + 32;  // [NS][4] exponent k of each 32-key quarter of each V tile
-    int *s_item = misc + 48;    // [kItemRing] the rank of the CTA's k-th item in slot k % kItemRing
+    ItemSlot *s_slot = reinterpret_cast<ItemSlot *>(smem + C::kOffSlot);  // the k-th item in slot k % kItemRing
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -568,15 +580,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto fetch = [&](int kk) {
             int r = 0;
             if (lane == 0) {
+                ItemSlot &sl = s_slot[kk % kItemRing];
                 r = min((int)atomicAdd(a.sched, 1u), n_items);
-                s_item[kk % kItemRing] = r;
+                sl.rank = r;
+                if (r < n_items) {
+                    sl.it = item_of(a, wl, r);
+                    sl.gm = geom_of<kWindow, kCausal>(a, sl.it);
+                    for (int x = 0; x < 2; ++x)
+                        sl.sink2[x] = a.sinks && x < ntiles ? a.sinks[sl.it.h0 + x] * kLog2e : -INFINITY;
+                    sl.kscale = kFp8 && a.k_scale ? a.k_scale[sl.gm.g] : 1.f;
+                    sl.vscale = kFp8 && a.v_scale ? a.v_scale[sl.gm.g] : 1.f;
+                }
                 mbar_arrive(&bars.item_full[kk % kItemRing]);
             }
+            __syncwarp();
             return __shfl_sync(0xffffffffu, r, 0);
         };
         for (int rank = fetch(0); ok && rank < n_items; rank = fetch(++k)) {
-            const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
+            const Item it = s_slot[k % kItemRing].it;
+            const ItemGeom gm = s_slot[k % kItemRing].gm;
             if (lane == 0 && a.prefix_lens) {
                 const int Praw = a.prefix_lens[it.req];
                 if (Praw < 0 || Praw > a.max_pages * kPageSize)
@@ -760,11 +782,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto take = [&](int kk) {
             if (!warp_wait(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1))) return -1;
-            return s_item[kk % kItemRing];
+            return s_slot[kk % kItemRing].rank;
         };
         int k = 0, j = 0, x = 0, kv = 0;
         int rank = take(0);
-        int n_kv = rank < n_items ? geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv : 0;
+        int n_kv = rank >= 0 && rank < n_items ? s_slot[0].gm.n_kv : 0;
         uint32_t i = 0;
         int b = 0, pb = 0;            // i % NBS, i % NBP
         uint32_t use = 0, use_p = 0;  // i / NBS, i / NBP
@@ -831,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     j = 0;
                     rank = take(++k);
                     if (rank < 0) break;
-                    if (rank < n_items) n_kv = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank)).n_kv;
+                    if (rank < n_items) n_kv = s_slot[k % kItemRing].gm.n_kv;
                 }
             }
             continue;
@@ -854,13 +876,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, wait_or_abort<true>(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1),
                                                         s_abort, a.status, a.wait_limit_cycles)))
                 return n_items;
-            return s_item[kk % kItemRing];
+            return s_slot[kk % kItemRing].rank;
         };
         for (int rank = take(0); ok && rank < n_items; rank = take(++k)) {
-            const ItemGeom gm = geom_of<kWindow, kCausal>(a, item_of(a, wl, rank));
+            const ItemGeom gm = s_slot[k % kItemRing].gm;
             // FP8 V: |value| <= 448 * v_scale, so one exponent k per item keeps every converted
             // value below 2^15 (k = 0 for any scale below 73): no per-tile maximum needed
-            const float vsc = kFp8 && a.v_scale ? a.v_scale[gm.g] : 1.f;
+            const float vsc = kFp8 ? s_slot[k % kItemRing].vscale : 1.f;
             int kexp8 = 0;
             if (kFp8) {
                 const float top = 448.f * vsc;
@@ -968,16 +990,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_or_abort(&bars.item_full[kk % kItemRing], (uint32_t)((kk / kItemRing) & 1), s_abort, a.status,
                                a.wait_limit_cycles))
                 return n_items;
-            return s_item[kk % kItemRing];
+            return s_slot[kk % kItemRing].rank;
         };
         for (int rank = ok ? take(0) : n_items; ok && rank < n_items; rank = take(++k)) {
-            const Item it = item_of(a, wl, rank);
-            const ItemGeom gm = geom_of<kWindow, kCausal>(a, it);
+            const Item it = s_slot[k % kItemRing].it;
+            const ItemGeom gm = s_slot[k % kItemRing].gm;
             const int h = it.h0 + x;
             const int t = it.qb * kBM + r;  // position among the request's new tokens
-            const float sink2 = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+            const float sink2 = s_slot[k % kItemRing].sink2[x];
             // score scale of FP8 prefix tiles: their K holds code values, the K scale joins here
-            const float sc_pre = kFp8 && a.k_scale ? a.scale_log2 * a.k_scale[gm.g] : a.scale_log2;
+            const float sc_pre = kFp8 ? a.scale_log2 * s_slot[k % kItemRing].kscale : a.scale_log2;
             float m_used = sink2;                      // running max, seeded with the sink
             float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
             for (int j = 0; j < gm.n_kv; ++j) {
