@@ -1053,51 +1053,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // row max: eight chains of three-input maxima over 16 keys each
-                float mx8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float *sf = reinterpret_cast<const float *>(sv) + 16 * e;
-                    float m = fmax3(sf[0], sf[1], sf[2]);
-#pragma unroll
-                    for (int t = 3; t < 15; t += 2) m = fmax3(m, sf[t], sf[t + 1]);
-                    mx8[e] = fmaxf(m, sf[15]);
-                }
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
                 const float sc = kFp8 && tt < gm.n_pre ? sc_pre : a.scale_log2;
-                const float mt = mx * sc;
+                // row max: eight chains of three-input maxima over 16 keys each
+                auto row_max = [&]() {
+                    float mx8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float *sf = reinterpret_cast<const float *>(sv) + 16 * e;
+                        float m = fmax3(sf[0], sf[1], sf[2]);
+#pragma unroll
+                        for (int t = 3; t < 15; t += 2) m = fmax3(m, sf[t], sf[t + 1]);
+                        mx8[e] = fmaxf(m, sf[15]);
+                    }
+                    return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                 fmaxf(mx8[6], mx8[7]));
+                };
                 if (j == 0) {
+                    const float mt = row_max() * sc;
                     const float mn = fmaxf(m_used, mt);
                     l = (m_used == -INFINITY) ? 0.f : l * fast_exp2(m_used - mn);
                     m_used = mn;
-                } else {
-                    const bool need = mt > m_used + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, need)) {
-                        // O_x must hold the P.V of this query tile's previous key tile,
-                        // product i - ntiles (its P buffer's previous use is long done)
-                        const uint32_t ip = i - ntiles;
-                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::fence_after_sync();
-                        const float mn = fmaxf(m_used, mt);
-                        const float alpha = need ? fast_exp2(m_used - mn) : 1.f;
-                        if (need) {
-                            l *= alpha;
-                            m_used = mn;
-                        }
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t o[32];
-                            tc::ld_32x32b_x32(tO + c * 32, o);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tc::st_32x32b_x32(tO + c * 32, o);
-                        }
-                    }
                 }
                 // P * 2^k = exp2(s * scale - m + k) in fp16 in the 64 columns of the P buffer
                 // (keys 2c, 2c + 1 in column c); 2^-k is the scale of the V quarter holding
@@ -1116,41 +1091,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                 }
                 const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
-                const bool k_uniform = kq.x == kq.y && kq.y == kq.z && kq.z == kq.w;  // warp-uniform
-                const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
                 const float2 sc2 = make_float2(sc, sc);
-                // running sums of keys c with c % 8 = 2q (.x) and 2q + 1 (.y)
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f)};
-                uint32_t pp[kBN / 2];
+                // writes P against the running max m_used; returns the row's sum of P * 2^-k
+                auto emit = [&]() {
+                    const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
+                    float tl = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < kBN / 32; ++ch) {
-                    const int kc = ch == 0 ? kq.x : ch == 1 ? kq.y : ch == 2 ? kq.z : kq.w;
-                    const float neg = neg0 + (float)kc;
-                    const float2 ng2 = make_float2(neg, neg);
+                    for (int ch = 0; ch < kBN / 32; ++ch) {
+                        const int kc = ch == 0 ? kq.x : ch == 1 ? kq.y : ch == 2 ? kq.z : kq.w;
+                        const float neg = neg0 + (float)kc;
+                        const float2 ng2 = make_float2(neg, neg);
+                        // running sums of keys c with c % 8 = 2q (.x) and 2q + 1 (.y)
+                        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                         make_float2(0.f, 0.f)};
+                        uint32_t pp[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = ch * 32 + 2 * e;
-                        const float2 t2 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                                sc2, ng2);
-                        const float p0 = fast_exp2(t2.x);
-                        const float p1 = fast_exp2(t2.y);
-                        acc[e & 3] = fadd2(acc[e & 3], make_float2(p0, p1));
-                        pp[ch * 16 + e] = pack_f16x2(p0, p1);
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = ch * 32 + 2 * e;
+                            const float2 t2 = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                                    sc2, ng2);
+                            const float p0 = fast_exp2(t2.x);
+                            const float p1 = fast_exp2(t2.y);
+                            acc[e & 3] = fadd2(acc[e & 3], make_float2(p0, p1));
+                            pp[e] = pack_f16x2(p0, p1);
+                        }
+                        tc::st_32x32b_x16(tp + ch * 16, pp);
+                        tl += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                               ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
+                              __uint_as_float((uint32_t)(127 - kc) << 23);
                     }
-                    tc::st_32x32b_x16(tp + ch * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pp[ch * 16]));
-                    if (!k_uniform) {  // quarters scaled differently: fold this chunk into l now
-                        l += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                              ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
-                             __uint_as_float((uint32_t)(127 - kc) << 23);
+                    return tl;
+                };
+                float tl = emit();
+                if (j > 0) {
+                    // every P * 2^-k at most 2^8 (so P fits fp16) unless the row's sum passes it
+                    const bool need = !(tl <= 256.f) || m_used == -INFINITY;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // the row max, a rescale of O and l, and P again (the P written above is
+                        // overwritten before p_full; rows that need nothing write the same P)
+                        const float mt = row_max() * sc;
+                        // O_x must hold the P.V of this query tile's previous key tile, product i - ntiles
+                        const uint32_t ip = i - ntiles;
+                        if (!wait_or_abort(&bars.pv_done[ip % NBP], (ip / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const float mn = fmaxf(m_used, mt);
+                        const float alpha = need && mn > m_used ? fast_exp2(m_used - mn) : 1.f;
+                        if (need && mn > m_used) {
+                            l *= alpha;
+                            m_used = mn;
+                        }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tc::ld_32x32b_x32(tO + c * 32, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tc::st_32x32b_x32(tO + c * 32, o);
+                        }
+                        tc::wait_st();  // the first P stores land before the second ones
+                        tl = emit();
                     }
                 }
-                if (k_uniform)
-                    l += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
-                         __uint_as_float((uint32_t)(127 - kq.x) << 23);
+                l += tl;
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
