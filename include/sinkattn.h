@@ -110,7 +110,22 @@ typedef struct sinkattn_paged_desc {
                                 * already complete when first tested (the first one never is:
                                 * its copy from HBM is in flight), and the prefill gives up
                                 * right after issuing its first copies. */
+    int32_t flags;             /* 0, or an OR of the SINKATTN_FLAG_* bits below; other bits:
+                                * SINKATTN_ERR_INVALID_ARG. */
 } sinkattn_paged_desc;
+
+/* Overlap of a prefill and the decode launched after it on the same stream (programmatic
+ * dependent launch).  A prefill given SINKATTN_FLAG_LAUNCH_NEXT_EARLY lets the next kernel on
+ * its stream start as soon as the prefill's own CTAs are running; a split-KV decode given
+ * SINKATTN_FLAG_START_EARLY is launched so that it may start then (otherwise, or after any
+ * other kernel, it starts when the kernel before it has completed).  With max_sms set so that
+ * the two grids fit side by side (the prefill's S SMs, the decode's on the other SMs), the two
+ * calls run at once on one stream, and the CTAs of each land on SMs of their own.  The decode
+ * must read nothing the prefill writes (the prefill writes only its out and lse).  The merge
+ * after the split-KV decode, and every later kernel on the stream, still wait for both.
+ * The one-launch sliding-window decode and the FP8 decode ignore SINKATTN_FLAG_START_EARLY. */
+#define SINKATTN_FLAG_LAUNCH_NEXT_EARLY 0x1
+#define SINKATTN_FLAG_START_EARLY 0x2
 
 /* Human-readable name of an error code (static string). */
 const char *sinkattn_error_string(int code);

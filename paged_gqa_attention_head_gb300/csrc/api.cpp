@@ -103,6 +103,7 @@ int check_heads(const sinkattn_paged_desc *d) {
     if (d->num_seqs < 0 || d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
         d->num_pages < 0 || d->max_pages_per_seq < 0 || d->max_sms < 0 || d->wait_limit_us < 0)
         return SINKATTN_ERR_INVALID_ARG;
+    if (d->flags & ~(SINKATTN_FLAG_LAUNCH_NEXT_EARLY | SINKATTN_FLAG_START_EARLY)) return SINKATTN_ERR_INVALID_ARG;
     if (d->num_qo_heads % d->num_kv_heads) return SINKATTN_ERR_INVALID_ARG;
     const int G = d->num_qo_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return SINKATTN_ERR_UNSUPPORTED;
@@ -223,6 +224,7 @@ int prepare_decode(const void *q, const int32_t *block_table, const int32_t *seq
     a.k_pages_w = nullptr;
     a.v_pages_w = nullptr;
     a.rope_on = 0;
+    a.start_early = (desc->flags & SINKATTN_FLAG_START_EARLY) != 0;
     a.rope_mscale = 1.f;
     return SINKATTN_OK;
 }
@@ -594,6 +596,7 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
     a.status = static_cast<uint32_t *>(workspace);
     a.fp8_prefix = fp8;
     a.causal = causal;
+    a.launch_dependents = (desc->flags & SINKATTN_FLAG_LAUNCH_NEXT_EARLY) != 0;
     a.sched = static_cast<uint32_t *>(workspace) + 16;  // header bytes 64..71
     a.k_scale = k_scale;
     a.v_scale = v_scale;

@@ -861,41 +861,49 @@ cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_
     return e;
 }
 
+namespace {
+// One launch of a split-KV kernel; with a.start_early it is a programmatic dependent of the
+// kernel before it on the stream (it may start once that kernel lets it).
+template <int D, bool kWindow, bool kAppend = false, bool kRope = false>
+cudaError_t launch_splitkv_d(const DecodeArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas,
+                             int smem_bytes, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(DecodeCfg<D>::kThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.start_early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, kWindow, kAppend, kRope>, kmap, vmap, a);
+}
+}  // namespace
+
 cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap &kmap,
                                   const CUtensorMap &vmap, int ctas, int smem_bytes,
                                   cudaStream_t stream) {
     const bool w = a.window > 0;
     if (a.k_new && a.rope_on) {  // decode with rotary embedding and append: same grid and plan
-        if (D == 64 && w)
-            decode_splitkv_kernel<64, true, true, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else if (D == 64)
-            decode_splitkv_kernel<64, false, true, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else if (w)
-            decode_splitkv_kernel<128, true, true, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else
-            decode_splitkv_kernel<128, false, true, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        return cudaGetLastError();
+        if (D == 64)
+            return w ? launch_splitkv_d<64, true, true, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+                     : launch_splitkv_d<64, false, true, true>(a, kmap, vmap, ctas, smem_bytes, stream);
+        return w ? launch_splitkv_d<128, true, true, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+                 : launch_splitkv_d<128, false, true, true>(a, kmap, vmap, ctas, smem_bytes, stream);
     }
     if (a.k_new) {  // decode with append: same grid and plan
-        if (D == 64 && w)
-            decode_splitkv_kernel<64, true, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else if (D == 64)
-            decode_splitkv_kernel<64, false, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else if (w)
-            decode_splitkv_kernel<128, true, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        else
-            decode_splitkv_kernel<128, false, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-        return cudaGetLastError();
+        if (D == 64)
+            return w ? launch_splitkv_d<64, true, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+                     : launch_splitkv_d<64, false, true>(a, kmap, vmap, ctas, smem_bytes, stream);
+        return w ? launch_splitkv_d<128, true, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+                 : launch_splitkv_d<128, false, true>(a, kmap, vmap, ctas, smem_bytes, stream);
     }
-    if (D == 64 && w)
-        decode_splitkv_kernel<64, true><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-    else if (D == 64)
-        decode_splitkv_kernel<64, false><<<ctas, DecodeCfg<64>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-    else if (w)
-        decode_splitkv_kernel<128, true><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-    else
-        decode_splitkv_kernel<128, false><<<ctas, DecodeCfg<128>::kThreads, smem_bytes, stream>>>(kmap, vmap, a);
-    return cudaGetLastError();
+    if (D == 64)
+        return w ? launch_splitkv_d<64, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+                 : launch_splitkv_d<64, false>(a, kmap, vmap, ctas, smem_bytes, stream);
+    return w ? launch_splitkv_d<128, true>(a, kmap, vmap, ctas, smem_bytes, stream)
+             : launch_splitkv_d<128, false>(a, kmap, vmap, ctas, smem_bytes, stream);
 }
 
 namespace {

@@ -50,6 +50,7 @@ struct DecodeArgs {
     float rope_mscale;
     float rope_hi[64];
     float rope_lo[64];
+    bool start_early;  // split-KV kernel: a programmatic dependent of the kernel before it
 };
 
 // Grid and shared memory of the split-KV decode kernel for head_dim D and
@@ -103,6 +104,7 @@ struct PrefillArgs {
     uint32_t *status;
     bool fp8_prefix;                   // the prefix pages are FP8 E4M3 codes (uint8)
     bool causal;                       // false: every query sees its whole request (no prefix, no window)
+    bool launch_dependents;            // the next kernel on the stream may start at once
     uint32_t *sched;                   // [2] in the workspace header: next item, CTAs done (zero between calls)
     const float *k_scale, *v_scale;    // FP8 prefix: [Hkv] per-KV-head scales, or nullptr (1)
 };

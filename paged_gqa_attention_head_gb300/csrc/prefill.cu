@@ -486,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vpmap, const PrefillArgs a) {
     using C = PrefillCfg<D>;
     constexpr int NS = C::kStages;
+    // the next kernel on the stream may start now (it takes the SMs this grid leaves free)
+    if (a.launch_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int NBS = C::kSBufs, NBP = C::kPBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &

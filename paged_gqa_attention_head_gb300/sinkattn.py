@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
 STATUS_BAD_PAGE, STATUS_BAD_LENGTH, STATUS_BAD_CU_SEQLENS, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS_VALUE_RANGE = 16
+FLAG_LAUNCH_NEXT_EARLY, FLAG_START_EARLY = 1, 2
 PAGE_SIZE = 16
 
 # every symbol the header declares, with (restype, argtypes)
@@ -31,7 +32,7 @@ class PagedDesc(ctypes.Structure):
     _fields_ = [("num_seqs", _I32), ("num_qo_heads", _I32), ("num_kv_heads", _I32),
                 ("head_dim", _I32), ("page_size", _I32), ("num_pages", _I32),
                 ("max_pages_per_seq", _I32), ("window", _I32), ("max_sms", _I32),
-                ("wait_limit_us", _I32)]
+                ("wait_limit_us", _I32), ("flags", _I32)]
 
 
 class RopeDesc(ctypes.Structure):
@@ -143,13 +144,15 @@ def workspace(nbytes: int, device: torch.device, tag: str = "default") -> torch.
 
 
 def paged_desc(num_seqs, num_qo_heads, num_kv_heads, head_dim, num_pages, max_pages_per_seq,
-               page_size=PAGE_SIZE, window=0, max_sms=0, wait_limit_us=0) -> PagedDesc:
+               page_size=PAGE_SIZE, window=0, max_sms=0, wait_limit_us=0, flags=0) -> PagedDesc:
     """window > 0: sliding window (each query sees the keys at its last `window`
     positions); 0: full attention.  max_sms > 0: the persistent decode and prefill grids
     use at most that many SMs (the rest stay free for concurrent work on other streams);
-    0: all SMs.  wait_limit_us > 0: give-up time of the kernels' pipeline waits (0: 2 s)."""
+    0: all SMs.  wait_limit_us > 0: give-up time of the kernels' pipeline waits (0: 2 s).
+    flags: FLAG_LAUNCH_NEXT_EARLY (prefill) / FLAG_START_EARLY (split-KV decode), the
+    overlap of a prefill and the decode after it on one stream."""
     return PagedDesc(num_seqs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
-                     max_pages_per_seq, int(window), int(max_sms), int(wait_limit_us))
+                     max_pages_per_seq, int(window), int(max_sms), int(wait_limit_us), int(flags))
 
 
 _ws_sizes: dict = {}
@@ -188,7 +191,7 @@ def _codes(t: torch.Tensor) -> torch.Tensor:
 
 
 def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, lse, ws,
-                 want_lse, window=0, kv_dtype=torch.bfloat16, max_sms=0, wait_limit_us=0):
+                 want_lse, window=0, kv_dtype=torch.bfloat16, max_sms=0, wait_limit_us=0, flags=0):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(k_pages, "k_pages", kv_dtype, dev, 4)
@@ -214,7 +217,7 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
     elif lse is not None:
         _need(lse, "lse", torch.float32, dev, 2)
     desc = paged_desc(B, Hq, Hkv, D, num_pages, block_table.shape[1], window=window,
-                      max_sms=max_sms, wait_limit_us=wait_limit_us)
+                      max_sms=max_sms, wait_limit_us=wait_limit_us, flags=flags)
     nbytes = decode_workspace_size(desc)
     if ws is None:
         ws = workspace(nbytes, dev)
@@ -225,12 +228,12 @@ def _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks, scale, out, 
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, sinks=None, scale=None, out=None, lse=None,
-           workspace_buf=None, return_lse=True, window=0, max_sms=0, wait_limit_us=0):
+           workspace_buf=None, return_lse=True, window=0, max_sms=0, wait_limit_us=0, flags=0):
     """Split-KV paged decode with sinks (sinkattn_decode).  window > 0: sliding window;
     max_sms > 0: the split-KV grid on at most that many SMs.  Returns (out, lse)."""
     desc, out, lse, ws, scale = _decode_prep(q, k_pages, v_pages, block_table, seq_lens, sinks,
                                              scale, out, lse, workspace_buf, return_lse, window,
-                                             max_sms=max_sms, wait_limit_us=wait_limit_us)
+                                             max_sms=max_sms, wait_limit_us=wait_limit_us, flags=flags)
     _check(load().sinkattn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                   _ptr(seq_lens), _ptr(sinks), scale, _ptr(out), _ptr(lse),
                                   ctypes.byref(desc), _ptr(ws), ws.numel(), _stream(q.device)),
@@ -261,7 +264,7 @@ def decode_merge(seq_lens, sinks, out, lse, desc, ws):
 
 def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=None,
             prefix_block_table=None, prefix_lens=None, out=None, lse=None, workspace_buf=None,
-            return_lse=True, window=0, max_sms=0, wait_limit_us=0):
+            return_lse=True, window=0, max_sms=0, wait_limit_us=0, flags=0):
     """Causal ragged prefill, optionally over a paged prefix (sinkattn_prefill).  window > 0:
     sliding window; max_sms > 0: the persistent grid on at most that many SMs.  Returns
     (out, lse)."""
@@ -289,7 +292,7 @@ def prefill(q, k, v, cu_seqlens, sinks=None, scale=None, k_pages=None, v_pages=N
     if lse is None and return_lse:
         lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
     desc = paged_desc(n, Hq, Hkv, D, num_pages, maxp, window=window, max_sms=max_sms,
-                      wait_limit_us=wait_limit_us)
+                      wait_limit_us=wait_limit_us, flags=flags)
     nbytes = prefill_workspace_size(desc)
     ws = workspace_buf if workspace_buf is not None else workspace(nbytes, dev, "prefill")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)

@@ -151,6 +151,21 @@ def test_noncausal_prefill_rejects_before_cuda(sa):
                                           256, None) == 1
 
 
+def test_flags_match_the_header_and_unknown_bits_are_rejected(sa):
+    text = open(HEADER).read()
+    for name in ("LAUNCH_NEXT_EARLY", "START_EARLY"):
+        m = re.search(r"#define SINKATTN_FLAG_%s (0x[0-9a-fA-F]+|\d+)" % name, text)
+        assert m, name
+        assert int(m.group(1), 0) == getattr(sa, "FLAG_" + name)
+    lib = sa.load()
+    size = ctypes.c_size_t(0)
+    ok = _desc(sa, flags=sa.FLAG_LAUNCH_NEXT_EARLY | sa.FLAG_START_EARLY)
+    assert lib.sinkattn_prefill_workspace_size(ctypes.byref(ok), ctypes.byref(size)) == 0
+    bad = _desc(sa, flags=4)
+    assert lib.sinkattn_prefill_workspace_size(ctypes.byref(bad), ctypes.byref(size)) == 1
+    assert lib.sinkattn_decode_workspace_size(ctypes.byref(bad), ctypes.byref(size)) == 1
+
+
 def test_desc_layout_matches_the_header(sa):
     """The binding's struct has the header's fields, in order, all int32."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)

@@ -96,3 +96,58 @@ def test_decode_on_fewer_sms_matches_the_oracle(sa, oracle_mod, cuda_dev, max_sm
     torch.cuda.synchronize()
     check_out(out, ro)
     check_lse(lse, rl)
+
+
+@pytest.mark.parametrize("split", [40, 100])
+def test_prefill_then_decode_started_early_on_one_stream(sa, cuda_dev, split):
+    """A chunked prefill that lets the next kernel start early (SINKATTN_FLAG_LAUNCH_NEXT_EARLY,
+    on `split` SMs) and a decode started early after it (SINKATTN_FLAG_START_EARLY, on the
+    other SMs), on one stream, in a captured graph and called directly: each result is bit for
+    bit that of the same call made alone, and the decode's merge waits for its split-KV pass."""
+    dev = cuda_dev
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    w = inputs.make_decode(("uniform", 200, 20000), 96, 64, 8, 64, seed=213, sinks=True)
+    c = w.cache
+    dargs = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
+             c.lens.to(dev), w.sinks.to(dev), w.scale)
+    p = inputs.make_prefill([700, 129, 512], 64, 8, 64, seed=214, sinks=True,
+                            prefix_lens=[3000, 0, 1200])
+    pre = p.prefix
+    pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+    pkw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
+               prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
+    dcap = n_sms - split
+    ref_d = tuple(t.clone() for t in sa.decode(*dargs, max_sms=dcap))
+    ref_p = tuple(t.clone() for t in sa.prefill(*pargs, **pkw, max_sms=split))
+    torch.cuda.synchronize()
+    dws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        w.q.shape[0], 64, 8, 64, c.k_pages.shape[0], c.block_table.shape[1], max_sms=dcap)),
+        dtype=torch.uint8, device=dev)
+    pws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    d_out, d_lse = torch.empty_like(ref_d[0]), torch.empty_like(ref_d[1])
+    p_out, p_lse = torch.empty_like(ref_p[0]), torch.empty_like(ref_p[1])
+
+    def step():
+        sa.prefill(*pargs, **pkw, out=p_out, lse=p_lse, workspace_buf=pws, max_sms=split,
+                   flags=sa.FLAG_LAUNCH_NEXT_EARLY)
+        sa.decode(*dargs, out=d_out, lse=d_lse, workspace_buf=dws, max_sms=dcap,
+                  flags=sa.FLAG_START_EARLY)
+
+    for _ in range(3):
+        d_out.fill_(0)
+        p_out.fill_(0)
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
+        assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        d_out.fill_(0)
+        p_out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
+        assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
+    assert sa.get_status(dws) == 0 and sa.get_status(pws) == 0
