@@ -685,7 +685,8 @@ def measure_rows(torch, sa, inputs, dev, stream, pk, peak_src):
                                  "frac_bf16": round(tf / pk["bf16_tflops"], 4), "flops": flops,
                                  "peak_source": f"{peak_src} bf16_tflops (burst)",
                                  "workload": "encoder_ragged: 2 x 4096 + 12 x 512 + 32 x 128 tokens, "
-                                             "16 / 8 heads, head_dim 128, no sinks", **st}
+                                             "16 / 8 heads, head_dim 128, no sinks",
+                                 "traffic": traffic_for("prefill_kernel", "encoder_ragged"), **st}
     del pargs
     # the long-context chunked prefill over an FP8 E4M3 prefix cache (the same FLOP)
     p = inputs.make_workload("longctx_chunked_fp8", seed=0)

@@ -361,7 +361,8 @@ WORKLOADS = {
     # (the lengths of the embedding benchmarks), attention heads of the Qwen3 family's small
     # models (16 query / 8 KV heads, head_dim 128), no sinks; non-causal attention
     "encoder_ragged": dict(kind="prefill", lens=[4096] * 2 + [512] * 12 + [128] * 32,
-                           num_qo_heads=16, num_kv_heads=8, head_dim=128, sinks=False),
+                           num_qo_heads=16, num_kv_heads=8, head_dim=128, sinks=False,
+                           causal=False),
     # the decode shapes over an FP8 E4M3 cache
     "gptoss_decode_fp8": dict(kind="decode", batch=64, lens=("uniform", 512, 8192),
                               num_qo_heads=64, num_kv_heads=8, head_dim=64, sinks=True,

@@ -3,7 +3,8 @@
   python -m paged_gqa_attention_head_gb300.run_workload <workload> [--iters N] [--op auto|append]
                                                          [--first N]
 
-Workloads are the seeded shapes in `inputs.WORKLOADS`.  `--first N` (decode workloads) keeps
+Workloads are the seeded shapes in `inputs.WORKLOADS` (a prefill marked causal=False runs
+through the non-causal entry point).  `--first N` (decode workloads) keeps
 the first N sequences of the batch, with the same lengths, in a pool of their own pages (a
 cut-down case whose device footprint suits a profiler capture).  Prints the mean time of
 the timed iterations (CUDA events) and the KV bytes one call reads; every launch goes
@@ -52,7 +53,10 @@ def main() -> None:
                       prefix_lens=w.prefix.lens.to(dev))
         t = (w.q.to(dev), w.k.to(dev), w.v.to(dev), w.cu_seqlens.to(dev),
              None if w.sinks is None else w.sinks.to(dev), w.scale)
-        fn = lambda: sa.prefill(*t, **kw)  # noqa: E731
+        if inputs.WORKLOADS[args.workload].get("causal", True):
+            fn = lambda: sa.prefill(*t, **kw)  # noqa: E731
+        else:
+            fn = lambda: sa.prefill_noncausal(*t)  # noqa: E731
     fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
