@@ -145,16 +145,24 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
                                          &L->warps_per_cta8, &L->smem8),
                  "fp8 decode launch shape");
     if (rc) return rc;
-    if (d->max_sms > 0) {
-        // both grids are (SMs x CTAs per SM); keep the CTAs per SM, on max_sms SMs
-        int sms = 0;
-        rc = cuda_rc(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
-                     "cudaDeviceGetAttribute");
-        if (rc) return rc;
-        if (d->max_sms < sms) {
-            L->ctas = L->ctas / sms * d->max_sms;
-            L->ctas8 = L->ctas8 / sms * d->max_sms;
-        }
+    // Both grids are (SMs x CTAs per SM); keep the CTAs per SM, on fewer SMs' worth of CTAs
+    // where max_sms asks for it.  The bf16 split-KV grid also stops at about two thirds of the
+    // SMs' worth: with every SM at full occupancy its rings hold ~29 MB of page reads in
+    // flight, and HBM delivered 5-6 % less than with ~19 MB (measured on GB300 for the
+    // long-context, Qwen3-shape and gpt-oss decode batches: best at 104 of 152 SMs' worth at
+    // head_dim 64, 96 at head_dim 128; the block scheduler still spreads the CTAs over every SM).
+    int sms = 0;
+    rc = cuda_rc(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
+                 "cudaDeviceGetAttribute");
+    if (rc) return rc;
+    if (sms > 0) {
+        const int per_sm = L->ctas / sms, per_sm8 = L->ctas8 / sms;
+        int use = sms, use8 = sms;
+        if (d->max_sms > 0 && d->max_sms < sms) use = use8 = d->max_sms;
+        const int keep = (sms * (d->head_dim == 64 ? 104 : 96) + 151) / 152;
+        if (use > keep) use = keep;
+        L->ctas = per_sm * use;
+        L->ctas8 = per_sm8 * use8;
     }
     L->total_warps = L->ctas * L->warps_per_cta;
     L->total_warps8 = L->ctas8 * L->warps_per_cta8;
