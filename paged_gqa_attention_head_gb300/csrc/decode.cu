@@ -239,11 +239,25 @@ __device__ __forceinline__ void page_step(const DecodeArgs &a, const uint8_t *kb
         }
     const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
     const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
+    // the running max is raised only when a score passes it by more than 8 (log2 units), so
+    // P = exp2(s - m) <= 2^8 and most pages leave the accumulators as they are
+    if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+        const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+        const float al0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mn0);
+        const float al1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int n = 0; n < kN; ++n) {
+            acc[n][0] *= al0;
+            acc[n][1] *= al0;
+            acc[n][2] *= al1;
+            acc[n][3] *= al1;
+        }
+        l0 *= al0;
+        l1 *= al1;
+    }
+    const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
     float p[2][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
@@ -252,15 +266,8 @@ __device__ __forceinline__ void page_step(const DecodeArgs &a, const uint8_t *kb
         p[n][2] = fast_exp2(s[n][2] - base1);
         p[n][3] = fast_exp2(s[n][3] - base1);
     }
-#pragma unroll
-    for (int n = 0; n < kN; ++n) {
-        acc[n][0] *= al0;
-        acc[n][1] *= al0;
-        acc[n][2] *= al1;
-        acc[n][3] *= al1;
-    }
-    l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-    l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+    l0 += (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+    l1 += (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
     // P = P_hi + P_lo, both bf16: the rounding of P to bf16 alone (relative 2^-9)
     // is too coarse for short sequences, the pair keeps ~16 bits
     uint32_t ph[4], pl[4];
