@@ -151,3 +151,26 @@ def test_prefill_then_decode_started_early_on_one_stream(sa, cuda_dev, split):
         assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
         assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
     assert sa.get_status(dws) == 0 and sa.get_status(pws) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_grid_stops_at_its_cap(sa, cuda_dev, D):
+    """The split-KV grid stops at 104 (head_dim 64) or 96 (128) of 152 SMs' worth of CTAs,
+    scaled to the device: a cap at or above that gives the same grid and bits as none."""
+    dev = cuda_dev
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    keep = (n_sms * (104 if D == 64 else 96) + 151) // 152
+    w = inputs.make_decode(("uniform", 100, 6000), 40, 16, 2, D, seed=215 + D, sinks=True)
+    c = w.cache
+    args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
+            w.sinks.to(dev), w.scale)
+    shape = (w.q.shape[0], 16, 2, D, c.k_pages.shape[0], c.block_table.shape[1])
+    assert sa.decode_workspace_size(sa.paged_desc(*shape, max_sms=n_sms)) == \
+        sa.decode_workspace_size(sa.paged_desc(*shape))
+    ref = sa.decode(*args)
+    torch.cuda.synchronize()
+    ref = tuple(t.clone() for t in ref)
+    for m in (keep, n_sms):
+        out, lse = sa.decode(*args, max_sms=m)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
