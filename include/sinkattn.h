@@ -416,9 +416,10 @@ int sinkattn_prefill_noncausal(const void *q, const void *k, const void *v, cons
  * and finite).  The new tokens' k, v stay bf16 (a serving step appends them to the FP8 cache
  * with sinkattn_append_kv_fp8 for later steps).  The prefix tiles are copied as codes and
  * converted in shared memory: K exactly to bf16 code values, the K scale multiplying those
- * tiles' scores; V to fp16 of value * 2^-k, one k per KV head from the format's largest value
- * (448 * v_scale < 2^15 * 2^k; k = 0 for any v_scale below 73; k > 7 sets
- * SINKATTN_STATUS_VALUE_RANGE), relative rounding <= 2^-11 as for bf16 V tiles.  NaN codes in
+ * tiles' scores.  V: with v_scale = m * 2^e (m in [1, 2), -12 <= e <= 6, i.e. 2^-12 <= v_scale
+ * < 128) to code * 2^e, exact in fp16, the softmax multiplying those keys' P by m; other scales
+ * to fp16 of value * 2^-k, one k per KV head from the format's largest value (448 * v_scale <
+ * 2^15 * 2^k; k > 7 sets SINKATTN_STATUS_VALUE_RANGE), relative rounding <= 2^-11.  NaN codes in
  * visible keys give unspecified outputs.  All four prefix
  * pointers and the prefix lengths are required; other arguments, workspace and errors as
  * for sinkattn_prefill. */

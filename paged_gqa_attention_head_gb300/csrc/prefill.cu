@@ -173,22 +173,32 @@ __device__ __forceinline__ uint32_t f16x2_scaled(uint32_t h, float sc) {
     return pack_f16x2(lo * sc, hi * sc);
 }
 
-// Eight E4M3 codes (two words) to one 16-byte vector: bf16 code values (kToBf16) or fp16
-// code values times sc.
-template <bool kToBf16>
-__device__ __forceinline__ uint4 codes8(uint32_t w0, uint32_t w1, float sc) {
+// Two f16 values times a power of two (given as an f16 pair), exact when the results stay
+// f16 normals or exact subnormals.
+__device__ __forceinline__ uint32_t f16x2_pow2(uint32_t h, uint32_t p2) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(p2));
+    return r;
+}
+
+// Eight E4M3 codes (two words) to one 16-byte vector: bf16 code values (kMode 0), fp16 code
+// values times sc (1), or fp16 code values times the power of two p2 (2).
+template <int kMode>
+__device__ __forceinline__ uint4 codes8(uint32_t w0, uint32_t w1, float sc, uint32_t p2) {
     const uint32_t h0 = e4m3x2_lo_to_f16x2(w0), h1 = e4m3x2_hi_to_f16x2(w0);
     const uint32_t h2 = e4m3x2_lo_to_f16x2(w1), h3 = e4m3x2_hi_to_f16x2(w1);
-    if (kToBf16) return make_uint4(f16x2_to_bf16x2(h0), f16x2_to_bf16x2(h1), f16x2_to_bf16x2(h2), f16x2_to_bf16x2(h3));
+    if (kMode == 0) return make_uint4(f16x2_to_bf16x2(h0), f16x2_to_bf16x2(h1), f16x2_to_bf16x2(h2), f16x2_to_bf16x2(h3));
+    if (kMode == 2) return make_uint4(f16x2_pow2(h0, p2), f16x2_pow2(h1, p2), f16x2_pow2(h2, p2), f16x2_pow2(h3, p2));
     return make_uint4(f16x2_scaled(h0, sc), f16x2_scaled(h1, sc), f16x2_scaled(h2, sc), f16x2_scaled(h3, sc));
 }
 
 // One converter warp's quarter of an FP8 prefix tile (keys 32q .. 32q + 31, pages 2q and
 // 2q + 1) from its staged codes to 128-byte swizzled rows in place: bf16 code values for K,
-// fp16 code values times sc for V.  Every lane reads its codes of a page (or half page)
-// before any lane writes, since the rows written cover the codes staged.
-template <int D, bool kToBf16>
-__device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane, float sc) {
+// fp16 code values times sc (kMode 1) or times the power of two p2 (kMode 2) for V.  Every
+// lane reads its codes of a page (or half page) before any lane writes, since the rows
+// written cover the codes staged.
+template <int D, int kMode>
+__device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane, float sc, uint32_t p2 = 0) {
     using C = PrefillCfg<D>;
 #pragma unroll 1
     for (int i = 0; i < 2; ++i) {
@@ -200,10 +210,10 @@ __device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane,
             const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 64 + h * 32);
             const uint4 y = *reinterpret_cast<const uint4 *>(src + r * 64 + h * 32 + 16);
             __syncwarp();
-            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 0)) = codes8<kToBf16>(x.x, x.y, sc);
-            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 1)) = codes8<kToBf16>(x.z, x.w, sc);
-            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 2)) = codes8<kToBf16>(y.x, y.y, sc);
-            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 3)) = codes8<kToBf16>(y.z, y.w, sc);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 0)) = codes8<kMode>(x.x, x.y, sc, p2);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 1)) = codes8<kMode>(x.z, x.w, sc, p2);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 2)) = codes8<kMode>(y.x, y.y, sc, p2);
+            *reinterpret_cast<uint4 *>(t + sw128(16 * p + r, 4 * h + 3)) = codes8<kMode>(y.z, y.w, sc, p2);
         } else {
             // two passes of eight rows: lane: row r, codes 32 h4 .. 32 h4 + 31 -> column block
             // h4 / 2, chunks 4 (h4 % 2) .. + 3 (the rows of block 1 are where the codes sit)
@@ -215,10 +225,10 @@ __device__ __forceinline__ void convert_fp8_quarter(uint8_t *t, int q, int lane,
                 __syncwarp();
                 uint8_t *blk = t + (h4 >> 1) * 16384;
                 const int c0 = 4 * (h4 & 1);
-                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 0)) = codes8<kToBf16>(x.x, x.y, sc);
-                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 1)) = codes8<kToBf16>(x.z, x.w, sc);
-                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 2)) = codes8<kToBf16>(y.x, y.y, sc);
-                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 3)) = codes8<kToBf16>(y.z, y.w, sc);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 0)) = codes8<kMode>(x.x, x.y, sc, p2);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 1)) = codes8<kMode>(x.z, x.w, sc, p2);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 2)) = codes8<kMode>(y.x, y.y, sc, p2);
+                *reinterpret_cast<uint4 *>(blk + sw128(16 * p + r, c0 + 3)) = codes8<kMode>(y.z, y.w, sc, p2);
                 __syncwarp();
             }
         }
@@ -896,8 +906,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // FP8 V: |value| <= 448 * v_scale, so one exponent k per item keeps every converted
             // value below 2^15 (k = 0 for any scale below 73): no per-tile maximum needed
             const float vsc = kFp8 ? s_slot[k % kItemRing].vscale : 1.f;
+            // v_scale = m * 2^e8 with m in [1, 2): for -12 <= e8 <= 6 the V codes become
+            // code * 2^e8, exact in fp16 and below 2^15, and the softmax multiplies those keys'
+            // P by m; other scales take the exponent k below
+            const int e8 = (int)((__float_as_uint(vsc) >> 23) & 0xFFu) - 127;
+            const bool fold8 = kFp8 && e8 >= -12 && e8 <= 6;
+            const uint32_t p2e8 = (uint32_t)(e8 + 15) << 10 | (uint32_t)(e8 + 15) << 26;  // f16 pair 2^e8
             int kexp8 = 0;
-            if (kFp8) {
+            if (kFp8 && !fold8) {
                 const float top = 448.f * vsc;
                 kexp8 = max(0, (int)((__float_as_uint(top) >> 23) & 0xFFu) - 127 - 14);
                 if (!(top < INFINITY) || kexp8 > 7) {
@@ -916,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (fp8_tile) convert_fp8_quarter<D, true>(sK + st * C::kKVBytes, q, lane, 1.f);
+                    if (fp8_tile) convert_fp8_quarter<D, 0>(sK + st * C::kKVBytes, q, lane, 1.f);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.k_conv[st]);
@@ -927,9 +943,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (fp8_tile) {
-                    // V: fp16 of value * 2^-k, value = scale * e4m3(code), k of the item
-                    convert_fp8_quarter<D, false>(sV + st * C::kKVBytes, q, lane, vmul8);
-                    if (lane == 0) s_vscale[st * 4 + q] = kexp8;
+                    // V: code * 2^e8 (the softmax takes the rest of the scale), or fp16 of
+                    // value * 2^-k, value = scale * e4m3(code), k of the item
+                    if (fold8)
+                        convert_fp8_quarter<D, 2>(sV + st * C::kKVBytes, q, lane, 1.f, p2e8);
+                    else
+                        convert_fp8_quarter<D, 1>(sV + st * C::kKVBytes, q, lane, vmul8);
+                    if (lane == 0) s_vscale[st * 4 + q] = fold8 ? 0 : kexp8;
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars.v_conv[st]);
@@ -1013,6 +1033,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float sink2 = s_slot[k % kItemRing].sink2[x];
             // score scale of FP8 prefix tiles: their K holds code values, the K scale joins here
             const float sc_pre = kFp8 ? a.scale_log2 * s_slot[k % kItemRing].kscale : a.scale_log2;
+            // FP8 prefix V in the converters' power-of-two form: P of those keys times m8, the
+            // mantissa of v_scale (m8 in [1, 2), so P * m8 < 2^9 stays in fp16)
+            const float vsc8 = kFp8 ? s_slot[k % kItemRing].vscale : 1.f;
+            const int e8 = (int)((__float_as_uint(vsc8) >> 23) & 0xFFu) - 127;
+            const bool fold8 = kFp8 && e8 >= -12 && e8 <= 6;
+            const float m8 = fold8 ? __uint_as_float((__float_as_uint(vsc8) & 0x807FFFFFu) | 0x3F800000u) : 1.f;
+            const float add8 = log2f(m8), mul8 = 1.f / m8;
             float m_used = sink2;                      // running max, seeded with the sink
             float l = sink2 == -INFINITY ? 0.f : 1.f;  // running denominator: e^(sink - m) = 1
             for (int j = 0; j < gm.n_kv; ++j) {
@@ -1106,13 +1133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
                 const float2 sc2 = make_float2(sc, sc);
                 // writes P against the running max m_used; returns the row's sum of P * 2^-k
+                const bool f8 = kFp8 && fold8 && tt < gm.n_pre;  // warp-uniform
                 auto emit = [&]() {
                     const float neg0 = m_used == -INFINITY ? 0.f : -m_used;
                     float tl = 0.f;
 #pragma unroll
                     for (int ch = 0; ch < kBN / 32; ++ch) {
                         const int kc = ch == 0 ? kq.x : ch == 1 ? kq.y : ch == 2 ? kq.z : kq.w;
-                        const float neg = neg0 + (float)kc;
+                        const float neg = neg0 + (f8 ? add8 : (float)kc);
                         const float2 ng2 = make_float2(neg, neg);
                         // running sums of keys c with c % 8 = 2q (.x) and 2q + 1 (.y)
                         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -1131,7 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::st_32x32b_x16(tp + ch * 16, pp);
                         tl += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
                                ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
-                              __uint_as_float((uint32_t)(127 - kc) << 23);
+                              (f8 ? mul8 : __uint_as_float((uint32_t)(127 - kc) << 23));
                     }
                     return tl;
                 };

@@ -142,3 +142,24 @@ def test_prefill_fp8_large_v_scale(sa, oracle_mod, cuda_dev):
     d["vs"] = torch.tensor([700.0, 20000.0], dtype=torch.float32, device=cuda_dev)
     _run(sa, p, d)
     assert sa.get_status(ws) & sa.STATUS_VALUE_RANGE
+
+
+@pytest.mark.parametrize("vs", [100.0, 1.5 * 2.0 ** -12, 127.9, 2.0 ** -12])
+def test_prefill_fp8_v_scale_at_the_power_of_two_form_edges(sa, oracle_mod, cuda_dev, vs):
+    """V scales m * 2^e with e from -12 to 6 take the form in which the converters write
+    code * 2^e (exact in fp16) and the softmax multiplies those keys' P by m; these sit at both
+    ends of that range (the values are the N(0,1) data scaled by vs / the old scale)."""
+    p = inputs.make_prefill([150, 40], 8, 2, 64, seed=141, sinks=True, prefix_lens=[260, 129],
+                            prefix_kv_dtype="fp8")
+    c = p.prefix
+    old = c.v_scale.clone()
+    c.v_scale = torch.full_like(c.v_scale, vs)
+    mag = np.maximum(1.0, (c.v_scale / old).double().repeat_interleave(4).numpy())[None, :, None]
+    d = _dev_prefill(p, cuda_dev)
+    ws = sa.workspace(256, cuda_dev, "prefill")
+    sa.get_status(ws)
+    out, lse = _run(sa, p, d)
+    assert sa.get_status(ws) == 0
+    ro, rl = _oracle(oracle_mod, p)
+    check_out(out, ro, what=f"fp8-prefix prefill, V scale {vs}", v_mag=mag)
+    check_lse(lse, rl, what=f"fp8-prefix lse, V scale {vs}")
