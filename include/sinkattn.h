@@ -374,7 +374,7 @@ int sinkattn_decode_noalloc(const void *q, const void *k_pages, const void *v_pa
  * k_pages, v_pages, prefix_block_table [num_seqs, max_pages_per_seq], prefix_lens
  *             [num_seqs]: the paged prefix; all four NULL for a plain causal prefill
  * sinks, scale, lse: as for decode, with lse [T, Hq]; scale must be positive and finite
- * out:        bf16 [T, Hq, D]
+ * out:        bf16 [T, Hq, D], 32-byte aligned (the other data pointers 16-byte aligned)
  * desc:       num_seqs, heads, head_dim, page_size; num_pages and max_pages_per_seq
  *             describe the prefix pages (ignored without a prefix)
  * workspace:  at least sinkattn_prefill_workspace_size bytes: the 256-byte header only,

@@ -549,7 +549,8 @@ int prefill_common(const void *q, const void *k, const void *v, const int32_t *c
     if (!(scale > 0.f) || !(scale < INFINITY)) return SINKATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !cu_seqlens || !out || !workspace) return SINKATTN_ERR_INVALID_ARG;
     if (ws_bytes < kStatusBytes) return SINKATTN_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+    // out: 32-byte stores of the output rows
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 32) ||
         !aligned(workspace, kAlign) || !aligned(cu_seqlens, 4) || (sinks && !aligned(sinks, 4)) ||
         (lse && !aligned(lse, 4)))
         return SINKATTN_ERR_INVALID_ARG;

@@ -1222,13 +1222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::wait_ld();
                 if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(og + c * 32 + e) = w;
+                    for (int e = 0; e < 32; e += 16) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            w[u] = pack_bf16x2(__uint_as_float(o[e + 2 * u]) * inv, __uint_as_float(o[e + 2 * u + 1]) * inv);
+                        st_global_v8(og + c * 32 + e, w);  // 32 bytes; the output rows are 32-byte aligned
                     }
                 }
             }

@@ -122,6 +122,11 @@ def test_misaligned_pointers_rejected(sa):
     rc = lib.sinkattn_prefill(p16 + 2, p16, p16, p16, 8, None, None, None, None, None, 0.125,
                               p16, None, ctypes.byref(d), (base + 255) // 256 * 256, 256, None)
     assert rc == 1
+    # a prefill whose out is 16-byte but not 32-byte aligned
+    p32 = (base + 31) // 32 * 32
+    rc = lib.sinkattn_prefill(p16, p16, p16, p16, 8, None, None, None, None, None, 0.125,
+                              p32 + 16, None, ctypes.byref(d), (base + 255) // 256 * 256, 256, None)
+    assert rc == 1
 
 
 def test_prefix_arguments_all_or_nothing(sa):
