@@ -174,3 +174,40 @@ def test_decode_grid_stops_at_its_cap(sa, cuda_dev, D):
         out, lse = sa.decode(*args, max_sms=m)
         torch.cuda.synchronize()
         assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+@pytest.mark.slow
+def test_long_context_step_with_early_start_matches_the_calls_alone(sa, cuda_dev):
+    """The long-context mixed step in the launch configuration the benchmark times (chunked
+    prefill on 76 SMs starting the decode early, the decode on the others): bit for bit the
+    results of the two calls made alone with the same SM caps."""
+    dev = cuda_dev
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    S = min(76, n_sms // 2)
+    w = inputs.make_workload("longctx_decode", seed=0)
+    c = w.cache
+    dargs = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
+             w.sinks.to(dev), w.scale)
+    p = inputs.make_workload("longctx_chunked", seed=0)
+    pre = p.prefix
+    pargs = (p.q.to(dev), p.k.to(dev), p.v.to(dev), p.cu_seqlens.to(dev), p.sinks.to(dev), p.scale)
+    pkw = dict(k_pages=pre.k_pages.to(dev), v_pages=pre.v_pages.to(dev),
+               prefix_block_table=pre.block_table.to(dev), prefix_lens=pre.lens.to(dev))
+    ref_d = tuple(t.clone() for t in sa.decode(*dargs, max_sms=n_sms - S))
+    ref_p = tuple(t.clone() for t in sa.prefill(*pargs, **pkw, max_sms=S))
+    torch.cuda.synchronize()
+    d_out, d_lse = torch.empty_like(ref_d[0]), torch.empty_like(ref_d[1])
+    p_out, p_lse = torch.empty_like(ref_p[0]), torch.empty_like(ref_p[1])
+    dws = torch.zeros(sa.decode_workspace_size(sa.paged_desc(
+        w.q.shape[0], 64, 8, 64, c.k_pages.shape[0], c.block_table.shape[1], max_sms=n_sms - S)),
+        dtype=torch.uint8, device=dev)
+    pws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        sa.prefill(*pargs, **pkw, out=p_out, lse=p_lse, workspace_buf=pws, max_sms=S,
+                   flags=sa.FLAG_LAUNCH_NEXT_EARLY)
+        sa.decode(*dargs, out=d_out, lse=d_lse, workspace_buf=dws, max_sms=n_sms - S,
+                  flags=sa.FLAG_START_EARLY)
+        torch.cuda.synchronize()
+        assert torch.equal(d_out, ref_d[0]) and torch.equal(d_lse, ref_d[1])
+        assert torch.equal(p_out, ref_p[0]) and torch.equal(p_lse, ref_p[1])
+    assert sa.get_status(dws) == 0 and sa.get_status(pws) == 0
