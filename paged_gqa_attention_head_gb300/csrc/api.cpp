@@ -148,8 +148,8 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
     // Both grids are (SMs x CTAs per SM); keep the CTAs per SM, on fewer SMs' worth of CTAs
     // where max_sms asks for it.  The bf16 split-KV grid also stops at about two thirds of the
     // SMs' worth: with every SM at full occupancy its rings hold ~29 MB of page reads in
-    // flight, and HBM delivered 5-6 % less than with ~19 MB (measured on GB300 for the
-    // long-context, Qwen3-shape and gpt-oss decode batches: best at 104 of 152 SMs' worth at
+    // flight, and HBM delivered 5-6 % less than with ~18 MB (measured on GB300 for the
+    // long-context, Qwen3-shape and gpt-oss decode batches: best at 92 of 152 SMs' worth at
     // head_dim 64, 96 at head_dim 128; the block scheduler still spreads the CTAs over every SM).
     int sms = 0;
     rc = cuda_rc(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
@@ -159,7 +159,7 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
         const int per_sm = L->ctas / sms, per_sm8 = L->ctas8 / sms;
         int use = sms, use8 = sms;
         if (d->max_sms > 0 && d->max_sms < sms) use = use8 = d->max_sms;
-        const int keep = (sms * (d->head_dim == 64 ? 104 : 96) + 151) / 152;
+        const int keep = (sms * (d->head_dim == 64 ? 92 : 96) + 151) / 152;
         if (use > keep) use = keep;
         L->ctas = per_sm * use;
         L->ctas8 = per_sm8 * use8;

@@ -14,8 +14,10 @@
 // whatever the length mix.  Each warp streams its pages through a private ring
 // of shared-memory stages filled by TMA (4-D tensor maps over the page pool,
 // 128-byte swizzle; the grid is as many 4-warp CTAs as fit on every SM), and
-// computes all G query heads of the KV head with
-// m16n8k16 tensor-core MMAs (heads on the M axis, 16 tokens of a page on N).
+// computes all G query heads of the KV head with m16n8k16 tensor-core MMAs taken
+// transposed: S^T = K Q^T (the 16 tokens of a page on the M axis) and O^T = V^T P^T
+// (head_dim on M), the heads on the N axis in tiles of 8, so that a group of up to 8
+// heads is not padded to the 16 rows of an A operand.
 // A (sequence, KV head) that one warp covers entirely is finished in place with
 // the sink folded in; otherwise the warp leaves a sink-free partial state and
 // the merge kernel combines the pieces and adds the sink.
@@ -62,8 +64,7 @@ struct DecodeCfg {
     static constexpr int kPageBytes = kPageSize * D * 2;  // one (page, head) of K or of V
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kWarpBytes = kStages * kStageBytes;
-    static constexpr int kKSteps = D / 16;
-    static constexpr int kNTiles = D / 8;
+    static constexpr int kKSteps = D / 16;  // k-steps of S^T over head_dim; m-tiles of O^T
 };
 
 template <int D>
@@ -112,11 +113,16 @@ __device__ __forceinline__ void rope_pairs(uint32_t &lo_w, uint32_t &hi_w, float
 
 
 // ---------------------------------------------------------------- per-warp page work
-// Shared by the split-KV kernel and the sliding-window kernel.  A warp holds the G query
-// rows of one (sequence, KV head) as m16n8k16 A fragments (rows = heads, padded to 16),
-// and an online-softmax state: running max m0 / m1 and per-lane partial sums l0 / l1 of
-// rows gr and gr + 8 (log2 domain), unnormalised output acc (rows gr, gr + 8; columns
-// n * 8 + tc, tc + 1).
+// Shared by the split-KV kernel and the sliding-window kernel.  The products are taken
+// transposed, S^T = K Q^T and O^T = V^T P^T: a page's 16 tokens are the M axis of the
+// first and the head_dim that of the second, and the G query heads of the group the N
+// axis of both, in NH tiles of 8 heads (NH = 1 for G <= 8).  A page then costs D/16 MMAs
+// per 8 heads for S and 2 D/16 for O (P as a bf16 pair), half of what padding G <= 8
+// heads to the 16 rows of an A operand costs.  A warp holds for one (sequence, KV head):
+//   qb[kk][nt]   q as B fragments: head 8nt + gr, head_dim columns 16kk + tc, +1 / +8, +9;
+//   acc[mt][nt]  the unnormalised O^T: head_dim rows 16mt + gr / +8, heads 8nt + tc, +1;
+//   mr[nt][e]    the running max of head 8nt + tc + e (log2 domain, equal in the 8 lanes
+//                that share lane & 3), ls[nt][e] this lane's partial sum of its P.
 
 // Rows nv..15 of a V stage past the sequence end (or of a skipped page) may hold
 // anything, even NaN; P is 0 there but 0 * NaN is not 0, so clear them.
@@ -131,21 +137,30 @@ __device__ __forceinline__ void clear_v_tail(uint8_t *vb, int nv, int lane) {
     __syncwarp();
 }
 
-// Decode with append: the new K/V row of (b, g) - the token at position L - 1, slot
-// (L - 1) % 16 of physical page pg - taken from the inputs (the key rotated first with
-// kRope), written over its slot in the stage (the copy read the slot before the row
-// existed) and into the cache.  Warp-uniform; every lane calls it.
+// Decode with append: the new K/V row of (b, g) as 16-byte chunks, lane l < D/8 holding
+// chunk l of the key and lane D/8 + l chunk l of the value.  Loaded when a warp starts the
+// segment that holds the row's page, so the load overlaps the pages before it.
+template <int D>
+__device__ __forceinline__ uint4 load_new_row(const DecodeArgs &a, int b, int g, int lane) {
+    constexpr int kChunks = D / 8;  // 16-byte chunks of one row
+    const bool isv = lane >= kChunks;
+    const int64_t row = ((int64_t)b * a.Hkv + g) * D + (lane % kChunks) * 8;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (lane < 2 * kChunks)
+        w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(isv ? a.v_new : a.k_new) + row);
+    return w;
+}
+
+// ... and that row - the token at position L - 1, slot (L - 1) % 16 of physical page pg -
+// (the key rotated first with kRope) written over its slot in the stage (the copy read the
+// slot before the row existed) and into the cache.  Warp-uniform; every lane calls it.
 template <int D, bool kRope>
 __device__ __forceinline__ void append_row(const DecodeArgs &a, int b, int g, int L, int pg, uint8_t *kb,
-                                           uint8_t *vb, int lane) {
+                                           uint8_t *vb, uint4 w, int lane) {
     constexpr int kChunks = D / 8;  // 16-byte chunks of one row
     const int slot = (L - 1) % kPageSize;
     const bool isv = lane >= kChunks;
     const int ck = lane % kChunks;
-    const int64_t row = ((int64_t)b * a.Hkv + g) * D + ck * 8;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (lane < 2 * kChunks)
-        w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(isv ? a.v_new : a.k_new) + row);
     if (kRope) {
         // NeoX pairs: chunk ck (elements 8ck .. 8ck + 7) with chunk ck ^ (kChunks / 2)
         uint4 o;
@@ -177,21 +192,24 @@ __device__ __forceinline__ void append_row(const DecodeArgs &a, int b, int g, in
     __syncwarp();
 }
 
-// The G query rows of (b, g) as A fragments; with kRope rotated at position L - 1.
-template <int D, bool kRope>
-__device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int g, int L, uint32_t (&qa)[D / 16][4],
+// The G query rows of (b, g) as B fragments (heads past G zero); with kRope rotated at
+// position L - 1.
+template <int D, int NH, bool kRope>
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int g, int L, uint32_t (&qb)[D / 16][NH][2],
                                        int lane) {
     constexpr int kK = D / 16;
     const int gr = lane >> 2, tc = (lane & 3) * 2;
     const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * a.G) * D;
 #pragma unroll
-    for (int kk = 0; kk < kK; ++kk) {
-        const int col = kk * 16 + tc;
-        const bool r0 = gr < a.G, r1 = gr + 8 < a.G;
-        qa[kk][0] = r0 ? *reinterpret_cast<const uint32_t *>(qg + gr * D + col) : 0u;
-        qa[kk][1] = r1 ? *reinterpret_cast<const uint32_t *>(qg + (gr + 8) * D + col) : 0u;
-        qa[kk][2] = r0 ? *reinterpret_cast<const uint32_t *>(qg + gr * D + col + 8) : 0u;
-        qa[kk][3] = r1 ? *reinterpret_cast<const uint32_t *>(qg + (gr + 8) * D + col + 8) : 0u;
+    for (int nt = 0; nt < NH; ++nt) {
+        const int h = nt * 8 + gr;
+        const bool ok = h < a.G;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const int col = kk * 16 + tc;
+            qb[kk][nt][0] = ok ? *reinterpret_cast<const uint32_t *>(qg + h * D + col) : 0u;
+            qb[kk][nt][1] = ok ? *reinterpret_cast<const uint32_t *>(qg + h * D + col + 8) : 0u;
+        }
     }
     if (kRope) {
         // the query rows turn at the new token's position: column c < D/2 (register step
@@ -204,130 +222,187 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int g, int L,
                 const int i0 = kk * 16 + tc + x * 8;
                 const float2 cs0 = rope_cs(p, a.rope_hi[i0], a.rope_lo[i0], a.rope_mscale);
                 const float2 cs1 = rope_cs(p, a.rope_hi[i0 + 1], a.rope_lo[i0 + 1], a.rope_mscale);
-                rope_pairs(qa[kk][2 * x], qa[kk + kK / 2][2 * x], cs0, cs1);          // row gr
-                rope_pairs(qa[kk][2 * x + 1], qa[kk + kK / 2][2 * x + 1], cs0, cs1);  // row gr + 8
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) rope_pairs(qb[kk][nt][x], qb[kk + kK / 2][nt][x], cs0, cs1);
             }
     }
 }
 
-// One page: S = Q K^T for its 16 tokens (keys klo .. nv - 1 visible), the online-softmax
-// update and O += P V.
-template <int D, bool kWindow>
+// One page: S^T = K Q^T for its 16 tokens (keys klo .. nv - 1 visible), the online-softmax
+// update and O^T += V^T P^T.
+template <int D, int NH, bool kWindow>
 __device__ __forceinline__ void page_step(const DecodeArgs &a, const uint8_t *kb, const uint8_t *vb, int nv,
-                                          int klo, const uint32_t (&qa)[D / 16][4], float (&acc)[D / 8][4],
-                                          float &m0, float &m1, float &l0, float &l1, int lane) {
-    constexpr int kK = D / 16, kN = D / 8;
-    const int tc = (lane & 3) * 2;
+                                          int klo, const uint32_t (&qb)[D / 16][NH][2],
+                                          float (&acc)[D / 16][NH][4], float (&mr)[NH][2], float (&ls)[NH][2],
+                                          int lane) {
+    constexpr int kK = D / 16;
+    const int gr = lane >> 2;
     const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix index, row within it
-    // S = Q K^T for the 16 tokens of this page (two n-tiles of 8 tokens)
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S^T: rows tokens gr / gr + 8, columns heads 8nt + tc, +1
+    float s[NH][4];
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     const uint32_t kbase = smem_u32(kb);
 #pragma unroll
     for (int kk = 0; kk < kK; ++kk) {
-        const int tok = (lm >> 1) * 8 + lr, chunk = kk * 2 + (lm & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), b0, b1, b2, b3);
-        mma_16816(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-        mma_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        // A fragments of K: tokens 0-7 / 8-15 (matrices 0, 2 / 1, 3), columns 16kk..+7 / +8..15
+        const int tok = (lm & 1) * 8 + lr, chunk = kk * 2 + (lm >> 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) mma_16816(s[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
     }
+    const bool ok0 = gr < nv && (!kWindow || gr >= klo), ok1 = gr + 8 < nv && (!kWindow || gr + 8 >= klo);
+    // the running max of a head is raised only when a score passes it by more than 8 (log2
+    // units), so P = exp2(s - m) <= 2^8 and most pages leave the accumulators as they are;
+    // whether any score does is voted on first, and only then are the column maxima taken
+    bool raise = false;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int tok = n * 8 + tc + (i & 1);
-            s[n][i] = (tok < nv && (!kWindow || tok >= klo)) ? s[n][i] * a.scale_log2 : -INFINITY;
-        }
-    const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
-    const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
-    // the running max is raised only when a score passes it by more than 8 (log2 units), so
-    // P = exp2(s - m) <= 2^8 and most pages leave the accumulators as they are
-    if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
-        const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
-        const float al0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mn0);
-        const float al1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int n = 0; n < kN; ++n) {
-            acc[n][0] *= al0;
-            acc[n][1] *= al0;
-            acc[n][2] *= al1;
-            acc[n][3] *= al1;
-        }
-        l0 *= al0;
-        l1 *= al1;
+    for (int nt = 0; nt < NH; ++nt) {
+        s[nt][0] = ok0 ? s[nt][0] * a.scale_log2 : -INFINITY;
+        s[nt][1] = ok0 ? s[nt][1] * a.scale_log2 : -INFINITY;
+        s[nt][2] = ok1 ? s[nt][2] * a.scale_log2 : -INFINITY;
+        s[nt][3] = ok1 ? s[nt][3] * a.scale_log2 : -INFINITY;
+        raise |= fmaxf(s[nt][0], s[nt][2]) > mr[nt][0] + 8.f || fmaxf(s[nt][1], s[nt][3]) > mr[nt][1] + 8.f;
     }
-    const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
-    float p[2][4];
+    if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
-        p[n][0] = fast_exp2(s[n][0] - base0);
-        p[n][1] = fast_exp2(s[n][1] - base0);
-        p[n][2] = fast_exp2(s[n][2] - base1);
-        p[n][3] = fast_exp2(s[n][3] - base1);
-    }
-    l0 += (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-    l1 += (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-    // P = P_hi + P_lo, both bf16: the rounding of P to bf16 alone (relative 2^-9)
-    // is too coarse for short sequences, the pair keeps ~16 bits
-    uint32_t ph[4], pl[4];
-    {
-        const float pv[4][2] = {{p[0][0], p[0][1]}, {p[0][2], p[0][3]}, {p[1][0], p[1][1]}, {p[1][2], p[1][3]}};
+        for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            ph[e] = pack_bf16x2(pv[e][0], pv[e][1]);
-            pl[e] = pack_bf16x2(pv[e][0] - __uint_as_float(ph[e] << 16), pv[e][1] - __uint_as_float(ph[e] & 0xFFFF0000u));
-        }
+            for (int e = 0; e < 2; ++e) {
+                const float mx = col_max(fmaxf(s[nt][e], s[nt][2 + e]));
+                const float mn = mx > mr[nt][e] + 8.f ? mx : mr[nt][e];
+                const float al = mr[nt][e] == -INFINITY ? 0.f : fast_exp2(mr[nt][e] - mn);
+                mr[nt][e] = mn;
+                ls[nt][e] *= al;
+#pragma unroll
+                for (int mt = 0; mt < kK; ++mt) {
+                    acc[mt][nt][e] *= al;
+                    acc[mt][nt][2 + e] *= al;
+                }
+            }
     }
-    // O += P V: V rows are tokens (the k axis), columns head_dim (n axis)
+    // P^T as B fragments of O^T = V^T P^T, P = P_hi + P_lo, both bf16 (the rounding of P to
+    // bf16 alone, relative 2^-9, is too coarse for short sequences; the pair keeps ~16 bits):
+    // each 8x8 (token, head) block is transposed in registers to (head, token)
+    uint32_t bh[NH][2], bl[NH][2];
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) {
+        const float base0 = mr[nt][0] == -INFINITY ? 0.f : mr[nt][0];
+        const float base1 = mr[nt][1] == -INFINITY ? 0.f : mr[nt][1];
+        const float p0 = fast_exp2(s[nt][0] - base0), p1 = fast_exp2(s[nt][1] - base1);
+        const float p2 = fast_exp2(s[nt][2] - base0), p3 = fast_exp2(s[nt][3] - base1);
+        ls[nt][0] += p0 + p2;
+        ls[nt][1] += p1 + p3;
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
+        const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
+        bh[nt][0] = movmatrix_t(h01);
+        bh[nt][1] = movmatrix_t(h23);
+        bl[nt][0] = movmatrix_t(l01);
+        bl[nt][1] = movmatrix_t(l23);
+    }
+    // O^T += V^T P^T: A fragments of V^T read transposed from the V rows (tokens 0-7 / 8-15 in
+    // matrices 0, 1 / 2, 3; head_dim 16mt..+7 / +8..15)
     const uint32_t vbase = smem_u32(vb);
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-        const int tok = (lm & 1) * 8 + lr, chunk = c * 2 + (lm >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), b0, b1, b2, b3);
-        mma_16816(acc[2 * c], ph[0], ph[1], ph[2], ph[3], b0, b1);
-        mma_16816(acc[2 * c + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-        mma_16816(acc[2 * c], pl[0], pl[1], pl[2], pl[3], b0, b1);
-        mma_16816(acc[2 * c + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+    for (int mt = 0; mt < kK; ++mt) {
+        const int tok = (lm >> 1) * 8 + lr, chunk = mt * 2 + (lm & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128(tok, chunk & 7), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) mma_16816(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) mma_16816(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
     }
+}
+
+// Hands each lane two adjacent head_dim columns of one head: the lanes of gr and gr ^ 1
+// (lane ^ 4) swap their values of the other's head, so the even one holds head 8nt + tc,
+// the odd one head 8nt + tc + 1, at columns 16mt + 8 half + (gr & ~1), +1.  Every lane
+// calls it (warp shuffles); e = gr & 1 is the head the lane keeps.
+template <int D, int NH>
+__device__ __forceinline__ float2 head_pair(const float (&acc)[D / 16][NH][4], int mt, int nt, int half, int lane) {
+    const bool odd = (lane >> 2) & 1;
+    const float c0 = acc[mt][nt][2 * half], c1 = acc[mt][nt][2 * half + 1];
+    const float got = __shfl_xor_sync(0xffffffffu, odd ? c0 : c1, 4);
+    return odd ? make_float2(got, c1) : make_float2(c0, got);
 }
 
 // The final out / lse rows of (b, g) from a state that covers every visible key: the sink
-// joins the max and the denominator.  L0 / L1 are the row sums (quad-reduced).
-template <int D>
-__device__ __forceinline__ void finish_rows(const DecodeArgs &a, int b, int g, const float (&acc)[D / 8][4],
-                                            float m0, float m1, float L0, float L1, int lane) {
-    const int gr = lane >> 2, tc = (lane & 3) * 2;
+// joins the max and the denominator.
+template <int D, int NH>
+__device__ __forceinline__ void finish_rows(const DecodeArgs &a, int b, int g, const float (&acc)[D / 16][NH][4],
+                                            const float (&mr)[NH][2], const float (&ls)[NH][2], int lane) {
+    const int gr = lane >> 2, tc = (lane & 3) * 2, e = gr & 1;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = gr + half * 8;
-        if (r < a.G) {
-            const int h = g * a.G + r;
-            const float m = half ? m1 : m0, l = half ? L1 : L0;
-            const float sk = a.sinks ? a.sinks[h] * kLog2e : -INFINITY;
+    for (int nt = 0; nt < NH; ++nt) {
+        float scl[2], lse2[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int hl = nt * 8 + tc + x;  // head within the group
+            const float l = col_sum(ls[nt][x]), m = mr[nt][x];
+            const float sk = a.sinks && hl < a.G ? a.sinks[g * a.G + hl] * kLog2e : -INFINITY;
             const float M = fmaxf(m, sk);
-            float scl = 0.f, lse2 = -INFINITY;
+            scl[x] = 0.f;
+            lse2[x] = -INFINITY;
             if (M != -INFINITY) {
                 const float wm = m == -INFINITY ? 0.f : exp2f(m - M);
                 const float den = l * wm + (sk == -INFINITY ? 0.f : exp2f(sk - M));
-                scl = wm / den;
-                lse2 = M + log2f(den);
+                scl[x] = wm / den;
+                lse2[x] = M + log2f(den);
             }
-            __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + ((int64_t)b * a.Hq + h) * D;
+        }
+        const int hl = nt * 8 + tc + e;
+        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + ((int64_t)b * a.Hq + g * a.G + hl) * D;
+        const float sc = e ? scl[1] : scl[0];
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n)
-                *reinterpret_cast<uint32_t *>(og + n * 8 + tc) =
-                    pack_bf16x2(acc[n][2 * half] * scl, acc[n][2 * half + 1] * scl);
-            if (a.lse && (lane & 3) == 0) a.lse[(int64_t)b * a.Hq + h] = lse2 * kLn2;
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const float2 v = head_pair<D, NH>(acc, mt, nt, half, lane);
+                if (hl < a.G)
+                    *reinterpret_cast<uint32_t *>(og + mt * 16 + half * 8 + (gr & ~1)) = pack_bf16x2(v.x * sc, v.y * sc);
+            }
+        if (a.lse && gr == 0)
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+                if (nt * 8 + tc + x < a.G) a.lse[(int64_t)b * a.Hq + g * a.G + nt * 8 + tc + x] = lse2[x] * kLn2;
+    }
+}
+
+// The partial state of (sequence, KV head) over part of its pages, unnormalised and without
+// the sink, into rows row0 .. row0 + G - 1 (head_dim values, and (m, l) per row).
+template <int D, int NH>
+__device__ __forceinline__ void write_partial(float *part_acc, float *part_ml, int64_t row0, int G,
+                                              const float (&acc)[D / 16][NH][4], const float (&mr)[NH][2],
+                                              const float (&ls)[NH][2], int lane) {
+    const int gr = lane >> 2, tc = (lane & 3) * 2, e = gr & 1;
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) {
+        const float l0 = col_sum(ls[nt][0]), l1 = col_sum(ls[nt][1]);
+        const int hl = nt * 8 + tc + e;
+        float *pa = part_acc + (row0 + hl) * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const float2 v = head_pair<D, NH>(acc, mt, nt, half, lane);
+                if (hl < G) *reinterpret_cast<float2 *>(pa + mt * 16 + half * 8 + (gr & ~1)) = v;
+            }
+        if (gr == 0) {
+            if (nt * 8 + tc < G) *reinterpret_cast<float2 *>(part_ml + (row0 + nt * 8 + tc) * 2) = make_float2(mr[nt][0], l0);
+            if (nt * 8 + tc + 1 < G)
+                *reinterpret_cast<float2 *>(part_ml + (row0 + nt * 8 + tc + 1) * 2) = make_float2(mr[nt][1], l1);
         }
     }
 }
 
-// kWindow: a sliding window is given (a.window > 0); the kernel without it carries no
-// window arithmetic.  kAppend: the new K/V rows a.k_new / a.v_new are appended (see above).
-// kRope (with kAppend): q and the new key are rotated first (see above).
-template <int D, bool kWindow, bool kAppend = false, bool kRope = false>
+// NH: 8-head tiles of the query group (1 for G <= 8, 2 for G <= 16).  kWindow: a sliding
+// window is given (a.window > 0); the kernel without it carries no window arithmetic.
+// kAppend: the new K/V rows a.k_new / a.v_new are appended (see above).  kRope (with
+// kAppend): q and the new key are rotated first (see above).
+template <int D, int NH, bool kWindow, bool kAppend = false, bool kRope = false>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeArgs a) {
@@ -454,15 +529,13 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         advance(pc);
     }
 
-    // per-lane fragment coordinates
-    const int gr = lane >> 2;        // row (query head) of c0/c1; +8 for c2/c3
-    const int tc = (lane & 3) * 2;   // first column of this lane's pair
-
-    uint32_t qa[C::kKSteps][4];
-    float acc[C::kNTiles][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qb[C::kKSteps][NH][2];
+    float acc[C::kKSteps][NH][4];
+    float mr[NH][2], ls[NH][2];
     int seg_p0 = cur.p;
     bool seg_start = true;
+    uint4 new_row = make_uint4(0, 0, 0, 0);  // with kAppend: the new K/V row of the segment's last page
+    int len_given = -1;                       // ... and its sequence's length as given
 
     for (int u = 0; u < n_units; ++u) {
         const int stage = u % S;
@@ -484,44 +557,40 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             // comes from the inputs, into the stage and into the cache (nv > 0: a valid page;
             // a length beyond the block table, clamped above, has no slot: nothing is written)
             const int L = s_len[cur.b];
+            // a segment that reaches the last visible page (the one holding L - 1) loads the
+            // new row, and the length as given (unclamped), as it starts
+            if (seg_start && u + (cur.pb - 1 - cur.p) < n_units) {
+                new_row = load_new_row<D>(a, cur.b, cur.g, lane);
+                len_given = a.seq_lens[cur.b];
+            }
             const int page = (kWindow ? s_first[cur.b] : 0) + cur.p;
-            if (nv > 0 && page == (L - 1) / kPageSize && a.seq_lens[cur.b] == L)
-                append_row<D, kRope>(a, cur.b, cur.g, L, wpg[stage], kb, vb, lane);
+            if (nv > 0 && page == (L - 1) / kPageSize && len_given == L)
+                append_row<D, kRope>(a, cur.b, cur.g, L, wpg[stage], kb, vb, new_row, lane);
         }
         if (seg_start) {
-            load_q<D, kRope>(a, cur.b, cur.g, s_len[cur.b], qa, lane);
+            load_q<D, NH, kRope>(a, cur.b, cur.g, s_len[cur.b], qb, lane);
 #pragma unroll
-            for (int n = 0; n < C::kNTiles; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
+            for (int mt = 0; mt < C::kKSteps; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                mr[nt][0] = mr[nt][1] = -INFINITY;
+                ls[nt][0] = ls[nt][1] = 0.f;
+            }
             seg_p0 = cur.p;
             seg_start = false;
         }
-        page_step<D, kWindow>(a, kb, vb, nv, klo, qa, acc, m0, m1, l0, l1, lane);
+        page_step<D, NH, kWindow>(a, kb, vb, nv, klo, qb, acc, mr, ls, lane);
 
         const bool seg_end = (cur.p == cur.pb - 1) || (u == n_units - 1);
         if (seg_end) {
-            const float L0 = quad_sum(l0), L1 = quad_sum(l1);
             const bool whole = seg_p0 == 0 && cur.p == cur.pb - 1;
             if (whole) {
-                finish_rows<D>(a, cur.b, cur.g, acc, m0, m1, L0, L1, lane);
+                finish_rows<D, NH>(a, cur.b, cur.g, acc, mr, ls, lane);
             } else {
                 const int64_t slot = (int64_t)wglob + (int64_t)cur.b * a.Hkv + cur.g;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int r = gr + half * 8;
-                    if (r < a.G) {
-                        const int64_t row = slot * a.G + r;
-                        float *pa = a.part_acc + row * D;
-#pragma unroll
-                        for (int n = 0; n < C::kNTiles; ++n)
-                            *reinterpret_cast<float2 *>(pa + n * 8 + tc) =
-                                make_float2(acc[n][2 * half], acc[n][2 * half + 1]);
-                        if ((lane & 3) == 0)
-                            *reinterpret_cast<float2 *>(a.part_ml + row * 2) =
-                                make_float2(half ? m1 : m0, half ? L1 : L0);
-                    }
-                }
+                write_partial<D, NH>(a.part_acc, a.part_ml, slot * a.G, a.G, acc, mr, ls, lane);
             }
             seg_start = true;
         }
@@ -563,7 +632,7 @@ struct WinCfg {
     static_assert(16 * D * 4 <= C::kWarpBytes, "partial state fits the ring");
 };
 
-template <int D, bool kAppend, bool kRope>
+template <int D, int NH, bool kAppend, bool kRope>
 __global__ void __launch_bounds__(kWinWarps * 32)
     decode_window_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          const __grid_constant__ DecodeArgs a) {
@@ -588,7 +657,6 @@ __global__ void __launch_bounds__(kWinWarps * 32)
     fence_mbar_init();
     __syncthreads();
 
-    const int gr = lane >> 2, tc = (lane & 3) * 2;
     const uint64_t policy = l2_policy_evict_first();
     const int cap = a.max_pages * kPageSize;
     const int items = a.B * a.Hkv;
@@ -639,12 +707,19 @@ __global__ void __launch_bounds__(kWinWarps * 32)
         };
         for (int j = 0; j < min(S, n); ++j) produce(j);
 
-        uint32_t qa[C::kKSteps][4];
-        float acc[C::kNTiles][4];
+        uint32_t qb[C::kKSteps][NH][2];
+        float acc[C::kKSteps][NH][4];
+        float mr[NH][2], ls[NH][2];
 #pragma unroll
-        for (int c = 0; c < C::kNTiles; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        if (n > 0) load_q<D, kRope>(a, b, g, L, qa, lane);
+        for (int nt = 0; nt < NH; ++nt) {
+#pragma unroll
+            for (int mt = 0; mt < C::kKSteps; ++mt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+            mr[nt][0] = mr[nt][1] = -INFINITY;
+            ls[nt][0] = ls[nt][1] = 0.f;
+        }
+        if (n > 0) load_q<D, NH, kRope>(a, b, g, L, qb, lane);
+        // the warp with the last visible page (the one holding L - 1) loads the new row now
+        const uint4 new_row = kAppend && n > 0 && p0 + n == npg ? load_new_row<D>(a, b, g, lane) : make_uint4(0, 0, 0, 0);
         for (int j = 0; j < n; ++j) {
             const int stage = (int)((uc + j) % S);
             if (!__all_sync(0xffffffffu,
@@ -655,7 +730,8 @@ __global__ void __launch_bounds__(kWinWarps * 32)
                 for (int v = j; v < min(n, j + S); ++v)
                     mbar_wait(&wbar[(uc + v) % S], (uint32_t)(((uc + v) / S) & 1), kDrainLimitNs);
                 dead = true;
-                m0 = m1 = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) mr[nt][0] = mr[nt][1] = -INFINITY;
                 break;
             }
             uint8_t *kb = wbuf + stage * C::kStageBytes;
@@ -666,9 +742,9 @@ __global__ void __launch_bounds__(kWinWarps * 32)
                 // the page holding the sequence's new token (position L - 1): that row comes
                 // from the inputs (a length beyond the table, clamped above, has no slot)
                 if (nv > 0 && first + p0 + j == (L - 1) / kPageSize && a.seq_lens[b] == L)
-                    append_row<D, kRope>(a, b, g, L, wpg[stage], kb, vb, lane);
+                    append_row<D, kRope>(a, b, g, L, wpg[stage], kb, vb, new_row, lane);
             }
-            page_step<D, true>(a, kb, vb, nv, wlo[stage], qa, acc, m0, m1, l0, l1, lane);
+            page_step<D, NH, true>(a, kb, vb, nv, wlo[stage], qb, acc, mr, ls, lane);
             // every lane's reads and V-row clears of this stage are ordered before the TMA
             // that lane 0 issues into it next
             fence_proxy_async_smem();
@@ -676,21 +752,8 @@ __global__ void __launch_bounds__(kWinWarps * 32)
             if (j + S < n) produce(j + S);
         }
         if (!dead) uc += n;
-        // this warp's partial state (sink-free) into shared memory
-        const float L0 = quad_sum(l0), L1 = quad_sum(l1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int r = gr + half * 8;
-            if (r < a.G) {
-                float *pa = reinterpret_cast<float *>(wbuf) + r * D;
-#pragma unroll
-                for (int c = 0; c < C::kNTiles; ++c)
-                    *reinterpret_cast<float2 *>(pa + c * 8 + tc) = make_float2(acc[c][2 * half], acc[c][2 * half + 1]);
-                if ((lane & 3) == 0)
-                    *reinterpret_cast<float2 *>(s_ml + (wid * 16 + r) * 2) =
-                        make_float2(half ? m1 : m0, half ? L1 : L0);
-            }
-        }
+        // this warp's partial state (sink-free) into shared memory: [16][D] fp32 in its ring
+        write_partial<D, NH>(reinterpret_cast<float *>(wbuf), s_ml + wid * 16 * 2, 0, a.G, acc, mr, ls, lane);
         __syncthreads();
         // merge the four partial states and fold in the sink
         constexpr int kQuads = D / 4;
@@ -807,12 +870,18 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     int sms = 0, occ = 1 << 30;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    const void *kernels[6] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, false>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, false, true>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true, true>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, false, true, true>),
-                              reinterpret_cast<const void *>(decode_splitkv_kernel<D, true, true, true>)};
+    const void *kernels[12] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, true, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false, true, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, true, true, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, false>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, false, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, true, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, false, true, true>),
+                               reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, true, true, true>)};
     for (const void *k : kernels) {
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, k);
@@ -874,6 +943,9 @@ namespace {
 template <int D, bool kWindow, bool kAppend = false, bool kRope = false>
 cudaError_t launch_splitkv_d(const DecodeArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap, int ctas,
                              int smem_bytes, cudaStream_t stream) {
+    // one tile of 8 heads for G <= 8, two for G <= 16
+    auto kern = a.G > 8 ? decode_splitkv_kernel<D, 2, kWindow, kAppend, kRope>
+                        : decode_splitkv_kernel<D, 1, kWindow, kAppend, kRope>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(DecodeCfg<D>::kThreads);
@@ -884,7 +956,7 @@ cudaError_t launch_splitkv_d(const DecodeArgs &a, const CUtensorMap &kmap, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.start_early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, kWindow, kAppend, kRope>, kmap, vmap, a);
+    return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 }  // namespace
 
@@ -914,11 +986,11 @@ cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap 
 }
 
 namespace {
-template <int D, bool kAppend, bool kRope>
-cudaError_t launch_window_d(const DecodeArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                            cudaStream_t stream) {
+template <int D, int NH, bool kAppend, bool kRope>
+cudaError_t launch_window_nh(const DecodeArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             cudaStream_t stream) {
     constexpr int bytes = WinCfg<D>::kSmemBytes;
-    auto kern = decode_window_kernel<D, kAppend, kRope>;
+    auto kern = decode_window_kernel<D, NH, kAppend, kRope>;
     // occupancy per (device, variant), asked once
     static int occ_of[64] = {};
     int device = 0, sms = 0;
@@ -942,6 +1014,12 @@ cudaError_t launch_window_d(const DecodeArgs &a, const CUtensorMap &kmap, const 
     if (grid == 0) return cudaSuccess;
     kern<<<grid, kWinWarps * 32, bytes, stream>>>(kmap, vmap, a);
     return cudaGetLastError();
+}
+template <int D, bool kAppend, bool kRope>
+cudaError_t launch_window_d(const DecodeArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                            cudaStream_t stream) {
+    return a.G > 8 ? launch_window_nh<D, 2, kAppend, kRope>(a, kmap, vmap, stream)
+                   : launch_window_nh<D, 1, kAppend, kRope>(a, kmap, vmap, stream);
 }
 }  // namespace
 

@@ -14,13 +14,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMinUnitsPerWarp = 4;  // pages per warp at least (keeps partials few)
 
-__device__ __forceinline__ float quad_max(float x) {
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-    return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+// Over the 8 lanes that share lane & 3: one column of an m16n8 accumulator (its rows are
+// spread over lane >> 2 and the two register halves).
+__device__ __forceinline__ float col_max(float x) {
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+    return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
 }
-__device__ __forceinline__ float quad_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+__device__ __forceinline__ float col_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    return x + __shfl_xor_sync(0xffffffffu, x, 16);
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held in MMA fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 // Lengths (validated, clamped), the first page each sequence's query sees (0, or the

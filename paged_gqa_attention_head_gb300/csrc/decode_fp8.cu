@@ -97,23 +97,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Transpose of an 8x8 matrix of 16-bit elements held in MMA fragment layout.
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-__device__ __forceinline__ float col_max(float x) {  // over the 8 lanes sharing lane & 3
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
-    return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
-}
-__device__ __forceinline__ float col_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    return x + __shfl_xor_sync(0xffffffffu, x, 16);
-}
 
 // NH: 8-head tiles of the query group (1 for G <= 8, 2 for G = 16).
 template <int D, int NH, bool kWindow>

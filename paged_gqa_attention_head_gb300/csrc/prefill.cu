@@ -1122,14 +1122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (C::kSplitP && i >= (uint32_t)NBP) {
-                    // the P buffer is free once the P.V of product i - NBP has completed
-                    if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status, a.wait_limit_cycles)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                }
+                // the P buffer is free once the P.V of product i - NBP has completed: waited for
+                // in emit, after the first chunk's exponentials
+                bool pwait = C::kSplitP && i >= (uint32_t)NBP, pfail = false;
                 const int4 kq = *reinterpret_cast<const int4 *>(s_vscale + vst * 4);
                 const float2 sc2 = make_float2(sc, sc);
                 // writes P against the running max m_used; returns the row's sum of P * 2^-k
@@ -1156,7 +1151,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[e & 3] = fadd2(acc[e & 3], make_float2(p0, p1));
                             pp[e] = pack_f16x2(p0, p1);
                         }
-                        tc::st_32x32b_x16(tp + ch * 16, pp);
+                        if (ch == 0 && pwait) {
+                            pwait = false;
+                            if (!wait_or_abort(&bars.pv_done[pb], ((i - NBP) / NBP) & 1, s_abort, a.status,
+                                               a.wait_limit_cycles))
+                                pfail = true;
+                            tc::fence_after_sync();
+                        }
+                        if (!pfail) tc::st_32x32b_x16(tp + ch * 16, pp);
                         tl += (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
                                ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) *
                               (f8 ? mul8 : __uint_as_float((uint32_t)(127 - kc) << 23));
@@ -1164,6 +1166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return tl;
                 };
                 float tl = emit();
+                if (pfail) {
+                    ok = false;
+                    break;
+                }
                 if (j > 0) {
                     // every P * 2^-k at most 2^8 (so P fits fp16) unless the row's sum passes it
                     const bool need = !(tl <= kPSumLimit) || m_used == -INFINITY;
