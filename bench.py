@@ -751,7 +751,7 @@ def mixed_row(torch, sa, dev, stream, pk, d, w, dws, dout, dlse, pargs, pkw, pou
     # (programmatic dependent launch); the decode's split-KV grid takes the other SMs
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     split = {}
-    for S in (80, 84, 88, 92, 96):
+    for S in (80, 84, 86, 88, 90, 92, 96):
         def one(S=S):
             sa.prefill(*pargs, **pkw, out=pout, lse=plse, workspace_buf=pws, max_sms=S,
                        flags=sa.FLAG_LAUNCH_NEXT_EARLY)
