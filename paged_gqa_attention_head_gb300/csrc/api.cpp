@@ -18,6 +18,8 @@ using namespace sinkattn;
 namespace {
 
 constexpr size_t kAlign = 256;
+// Page copies the bf16 split-KV grid keeps in flight at most (its CTAs' copy rings).
+constexpr size_t kDecodeInflightBytes = size_t(18) << 20;
 
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
@@ -136,21 +138,23 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
     int device = 0;
     int rc = cuda_rc(cudaGetDevice(&device), "cudaGetDevice");
     if (rc) return rc;
-    rc = cuda_rc(decode_launch_shape(d->head_dim, d->num_seqs, device, &L->ctas, &L->warps_per_cta,
-                                     &L->smem),
+    const int G = d->num_qo_heads / d->num_kv_heads;
+    int ring = 0;  // bytes of page copies one bf16 split-KV CTA keeps in flight
+    rc = cuda_rc(decode_launch_shape(d->head_dim, d->num_seqs, G, device, &L->ctas, &L->warps_per_cta,
+                                     &L->smem, &ring),
                  "decode launch shape");
     if (rc) return rc;
-    const int G = d->num_qo_heads / d->num_kv_heads;
     rc = cuda_rc(decode_fp8_launch_shape(d->head_dim, G, d->num_seqs, device, &L->ctas8,
                                          &L->warps_per_cta8, &L->smem8),
                  "fp8 decode launch shape");
     if (rc) return rc;
     // Both grids are (SMs x CTAs per SM); keep the CTAs per SM, on fewer SMs' worth of CTAs
-    // where max_sms asks for it.  The bf16 split-KV grid also stops at about two thirds of the
-    // SMs' worth: with every SM at full occupancy its rings hold ~29 MB of page reads in
-    // flight, and HBM delivered 5-6 % less than with ~18 MB (measured on GB300 for the
-    // long-context, Qwen3-shape and gpt-oss decode batches: best at 92 of 152 SMs' worth at
-    // head_dim 64, 96 at head_dim 128; the block scheduler still spreads the CTAs over every SM).
+    // where max_sms asks for it.  The bf16 split-KV grid also stops at kDecodeInflightBytes of
+    // page copies in flight: with every SM at full occupancy its rings hold 25-29 MB, and HBM
+    // delivered 2-5 % less than with ~18 MB (measured on GB300 for the long-context, Qwen3-shape
+    // and gpt-oss decode batches: best at 104-120 SMs' worth of five 32 KB CTAs at head_dim 64,
+    // 96 SMs' worth of three 64 KB CTAs at 128; the block scheduler still spreads the CTAs over
+    // every SM).
     int sms = 0;
     rc = cuda_rc(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device),
                  "cudaDeviceGetAttribute");
@@ -159,10 +163,10 @@ int decode_layout(const sinkattn_paged_desc *d, DecodeLayout *L) {
         const int per_sm = L->ctas / sms, per_sm8 = L->ctas8 / sms;
         int use = sms, use8 = sms;
         if (d->max_sms > 0 && d->max_sms < sms) use = use8 = d->max_sms;
-        const int keep = (sms * (d->head_dim == 64 ? 92 : 96) + 151) / 152;
-        if (use > keep) use = keep;
         L->ctas = per_sm * use;
         L->ctas8 = per_sm8 * use8;
+        const int most = ring > 0 ? (int)(kDecodeInflightBytes / ring) : L->ctas;
+        if (L->ctas > most) L->ctas = most;
     }
     L->total_warps = L->ctas * L->warps_per_cta;
     L->total_warps8 = L->ctas8 * L->warps_per_cta8;

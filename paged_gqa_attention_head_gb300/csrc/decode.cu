@@ -54,12 +54,14 @@ template <int D>
 struct DecodeCfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = kWarps * 32;
-    // Ring depth per warp.  An SM keeps ~192 KB of pages in flight either way; shallow
-    // rings let more warps share it (D=64: 3 x 4 KB per warp, four 4-warp CTAs per SM;
-    // D=128: 2 x 8 KB, three CTAs, bounded by registers), and the per-warp work on a page
-    // (ldmatrix, MMAs, softmax), not HBM, is what more warps hide: measured 6 -> 3 stages
-    // at D=64 raised a 256-sequence long-context batch from 6.04 to 6.57 TB/s.
-    static constexpr int kStages = D == 64 ? 3 : 2;
+    // Ring depth per warp.  Shallow rings let more warps share an SM's shared memory, and
+    // the per-warp work on a page (ldmatrix, MMAs, softmax), not HBM, is what more warps
+    // hide: measured at D=64, 6 -> 3 stages (8 -> 16 warps an SM) raised a 256-sequence
+    // long-context batch from 6.04 to 6.57 TB/s, and 3 -> 2 stages (16 -> 20 warps, with the
+    // transposed MMAs' lower register count) from 6.98 to 7.21 TB/s.  D=64: 2 x 4 KB per
+    // warp, five 4-warp CTAs per SM for groups of up to 8 heads (four for 16, by registers);
+    // D=128: 2 x 8 KB, three CTAs.
+    static constexpr int kStages = 2;
     static constexpr int kHalves = D / 64;               // 128-byte column blocks per row
     static constexpr int kPageBytes = kPageSize * D * 2;  // one (page, head) of K or of V
     static constexpr int kStageBytes = 2 * kPageBytes;
@@ -854,7 +856,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
 }
 
 template <int D>
-cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
+cudaError_t shape_for(int B, int G, int device, int *ctas, int *warps, int *smem, int *ring) {
     using C = DecodeCfg<D>;
     const int bytes = decode_smem_bytes<D>(B);
     // The kernel's dynamic shared-memory ceiling is one setting per kernel, shared
@@ -863,14 +865,13 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    // every variant (with and without a window, with and without append and rotation) gets
-    // the same grid:
-    // the split plan and the
-    // workspace layout depend on it
+    // every variant of one group size (with and without a window, with and without append
+    // and rotation) gets the same grid: the split plan and the workspace layout depend on it;
+    // groups of up to 8 heads (one 8-head tile) use fewer registers and may fit more CTAs
     int sms = 0, occ = 1 << 30;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    const void *kernels[12] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false>),
+    const void *all[12] = {reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false>),
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, true>),
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, false, true>),
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 1, true, true>),
@@ -882,7 +883,9 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, true, true>),
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, false, true, true>),
                                reinterpret_cast<const void *>(decode_splitkv_kernel<D, 2, true, true, true>)};
-    for (const void *k : kernels) {
+    const void *const *kernels = all + (G > 8 ? 6 : 0);  // the variants of this group size
+    for (int ki = 0; ki < 6; ++ki) {
+        const void *k = kernels[ki];
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
@@ -899,40 +902,42 @@ cudaError_t shape_for(int B, int device, int *ctas, int *warps, int *smem) {
     *ctas = sms * occ;
     *warps = C::kWarps;
     *smem = bytes;
+    *ring = C::kWarps * C::kWarpBytes;
     return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_per_cta,
-                                int *smem_bytes) {
-    // occupancy queries cost microseconds; remember the answer per (device, D, B)
+cudaError_t decode_launch_shape(int D, int B, int G, int device, int *ctas, int *warps_per_cta,
+                                int *smem_bytes, int *ring_bytes) {
+    // occupancy queries cost microseconds; remember the answer per (device, D, B, head tiles)
     struct Entry {
-        int device, D, B, ctas, warps, smem;
+        int device, D, B, G, ctas, warps, smem, ring;
     };
     static std::mutex mu;
     static std::vector<Entry> cache;
     {
         std::lock_guard<std::mutex> lock(mu);
         for (const Entry &e : cache)
-            if (e.device == device && e.D == D && e.B == B) {
+            if (e.device == device && e.D == D && e.B == B && (e.G > 8) == (G > 8)) {
                 *ctas = e.ctas;
                 *warps_per_cta = e.warps;
                 *smem_bytes = e.smem;
+                *ring_bytes = e.ring;
                 return cudaSuccess;
             }
     }
     cudaError_t e;
     if (D == 64)
-        e = shape_for<64>(B, device, ctas, warps_per_cta, smem_bytes);
+        e = shape_for<64>(B, G, device, ctas, warps_per_cta, smem_bytes, ring_bytes);
     else if (D == 128)
-        e = shape_for<128>(B, device, ctas, warps_per_cta, smem_bytes);
+        e = shape_for<128>(B, G, device, ctas, warps_per_cta, smem_bytes, ring_bytes);
     else
         return cudaErrorInvalidValue;
     if (e == cudaSuccess) {
         std::lock_guard<std::mutex> lock(mu);
         if (cache.size() > 256) cache.clear();
-        cache.push_back({device, D, B, *ctas, *warps_per_cta, *smem_bytes});
+        cache.push_back({device, D, B, G, *ctas, *warps_per_cta, *smem_bytes, *ring_bytes});
     }
     return e;
 }

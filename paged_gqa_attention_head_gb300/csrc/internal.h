@@ -55,8 +55,8 @@ struct DecodeArgs {
 
 // Grid and shared memory of the split-KV decode kernel for head_dim D and
 // batch B on `device`.  Deterministic for a given (device, D, B).
-cudaError_t decode_launch_shape(int D, int B, int device, int *ctas, int *warps_per_cta,
-                                int *smem_bytes);
+cudaError_t decode_launch_shape(int D, int B, int G, int device, int *ctas, int *warps_per_cta,
+                                int *smem_bytes, int *ring_bytes);
 cudaError_t launch_decode_splitkv(int D, const DecodeArgs &a, const CUtensorMap &kmap,
                                   const CUtensorMap &vmap, int ctas, int smem_bytes,
                                   cudaStream_t stream);

@@ -155,11 +155,12 @@ def test_prefill_then_decode_started_early_on_one_stream(sa, cuda_dev, split):
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_decode_grid_stops_at_its_cap(sa, cuda_dev, D):
-    """The split-KV grid stops at 104 (head_dim 64) or 96 (128) of 152 SMs' worth of CTAs,
-    scaled to the device: a cap at or above that gives the same grid and bits as none."""
+    """The split-KV grid stops at 18 MB of page copies in flight (576 CTAs of 32 KB rings at
+    head_dim 64, 288 of 64 KB at 128; 115 and 96 of GB300's 152 SMs' worth): an SM cap that
+    leaves more CTAs than that gives the same grid and bits as none."""
     dev = cuda_dev
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    keep = (n_sms * (104 if D == 64 else 96) + 151) // 152
+    keep = (n_sms * 130) // 152  # five CTAs an SM at 64 (three at 128): above the budget
     w = inputs.make_decode(("uniform", 100, 6000), 40, 16, 2, D, seed=215 + D, sinks=True)
     c = w.cache
     args = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
