@@ -98,9 +98,11 @@ typedef struct sinkattn_paged_desc {
                                 * sums may round differently than with all SMs; prefill
                                 * results do not depend on it.  The decode workspace size
                                 * query takes it into account (a smaller grid needs fewer
-                                * partial-state slots).  With 0, or a value above it, the
-                                * split-KV decode's grid still stops at about two thirds of
-                                * the SMs' worth of CTAs, where HBM measured fastest. */
+                                * partial-state slots).  With 0, or a large value, the
+                                * split-KV decode's grid still stops where its CTAs' copy
+                                * rings hold about 18 MB of page reads in flight (about
+                                * three quarters of GB300's SMs' worth of CTAs), where HBM
+                                * measured fastest. */
     int32_t wait_limit_us;     /* watchdog of the kernels' pipeline waits (decode, FP8
                                 * decode, prefill), in microseconds: a wait that has not
                                 * completed after this long gives up, the kernel sets
