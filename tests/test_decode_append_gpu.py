@@ -49,6 +49,9 @@ CASES = [
     ([1, 16, 17, 64, 129, 0, 300, 2049], 32, 2, 128, 0),
     ([5, 15, 32, 33, 700, 1000, 128, 129], 16, 4, 64, 128),
     ([2, 31, 48, 4000], 4, 4, 128, 100),
+    # two 8-head tiles at head_dim 64: split-KV, and the one-launch window kernel
+    ([1, 16, 17, 129, 0, 300, 2049], 32, 2, 64, 0),
+    ([5, 15, 33, 700, 129, 0], 32, 2, 64, 128),
 ]
 
 

@@ -62,7 +62,7 @@ def _run(sa, oracle_mod, dev, w, rope, window=0, sample=None):
         assert np.all(np.abs(got - exact[b]) <= step + 1e-30), f"rotated key of sequence {b}"
 
 
-@pytest.mark.parametrize("D,G", [(64, 8), (64, 1), (128, 16), (128, 4)])
+@pytest.mark.parametrize("D,G", [(64, 8), (64, 1), (128, 16), (128, 4), (64, 16)])
 @pytest.mark.parametrize("rope", ["gptoss", "plain"])
 def test_rope_decode_shapes(sa, oracle_mod, cuda_dev, D, G, rope):
     Hkv = 2 if G < 16 else 4
@@ -78,8 +78,10 @@ def test_rope_decode_long_positions(sa, oracle_mod, cuda_dev):
     _run(sa, oracle_mod, cuda_dev, w, GPTOSS, sample=1)
 
 
-def test_rope_decode_window(sa, oracle_mod, cuda_dev):
-    w = inputs.make_decode([5, 128, 129, 3000], 4, 16, 2, 64, seed=45, sinks=True)
+@pytest.mark.parametrize("G", [8, 16])
+def test_rope_decode_window(sa, oracle_mod, cuda_dev, G):
+    # the one-launch window kernel, one and two 8-head tiles
+    w = inputs.make_decode([5, 128, 129, 3000], 4, 2 * G, 2, 64, seed=45 + G, sinks=True)
     _run(sa, oracle_mod, cuda_dev, w, GPTOSS, window=128)
 
 

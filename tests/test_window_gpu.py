@@ -134,12 +134,13 @@ def test_gptoss_prefill_window_128_full_config_sampled(sa, oracle_mod, cuda_dev)
 # ---- the one-launch plan of short sliding windows (W <= 2032: a CTA per (sequence, KV head),
 # its four warps splitting the visible pages, merged in shared memory) against the two-stage
 # split-KV plan (sinkattn_decode_splitkv + sinkattn_decode_merge) and the oracle
-@pytest.mark.parametrize("D,window", [(64, 16), (64, 128), (128, 128), (64, 2032), (128, 1000)])
-def test_window_one_launch_matches_split_kv_plan(sa, oracle_mod, cuda_dev, D, window):
+# (one 8-head tile for G <= 8, two for 16)
+@pytest.mark.parametrize("D,window,G", [(64, 16, 8), (64, 128, 8), (128, 128, 16), (64, 2032, 8), (128, 1000, 16),
+                                        (64, 128, 16), (128, 128, 1)])
+def test_window_one_launch_matches_split_kv_plan(sa, oracle_mod, cuda_dev, D, window, G):
     lens = [0, 1, 15, 16, 17, 127, 128, 129, 2049, 5000]
     Hkv = 2
-    w = inputs.make_decode(lens, len(lens), Hkv * (8 if D == 64 else 16), Hkv, D, seed=90 + window,
-                           sinks=True)
+    w = inputs.make_decode(lens, len(lens), Hkv * G, Hkv, D, seed=90 + window + G, sinks=True)
     c = w.cache
     dev = cuda_dev
     q, kp, vp, bt, sl, sk = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev),
