@@ -179,12 +179,12 @@ def test_decode_grid_stops_at_its_cap(sa, cuda_dev, D):
 
 @pytest.mark.slow
 def test_long_context_step_with_early_start_matches_the_calls_alone(sa, cuda_dev):
-    """The long-context mixed step in the launch configuration the benchmark times (chunked
-    prefill on 76 SMs starting the decode early, the decode on the others): bit for bit the
-    results of the two calls made alone with the same SM caps."""
+    """The long-context mixed step in the launch configuration the benchmark picks on GB300
+    (chunked prefill on 88 of 152 SMs starting the decode early, the decode on the others): bit
+    for bit the results of the two calls made alone with the same SM caps."""
     dev = cuda_dev
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    S = min(76, n_sms // 2)
+    S = (n_sms * 88) // 152
     w = inputs.make_workload("longctx_decode", seed=0)
     c = w.cache
     dargs = (w.q.to(dev), c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev), c.lens.to(dev),
